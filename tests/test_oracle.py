@@ -1,0 +1,354 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test names what it pins and where the fact comes from: numpy's independent binary16
+conversion, exact rational or integer arithmetic, closed forms and invariants of the method, and
+the worked example printed on the source pages.  A plausible slip in the oracle (a dropped term,
+a wrong sign or index, a transposed operand, the wrong rounding) fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from weight_quantized_linear_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------------------------------------
+# binary16 conversion: pinned against numpy's own float16 implementation
+# ------------------------------------------------------------------------------------------------
+
+def test_half_to_float_all_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_to_float(bits)
+    ref = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_float_to_half_matches_numpy_including_ties_and_subnormals():
+    rng = np.random.default_rng(1)
+    vals = [rng.standard_normal(200000).astype(np.float32) * s for s in (1e-6, 1e-3, 1.0, 100.0, 3e4)]
+    # exact midpoints between adjacent fp16 values (ties), normal and subnormal, both signs
+    h = np.arange(0, 0x7bff, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    special = np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e9, -1e9, np.inf, -np.inf, 2.0 ** -25,
+                        2.0 ** -24, 1.5 * 2.0 ** -24, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -26], np.float32)
+    x = np.concatenate(vals + [mid, -mid, special])
+    ours = oracle.float_to_half(x).view(np.uint16)
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------------------------------------------
+# AWQ int4 quantisation and packing
+# ------------------------------------------------------------------------------------------------
+
+def _exact_grid_weight(K, N, G, seed=3):
+    """Weights that are exactly (c - z) * 2^-6 with codes c covering 0 and 15 in every group."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(K, N))
+    for g in range(K // G):
+        codes[g * G, :] = 0
+        codes[g * G + 1, :] = 15
+    zs = rng.integers(1, 15, size=(K // G, N))
+    z_full = np.repeat(zs, G, axis=0)
+    W = ((codes - z_full) * 2.0 ** -6).astype(np.float32)
+    return W, codes, zs
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_awq_recovers_exactly_representable_weights(G):
+    # Closed form: if every group holds (c - z) * s for an fp16 scale s with both code 0 and code 15
+    # present, min/max quantisation returns exactly s, z and c, and dequantisation is exact.
+    K, N = 2 * G, 40
+    W, codes, zs = _exact_grid_weight(K, N, G)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    q, z = oracle.awq_unpack(qw, qz, K, N, G)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(z, zs)
+    assert np.all(s.astype(np.float32) == np.float32(2.0 ** -6))
+    assert np.array_equal(oracle.awq_dequant(qw, s, qz, K, N, G), W)
+
+
+def test_awq_nibble_layout_is_column_n_at_bits_4_n_mod_8():
+    # Layout pin by construction: a single nonzero code per word at a known column.
+    G, K, N = 32, 32, 32
+    W, codes, zs = _exact_grid_weight(K, N, G, seed=11)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    for k in range(K):
+        for n in range(N):
+            assert (int(qw[k, n // 8]) >> (4 * (n % 8))) & 15 == codes[k, n]
+    for n in range(N):
+        assert (int(qz[0, n // 8]) >> (4 * (n % 8))) & 15 == zs[0, n]
+
+
+def test_awq_unpack_roundtrip_exhaustive_over_positions_and_values():
+    # Every value 0..15 at every nibble position of a word survives pack -> unpack.
+    G, K, N = 32, 32, 128
+    codes = np.zeros((K, N), np.int64)
+    for n in range(N):
+        codes[:, n] = (np.arange(K) + n) % 16
+    codes[0, :] = 0
+    codes[1, :] = 15
+    z = 7
+    W = ((codes - z) * 2.0 ** -5).astype(np.float32)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    q, zz = oracle.awq_unpack(qw, qz, K, N, G)
+    assert np.array_equal(q, codes)
+    assert np.all(zz == z)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_awq_error_bound_and_code_range(G):
+    # For groups whose range contains zero: |w - (q - z) s| <= s/2 + 15 |s16 - s32| (+ fp32 slack),
+    # the group minimum maps to code 0 and the maximum to code 14 or 15.
+    K, N = 512, 256
+    W = inputs.weight(K, N, seed=5, outliers=True)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    q, z = oracle.awq_unpack(qw, qz, K, N, G)
+    deq = oracle.awq_dequant(qw, s, qz, K, N, G).astype(np.float64)
+    Wg = W.reshape(K // G, G, N).astype(np.float64)
+    mn, mx = Wg.min(axis=1), Wg.max(axis=1)
+    s16 = s.astype(np.float64)
+    s_exact = (mx - mn) / 15.0
+    bound = s16 / 2 + 15 * np.abs(s16 - s_exact) + 1e-7 * np.abs(Wg).max(axis=1)
+    err = np.abs(deq.reshape(K // G, G, N) - Wg).max(axis=1)
+    straddle = (mn <= 0) & (mx >= 0)
+    assert straddle.mean() > 0.99
+    assert np.all(err[straddle] <= bound[straddle])
+    qg = q.reshape(K // G, G, N).astype(np.int64)
+    assert np.all(qg.min(axis=1)[straddle] == 0)
+    assert np.all(np.isin(qg.max(axis=1)[straddle], [14, 15]))
+    # the scale spreads the range over 15 steps, up to one fp16 rounding
+    assert np.all(np.abs(s16 * 15 - (mx - mn)) <= (mx - mn) * 2.0 ** -10 + 1e-12)
+
+
+def test_awq_degenerate_group_gets_scale_one():
+    G, K, N = 32, 64, 32
+    W = np.zeros((K, N), np.float32)
+    W[G:, :] = np.random.default_rng(0).normal(0, 0.02, (K - G, N)).astype(np.float32)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    assert np.all(s[0].astype(np.float32) == 1.0)
+    assert np.all(oracle.awq_dequant(qw, s, qz, K, N, G)[:G] == 0.0)
+
+
+def test_w4a16_linear_matches_exact_rational_brute_force():
+    # Brute force with exact rationals (fp16 / fp32 values are dyadic) on a tiny shape.
+    M, K, N, G = 2, 64, 16, 32
+    W = inputs.weight(K, N, seed=7, outliers=True)
+    X = inputs.activations(M, K, seed=7)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    q, z = oracle.awq_unpack(qw, qz, K, N, G)
+    Y = oracle.w4a16_linear(X, qw, s, qz, G)
+    Xf = X.astype(np.float64)
+    sf = s.astype(np.float64)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(float(Xf[m, k])) * (int(q[k, n]) - int(z[k // G, n])) * Fraction(float(sf[k // G, n]))
+            exact = float(acc)
+            assert abs(Y[m, n] - exact) <= 1e-13 * max(1.0, abs(exact))
+
+
+def test_w4a16_linear_one_hot_rows_and_special_cases():
+    M, K, N, G = 5, 128, 64, 64
+    W = inputs.weight(K, N, seed=9, outliers=True)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    deq = oracle.awq_dequant(qw, s, qz, K, N, G)
+    # one-hot activations select one row of the dequantised weight (pins the k index and layout)
+    X = np.zeros((M, K), np.float16)
+    ks = [0, 1, 63, 64, 127]
+    for m, k in enumerate(ks):
+        X[m, k] = 1.0
+    Y = oracle.w4a16_linear(X, qw, s, qz, G)
+    for m, k in enumerate(ks):
+        assert np.array_equal(Y[m], deq[k].astype(np.float64))
+    # zero activations give zero output
+    assert np.all(oracle.w4a16_linear(np.zeros((2, K), np.float16), qw, s, qz, G) == 0.0)
+    # rows selection returns the same rows as the full product
+    Xr = inputs.activations(6, K, seed=2)
+    full = oracle.w4a16_linear(Xr, qw, s, qz, G)
+    part = oracle.w4a16_linear(Xr, qw, s, qz, G, rows=np.array([4, 1]))
+    assert np.array_equal(part, full[[4, 1]])
+
+
+def test_w4a16_linear_single_group_equals_numpy_float64_product():
+    # G == K: one group; compare with numpy's float64 matmul of the dequantised weight.
+    M, K, N, G = 3, 128, 32, 128
+    W = inputs.weight(K, N, seed=4)
+    X = inputs.activations(M, K, seed=4)
+    qw, s, qz = oracle.awq_quantize(W, G)
+    deq = oracle.awq_dequant(qw, s, qz, K, N, G).astype(np.float64)
+    ref = X.astype(np.float64) @ deq
+    assert np.allclose(oracle.w4a16_linear(X, qw, s, qz, G), ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------------
+# QRMSNorm + per-token int8
+# ------------------------------------------------------------------------------------------------
+
+def _rmsnorm64(X, g, eps):
+    Xf = X.astype(np.float64)
+    r = 1.0 / np.sqrt((Xf * Xf).mean(axis=1, keepdims=True) + eps)
+    return Xf * r * g.astype(np.float64)[None, :]
+
+
+def test_sumsq_close_to_exact_sum():
+    X = inputs.activations(4, 4096, seed=1, outlier_channels=True)
+    for row in X:
+        exact = math.fsum(float(v) * float(v) for v in row.astype(np.float64))
+        assert abs(oracle.sumsq(row) - exact) <= 1e-6 * exact
+
+
+def test_qrmsnorm_against_float64_definition():
+    # Independent fp64 evaluation of RMSNorm + absmax/127 + round-half-even: codes may differ only
+    # where the fp64 quotient sits within 1e-4 of a .5 boundary; scales agree to fp32 precision.
+    M, K = 16, 4096
+    X = inputs.activations(M, K, seed=2, outlier_channels=True)
+    g = inputs.gamma(K, seed=2)
+    q, xs = oracle.qrmsnorm_quant_i8(X, g, inputs.EPS)
+    y64 = _rmsnorm64(X, g, inputs.EPS)
+    xs64 = np.abs(y64).max(axis=1) / 127.0
+    assert np.allclose(xs, xs64, rtol=1e-5)
+    t = y64 / xs64[:, None]
+    q64 = np.clip(np.rint(t), -128, 127)
+    near_tie = np.abs(np.abs(t - np.floor(t)) - 0.5) < 1e-4
+    assert np.all((q == q64) | near_tie)
+    assert (q != q64).mean() < 1e-3
+    # the row maximum lands on +-127 and the dequantisation error is at most half a step
+    assert np.all(np.abs(q.astype(np.int64)).max(axis=1) == 127)
+    y32 = oracle.rmsnorm(X, g, inputs.EPS).astype(np.float64)
+    assert np.all(np.abs(q * xs[:, None].astype(np.float64) - y32) <= xs[:, None] * (0.5 + 1e-5))
+
+
+def test_qrmsnorm_closed_forms():
+    K = 512
+    g1 = np.ones(K, np.float16)
+    # constant row: every code is +-127 (or 0 for a zero row, whose scale is 1)
+    X = np.stack([np.full(K, 0.75, np.float16), np.full(K, -3.0, np.float16), np.zeros(K, np.float16)])
+    q, xs = oracle.qrmsnorm_quant_i8(X, g1, 1e-6)
+    assert np.all(q[0] == 127) and np.all(q[1] == -127) and np.all(q[2] == 0)
+    assert xs[2] == 1.0
+    # with eps = 0, scaling a row by a power of two leaves every code unchanged
+    Xr = inputs.activations(3, K, seed=8, outlier_channels=True)
+    g = inputs.gamma(K, seed=8)
+    qa, xa = oracle.qrmsnorm_quant_i8(Xr, g, 0.0)
+    qb, xb = oracle.qrmsnorm_quant_i8((Xr.astype(np.float32) * 0.25).astype(np.float16), g, 0.0)
+    assert np.array_equal(qa, qb) and np.array_equal(xa, xb)
+
+
+def test_act_absmax_matches_float64_rmsnorm():
+    M, K = 32, 1024
+    X = inputs.activations(M, K, seed=3, outlier_channels=True)
+    g = inputs.gamma(K, seed=3)
+    a = oracle.act_absmax(X, g, inputs.EPS)
+    a64 = np.abs(_rmsnorm64(X, g, inputs.EPS)).max(axis=0)
+    assert np.allclose(a, a64, rtol=1e-5)
+
+
+# ------------------------------------------------------------------------------------------------
+# SmoothQuant smoothing and per-channel weight quantisation
+# ------------------------------------------------------------------------------------------------
+
+def test_smoothing_invariance_and_balance():
+    M, K, N = 64, 512, 256
+    X = inputs.activations(M, K, seed=4, outlier_channels=True)
+    g = inputs.gamma(K, seed=4)
+    W = inputs.weight(K, N, seed=4)
+    a = oracle.act_absmax(X, g, inputs.EPS)
+    s, g2, W2 = oracle.smooth(a, g, W)
+    s64 = s.astype(np.float64)
+    # X W = (X diag(s)^-1)(diag(s) W) in exact arithmetic; the oracle's W' is diag(s) W to fp32 rounding
+    assert np.allclose(W2.astype(np.float64), W.astype(np.float64) * s64[:, None], rtol=2 ** -23, atol=0)
+    Xn = _rmsnorm64(X, g, inputs.EPS)
+    lhs = (Xn / s64[None, :]) @ (W.astype(np.float64) * s64[:, None])
+    assert np.allclose(lhs, Xn @ W.astype(np.float64), rtol=1e-12, atol=1e-12)
+    # the stored model (fp16 gamma', fp32 W') reproduces the original layer to fp16 precision
+    Xn2 = _rmsnorm64(X, g2, inputs.EPS)
+    y_new, y_old = Xn2 @ W2.astype(np.float64), Xn @ W.astype(np.float64)
+    rel = np.linalg.norm(y_new - y_old, axis=1) / np.linalg.norm(y_old, axis=1)
+    assert rel.max() < 2e-3
+    # alpha = 0.5 balances the per-channel ranges: max|act'_j| == max|W'_j| == sqrt(a_j w_j)
+    w_j = np.abs(W.astype(np.float64)).max(axis=1)
+    assert np.allclose(np.abs(W2.astype(np.float64)).max(axis=1), np.sqrt(a * w_j), rtol=1e-6)
+    assert np.allclose(a / s64, np.sqrt(a * w_j), rtol=1e-6)
+
+
+def test_per_channel_quant_bounds():
+    K, N = 256, 96
+    W = inputs.weight(K, N, seed=6, outliers=True)
+    W[:, 5] = 0.0
+    qW, ws = oracle.per_channel_quant_i8(W)
+    assert qW.shape == (N, K)
+    deq = qW.astype(np.float64).T * ws.astype(np.float64)[None, :]
+    assert np.all(np.abs(deq - W) <= ws[None, :] * (0.5 + 1e-6))
+    nz = np.abs(W).max(axis=0) > 0
+    assert np.all(np.abs(qW.astype(np.int64)).max(axis=1)[nz] == 127)
+    assert ws[5] == 1.0 and np.all(qW[5] == 0)
+    assert np.allclose(ws[nz], np.abs(W).max(axis=0)[nz] / 127.0, rtol=1e-6)
+
+
+# ------------------------------------------------------------------------------------------------
+# int8 GEMM and its dequantising epilogue
+# ------------------------------------------------------------------------------------------------
+
+def test_w8a8_acc_matches_python_integers_and_numpy_int64():
+    rng = np.random.default_rng(0)
+    M, K, N = 3, 48, 8
+    q = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    qW = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    acc = oracle.w8a8_acc(q, qW)
+    for m in range(M):
+        for n in range(N):
+            assert acc[m, n] == sum(int(q[m, k]) * int(qW[n, k]) for k in range(K))
+    q2 = rng.integers(-128, 128, size=(17, 4096), dtype=np.int8)
+    W2 = rng.integers(-127, 128, size=(40, 4096), dtype=np.int8)
+    assert np.array_equal(oracle.w8a8_acc(q2, W2), q2.astype(np.int64) @ W2.astype(np.int64).T)
+    # the adversarial extreme exceeds 2^24 but not 2^31
+    q3 = np.full((1, 4096), -128, np.int8)
+    W3 = np.full((2, 4096), -127, np.int8)
+    assert np.all(oracle.w8a8_acc(q3, W3) == 4096 * 128 * 127)
+
+
+def test_w8a8_epilogue_against_float64():
+    rng = np.random.default_rng(1)
+    acc = rng.integers(-2 ** 20, 2 ** 20, size=(5, 64), dtype=np.int32)
+    xs = rng.uniform(0.001, 0.1, 5).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, 64).astype(np.float32)
+    y = oracle.w8a8_epilogue(acc, xs, ws).astype(np.float64)
+    y64 = acc.astype(np.float64) * xs[:, None].astype(np.float64) * ws[None, :].astype(np.float64)
+    assert np.array_equal(oracle.w8a8_epilogue_f64(acc, xs, ws), y64)
+    assert np.all(np.abs(y - y64) <= np.abs(y64) * (2.0 ** -11 + 2.0 ** -22) + 2.0 ** -25)
+
+
+# ------------------------------------------------------------------------------------------------
+# The worked example printed on the pages (off-path symmetric per-tensor int4)
+# ------------------------------------------------------------------------------------------------
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def test_printed_symmetric_int4_example():
+    gv = _golden("p1_symmetric_int4.txt")
+    w = np.array([gv["max_abs"], -0.05, 0.0166, -gv["max_abs"], 0.02], np.float32)
+    scale, q = oracle.sym_int4_per_tensor(w)
+    assert abs(scale - gv["scale"]) <= gv["scale_abs_tol"]
+    assert q.min() >= gv["code_min"] and q.max() <= gv["code_max"]
+    assert q[0] == gv["code_max"] and q[3] == gv["code_min"]
