@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 weight-quantized linear layers (one JSON line on stdout, rank 0).
+
+Default workload: decode-shaped AWQ W4A16 GEMM on the Llama-2-7B q_proj shape (K = N = 4096,
+group 128, 0.1% x10 weight outliers), M in {1, 4, 16} tokens.  One step runs every M over a stack
+of distinct packed copies of the layer whose total size is more than 3x the L2 cache, so every
+launch streams its weights from HBM.  The step is captured once in a CUDA graph and replayed.
+
+  value      algorithmic bytes of the step / device time (GB/s), all ranks summed
+  e2e        the same, through the public call with the step's activations copied in from pinned
+             host memory and the outputs copied back inside the timed region
+  roofline   the decode kernel against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on a bounded sample, rank 0 only
+
+``--impl reference`` times the CPU oracle itself on the same metric (the source pages ship no
+runnable code; the oracle is the reference arm).  ``--sweep FILE`` additionally measures every
+hot-path row over the five workload families and writes one JSON line per case to FILE.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16/W8A8 GEMM TFLOP/s & GB/s vs GB300 roofline, Llama-7B shapes, M=1..8192"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+DECODE_K, DECODE_N, DECODE_G = 4096, 4096, 128
+DECODE_MS = (1, 4, 16)
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work
+# ------------------------------------------------------------------------------------------------
+
+def w4a16_bytes(M, K, N, G):
+    return K * N // 2 + (K // G) * N * 2 + (K // G) * N // 2 + 2 * M * K + 2 * M * N
+
+
+def w8a8_bytes(M, K, N):
+    return N * K + 4 * N + M * K + 4 * M + 2 * M * N
+
+
+def qrmsnorm_bytes(M, K):
+    return 2 * M * K + 2 * K + M * K + 4 * M
+
+
+def gemm_flops(M, K, N):
+    return 2 * M * K * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        window = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 - 0.15 <= r[0] <= self.t1 + 0.15]
+        use = window if window else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {
+            "sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+            "sm_max_mhz": max([r[2] for r in use]) if use else None,
+            "reasons": reasons,
+            "samples": len(window),
+            "samples_total": len(rows),
+        }
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def aggregate(local_units: float, local_seconds: float, device=None):
+    """Whole-job throughput: units summed over ranks / slowest rank's time (max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_units, local_seconds
+    t = torch.tensor([local_units, local_seconds], dtype=torch.float64, device=device)
+    units = t[:1].clone()
+    secs = t[1:].clone()
+    dist.all_reduce(units, op=dist.ReduceOp.SUM)
+    dist.all_reduce(secs, op=dist.ReduceOp.MAX)
+    return float(units.item()), float(secs.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------
+# ncu-derived DRAM traffic (null unless the profile was taken on the current kernel source)
+# ------------------------------------------------------------------------------------------------
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_md, src_files):
+    path = os.path.join(ROOT, "profiles", profile_md)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_sha(src_files):
+        return None
+    return float(m.group(1))
+
+
+DECODE_SRC = ["weight_quantized_linear_gb300/csrc/w4a16_decode.cu", "weight_quantized_linear_gb300/csrc/common.cuh"]
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle as a baseline
+# ------------------------------------------------------------------------------------------------
+
+def oracle_decode_sample(target_seconds: float):
+    """Time the oracle on the decode workload (one q_proj layer, every M) until ~target_seconds."""
+    import numpy as np
+    import oracle
+    from weight_quantized_linear_gb300 import inputs
+    W = inputs.weight(DECODE_K, DECODE_N, seed=0, outliers=True)
+    qw, s, qz = oracle.awq_quantize(W, DECODE_G)
+    xs = {m: inputs.activations(m, DECODE_K, seed=0) for m in DECODE_MS}
+    done_bytes = 0
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        for m in DECODE_MS:
+            oracle.w4a16_linear(xs[m], qw, s, qz, DECODE_G)
+            done_bytes += w4a16_bytes(m, DECODE_K, DECODE_N, DECODE_G)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= target_seconds:
+            break
+    return done_bytes, el, passes, oracle.num_threads()
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_decode_sample(0.0)
+    t_total = 0.0
+    b_total = 0
+    passes = 0
+    for _ in range(args.steps):
+        b, el, p, cores = oracle_decode_sample(0.0)
+        t_total += el
+        b_total += b
+        passes += p
+    value = b_total / t_total / 1e9
+    cores = oracle.num_threads()
+    sample = (f"one step = one pass of the oracle over the q_proj layer (K=N=4096, G=128) at M=1,4,16 "
+              f"(fp64 accumulation, {cores} OpenMP threads); {passes} passes timed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "decode W4A16 q_proj K=N=4096 G=128, M in {1,4,16}",
+                                        "where": "host CPU cores"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def l2_bytes(torch, dev):
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 132 * 1024 * 1024
+
+
+def build_decode_workload(torch, wql, dev, layers):
+    import numpy as np
+    from weight_quantized_linear_gb300 import inputs
+    W = torch.from_numpy(inputs.weight(DECODE_K, DECODE_N, seed=0, outliers=True)).to(dev)
+    qw, s, qz = wql.awq_pack(W, DECODE_G)
+    del W
+    stack = [(qw, s, qz)] + [(qw.clone(), s.clone(), qz.clone()) for _ in range(layers - 1)]
+    xs = {m: torch.from_numpy(inputs.activations(m, DECODE_K, seed=0)).to(dev) for m in DECODE_MS}
+    ys = {m: [torch.empty((m, DECODE_N), dtype=torch.float16, device=dev) for _ in range(layers)] for m in DECODE_MS}
+    return stack, xs, ys
+
+
+def run_decode_step(wql, stack, xs, ys, ms=DECODE_MS):
+    for m in ms:
+        x = xs[m]
+        for i, (qw, s, qz) in enumerate(stack):
+            wql.w4a16_gemm(x, qw, s, qz, DECODE_G, out=ys[m][i])
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the launch path outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(torch, graph, n, stream):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    rank, local_rank, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from weight_quantized_linear_gb300 import build
+    import weight_quantized_linear_gb300 as wql
+    build.build()
+    wql.load()
+
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    per_layer = w4a16_bytes(0, DECODE_K, DECODE_N, DECODE_G)
+    layers = max(8, -(-3 * l2_bytes(torch, dev) // per_layer) + 1)
+    stack, xs, ys = build_decode_workload(torch, wql, dev, layers)
+    step_bytes = sum(w4a16_bytes(m, DECODE_K, DECODE_N, DECODE_G) for m in DECODE_MS) * layers
+    step_flops = sum(gemm_flops(m, DECODE_K, DECODE_N) for m in DECODE_MS) * layers
+    launches_per_step = len(DECODE_MS) * layers
+
+    stream = torch.cuda.Stream(device=dev)
+    graph = capture(torch, lambda: run_decode_step(wql, stack, xs, ys), stream)
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    wql.device_status(dev)
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    # the timed region: K steps, barrier + synchronize on both sides
+    barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("start")
+    secs = time_replays(torch, graph, args.steps, stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("stop")
+    barrier()
+    # keep the GPU busy for the clock sampler when the timed region was short
+    if clocks and secs < 1.0:
+        extra = max(1, int(1.0 / max(secs / max(args.steps, 1), 1e-6)))
+        clocks.mark("start")
+        time_replays(torch, graph, extra, stream)
+        clocks.mark("stop")
+    clock_info = clocks.stop() if clocks else None
+    wql.device_status(dev)
+
+    units, tmax = aggregate(step_bytes * args.steps, secs, dev)
+    value = units / tmax / 1e9
+    ms_per_step = 1e3 * tmax / args.steps
+
+    # per-M breakdown (device time per launch of the decode kernel)
+    cases = []
+    for m in DECODE_MS:
+        g = capture(torch, lambda m=m: run_decode_step(wql, stack, xs, ys, ms=(m,)), stream)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(50, args.steps))
+        t = time_replays(torch, g, reps, stream)
+        per_launch = t / (reps * layers)
+        b = w4a16_bytes(m, DECODE_K, DECODE_N, DECODE_G)
+        cases.append({"M": m, "us_per_launch": round(per_launch * 1e6, 3),
+                      "GB_s": round(b / per_launch / 1e9, 1), "TFLOP_s": round(gemm_flops(m, DECODE_K, DECODE_N) / per_launch / 1e12, 2),
+                      "frac_hbm": round(b / per_launch / 1e9 / hbm, 4)})
+        del g
+
+    # end to end through the public call: activations in from pinned host memory, outputs back
+    h_x = {m: xs[m].cpu().pin_memory() for m in DECODE_MS}
+    h_y = {m: torch.empty((layers, m, DECODE_N), dtype=torch.float16).pin_memory() for m in DECODE_MS}
+    d_x = {m: torch.empty_like(xs[m]) for m in DECODE_MS}
+    h2d = sum(h_x[m].numel() * 2 for m in DECODE_MS)
+    d2h = sum(h_y[m].numel() * 2 for m in DECODE_MS)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for m in DECODE_MS:
+                d_x[m].copy_(h_x[m], non_blocking=True)
+                for i, (qw, s, qz) in enumerate(stack):
+                    wql.w4a16_gemm(d_x[m], qw, s, qz, DECODE_G, out=ys[m][i])
+                    h_y[m][i].copy_(ys[m][i], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_secs = time.perf_counter() - t0
+    barrier()
+    e_units, e_t = aggregate(step_bytes * e2e_steps, e2e_secs, dev)
+    e2e_value = e_units / e_t / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, el, passes, cores = oracle_decode_sample(args.cpu_seconds)
+        cpu = {"value": b / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{passes} passes of the oracle over one q_proj layer at M=1,4,16 ({el:.1f} s)"}
+
+    achieved = step_bytes / (secs / args.steps) / 1e9
+    traffic = profiled_traffic("w4a16_decode_qproj.md", DECODE_SRC)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+                "kernel": "w4a16_decode_kernel", "algorithmic_bytes_per_launch": round(step_bytes / launches_per_step)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "decode W4A16 GEMM, Llama-2-7B q_proj K=N=4096, group 128, M in {1,4,16}",
+                       "layers_per_step": layers, "launch": "CUDA graph, programmatic dependent launch",
+                       "l2": f"inputs larger than L2: {layers} distinct packed weight copies = {layers * per_layer / 1e6:.0f} MB",
+                       "parallelism": f"replicas x{world}", "tflops": round(step_flops * args.steps * world / tmax / 1e12, 3)},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clock_info,
+            "cases": cases,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,156 @@
+/*
+ * wql.h -- C ABI of the GB300 (sm_103a) weight-quantized linear library (libwql.so).
+ *
+ * Two quantized linear layers as used by LLM serving engines:
+ *   - AWQ-format W4A16: int4 weights packed 8 per uint32, one fp16 scale and one 4-bit zero
+ *     point per group of 32/64/128 input channels, fp16 activations and output.
+ *   - SmoothQuant W8A8: RMSNorm fused with per-token dynamic int8 quantisation, then an
+ *     int8 x int8 -> int32 GEMM dequantised by per-token x per-channel scales.
+ *
+ * Sources (titles of the public write-ups the operations follow):
+ *   [AWQ]  "LMDeploy ... INT4 quantisation" tutorial, section 2: AWQ quantises weights per group
+ *          with an asymmetric zero point from each group's own min/max; group sizes 32/64/128.
+ *   [TM]   same tutorial, section 5.1: the fp16 x int4 GEMM kernel of the serving engine.
+ *   [AUQ]  "AUQ dual-process framework" article, section 3.3 (per-group scale and zero point)
+ *          and section 5.4 (checkpoint tensors qweight, scales, zeros; dim 0 of qweight is the
+ *          grouped input dimension, a multiple of 128 for group 128).
+ *   [W8A8] "LMDeploy W8A8 quantisation guide": weight smoothing (smooth_ln_fcs, alpha 0.5),
+ *          QRMSNorm / QLinear modules, per_token_quant_int8 (scale = absmax / 127),
+ *          per_channel_quant (fp32 scale per output channel), matmul_kernel_dynamic_quant
+ *          (int32 accumulator, c = c * rms_scale * linear_scale).
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major and dense (no strides).  K = input features, N = output
+ *     features, M = tokens (rows of the activation), G = group size.
+ *   - fp16 data is passed as uint16_t bit patterns (IEEE binary16).
+ *   - Every pointer is DEVICE memory owned by the caller, 16-byte aligned.  The library never
+ *     allocates, frees or keeps a pointer after the call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue work
+ *     on that stream and return; outputs are valid once the stream reaches that point.
+ *   - Arguments are validated before anything is enqueued.  On WQL_EINVAL / WQL_EUNSUPPORTED
+ *     nothing is launched and outputs are untouched; wql_last_error() describes the problem.
+ *     WQL_ECUDA reports a launch failure (cudaGetLastError after the launch).
+ *   - Kernels that wait on on-chip barriers give up after a bounded time instead of hanging;
+ *     they then record a device-side error that wql_device_status() returns as WQL_ETIMEOUT.
+ *   - M = 0 is a valid empty call: it returns WQL_OK and launches nothing.
+ *   - The library holds no per-call state; calls on different streams may run concurrently.
+ */
+#ifndef WQL_H_
+#define WQL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum wql_status {
+  WQL_OK = 0,
+  WQL_EINVAL = 1,        /* bad argument: shape, alignment, null pointer, group size */
+  WQL_EUNSUPPORTED = 2,  /* valid request this build does not cover (e.g. K too large) */
+  WQL_ECUDA = 3,         /* CUDA runtime/driver error at launch */
+  WQL_ETIMEOUT = 4       /* a kernel's bounded on-chip wait expired (see wql_device_status) */
+} wql_status;
+
+/* Short constant description of a status code. */
+const char* wql_status_string(int status);
+
+/* Detail message of the last failing call on this host thread ("" if none). */
+const char* wql_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int wql_version(void);
+
+/* Synchronises `stream`, then reports and clears the device-side error word of the current
+ * device: WQL_ETIMEOUT if a kernel abandoned a bounded wait since the last check, WQL_ECUDA if
+ * the synchronisation itself failed, WQL_OK otherwise. */
+wql_status wql_device_status(void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * awq_pack  [AWQ] section 2; [AUQ] sections 3.3 and 5.4.
+ * Quantise fp32 weights w [K, N] to asymmetric int4, per group of G consecutive input
+ * channels (k) and per output channel (n):
+ *     s  = fp16((max_k w - min_k w) / 15)       (1.0 if that rounds to zero)
+ *     z  = clamp(round(-min_k w / s), 0, 15)
+ *     q  = clamp(round(w / s) + z, 0, 15)        round = half to even, fp32 arithmetic
+ * so that w ~ (q - z) * s.  Outputs (all written in full):
+ *     qweight [K, N/8] uint32: code of column n at bits 4*(n%8) of word n/8 of row k
+ *     scales  [K/G, N] fp16
+ *     qzeros  [K/G, N/8] uint32: zero points packed like qweight
+ * Requires G in {32, 64, 128}, K % G == 0, N % 32 == 0, K >= 1.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_awq_pack(const float* w, int K, int N, int group, uint32_t* qweight,
+                        uint16_t* scales, uint32_t* qzeros, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * w4a16_gemm  [AWQ] section 2, [TM] section 5.1.
+ *     y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n]
+ * x [M, K] fp16, packed weight as produced by wql_awq_pack, y [M, N] fp16 (written in full;
+ * accumulation in fp32).  Decode-shaped calls (small M) stream the packed weight once with
+ * tensor-core dot products; prefill-shaped calls use the tcgen05 tensor-core kernel.
+ * Requires G in {32, 64, 128}, K % G == 0, N % 32 == 0, M >= 0.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                          const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                          void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * qrmsnorm_quant_i8  [W8A8] QRMSNorm.forward + rms_norm_dynamic_quant / per_token_quant_int8.
+ * Per row m of x [M, K] fp16, with gamma [K] fp16 (smoothing already folded in):
+ *     ss   = sum_k x^2 in a fixed order: element k joins lane (k/8) % 256, lanes add in
+ *            increasing k, then lanes fold pairwise (t, t+128), (t, t+64), ..., (t, t+1)
+ *     r    = 1 / sqrt(ss / K + eps)
+ *     y_k  = (x_k * r) * gamma_k            (fp32, one rounding per operation, kept in fp32)
+ *     xs_m = max_k |y_k| / 127              (1.0 if the row is all zero)
+ *     q_mk = clamp(round_half_even(y_k / xs_m), -128, 127)
+ * Outputs q [M, K] int8 and xs [M] fp32, bit-exact with the definition above.
+ * Requires K % 8 == 0, 8 <= K <= 16384.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M,
+                                 int K, int8_t* q, float* xs, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * w8a8_gemm  [W8A8] QLinear.forward / matmul_kernel_dynamic_quant.
+ *     acc[m, n] = sum_k q[m, k] * qw[n, k]                 (exact int32)
+ *     y[m, n]   = fp16((float(acc[m, n]) * xs[m]) * ws[n])  (fp32, left to right)
+ * q [M, K] int8 with per-token scales xs [M] fp32; qw [N, K] int8 (input dimension
+ * contiguous, as a torch Linear weight) with per-channel scales ws [N] fp32.
+ * y [M, N] fp16 is written in full; acc_out [M, N] int32 is written too when non-NULL.
+ * The int32 result is exact for every input (|acc| < 2^31 holds for K <= 131072).
+ * workspace: device scratch of at least wql_w8a8_workspace_bytes(M, K, N) bytes, used only
+ * during the call (may be NULL when that size is 0).
+ * Requires K % 16 == 0, N % 32 == 0, M >= 0, K <= 131072.
+ * ---------------------------------------------------------------------------------------- */
+size_t wql_w8a8_workspace_bytes(int M, int K, int N);
+wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
+                         int M, int K, int N, uint16_t* y, int32_t* acc_out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Offline preparation for W8A8 ([W8A8] "weight smoothing" and QLinear.from_float).
+ *
+ * wql_act_absmax: calibration statistic a_j = max_m |RMSNorm_gamma(x)[m, j]| over x [M, K]
+ *   (same fp32 RMSNorm as wql_qrmsnorm_quant_i8, original gamma).  absmax [K] fp32 is
+ *   overwritten.  Requires K % 8 == 0, 8 <= K <= 16384.
+ * wql_smooth: smooth_ln_fcs with alpha = 0.5 for one norm feeding one linear w [K, N] fp32:
+ *     w_j = max_n |w[j, n]|;  s_j = sqrt(a_j / w_j)  (1 where a_j or w_j is 0)
+ *     gamma_out_j = fp16(gamma_j / s_j);  w_out[j, n] = w[j, n] * s_j
+ *   Outputs s [K] fp32, gamma_out [K] fp16, w_out [K, N] fp32 (may alias w).
+ * wql_per_channel_quant_i8: ws_n = max_k |w[k, n]| / 127 (1.0 for a zero column);
+ *     qw[n, k] = clamp(round_half_even(w[k, n] / ws_n), -127, 127)
+ *   w [K, N] fp32 -> qw [N, K] int8 (transposed), ws [N] fp32.
+ * Requires K % 16 == 0, N % 32 == 0.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                          float* absmax, void* stream);
+wql_status wql_smooth(const float* absmax, const uint16_t* gamma, const float* w, int K, int N,
+                      float* s, uint16_t* gamma_out, float* w_out, void* stream);
+wql_status wql_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQL_H_ */

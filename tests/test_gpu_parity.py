@@ -1,0 +1,253 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Bars: packed weights, int8 activations and scales, per-channel weights and int32 accumulators
+bit-exact; fp16 outputs within 1e-2 of the fp64 oracle, normalised by each row's L2 norm.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from weight_quantized_linear_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ROW_TOL = 1e-2  # max over rows of ||y_gpu - y_ref||_2 / ||y_ref||_2
+
+
+@pytest.fixture(scope="module")
+def wql(wql_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return wql_lib
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def u32_to_i32(a):
+    return np.ascontiguousarray(a).view(np.int32)
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def row_rel_err(y, ref):
+    y = y.astype(np.float64)
+    num = np.linalg.norm(y - ref, axis=1)
+    den = np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    return float((num / den).max())
+
+
+def sample_rows(M, n=16):
+    if M <= n:
+        return np.arange(M, dtype=np.int64)
+    r = np.unique(np.concatenate([[0, M - 1], np.linspace(0, M - 1, n - 2).astype(np.int64)]))
+    return r.astype(np.int64)
+
+
+# ------------------------------------------------------------------------------------------------
+# awq_pack: bit-exact
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,N,G,outl", [(512, 512, 128, False), (256, 96, 32, True), (128, 160, 64, True),
+                                        (4096, 4096, 128, True), (11008, 4096, 64, True), (4096, 22016, 32, True)])
+def test_awq_pack_bit_exact(wql, K, N, G, outl):
+    W = inputs.weight(K, N, seed=0, outliers=outl)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    assert np.array_equal(host(qw), u32_to_i32(qw_r))
+    assert np.array_equal(host(s).view(np.uint16), s_r.view(np.uint16))
+    assert np.array_equal(host(qz), u32_to_i32(qz_r))
+
+
+def test_awq_pack_degenerate_groups(wql):
+    K, N, G = 64, 32, 32
+    W = np.zeros((K, N), np.float32)
+    W[G:, :16] = 0.5  # constant nonzero group
+    W[G:, 16:] = inputs.weight(G, 16, seed=1)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    assert np.array_equal(host(qw), u32_to_i32(qw_r))
+    assert np.array_equal(host(s).view(np.uint16), s_r.view(np.uint16))
+    assert np.array_equal(host(qz), u32_to_i32(qz_r))
+
+
+# ------------------------------------------------------------------------------------------------
+# w4a16_gemm: fp16 output vs fp64 oracle
+# ------------------------------------------------------------------------------------------------
+
+def _w4a16_case(wql, M, K, N, G, w_out=True, x_out=False, seed=0, rows=None):
+    W = inputs.weight(K, N, seed=seed, outliers=w_out)
+    X = inputs.activations(M, K, seed=seed, outlier_channels=x_out)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    y = host(wql.w4a16_gemm(dev(X), dev(u32_to_i32(qw_r)), dev(s_r), dev(u32_to_i32(qz_r)), G))
+    rows = np.arange(M, dtype=np.int64) if rows is None else rows
+    ref = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
+    return y[rows], ref
+
+
+TINY_AND_EDGE = [
+    (1, 512, 512, 128),   # tiny config
+    (1, 32, 32, 32),      # smallest legal shape: one group, one word column group
+    (3, 256, 96, 32),     # ragged N (not a multiple of the 128-column strip)
+    (17, 128, 160, 128),  # K == G, ragged M and N
+    (33, 512, 64, 64),    # M just above a 32-token block
+    (8, 4096, 4096, 128),
+    (5, 11008, 4096, 128),  # K with 172 stages of 64 rows
+]
+
+
+@pytest.mark.parametrize("M,K,N,G", TINY_AND_EDGE)
+def test_w4a16_parity_small_and_edge(wql, M, K, N, G):
+    y, ref = _w4a16_case(wql, M, K, N, G)
+    assert np.isfinite(y).all()
+    assert row_rel_err(y, ref) <= ROW_TOL
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_w4a16_parity_decode_qproj(wql, M):
+    y, ref = _w4a16_case(wql, M, 4096, 4096, 128)
+    err = row_rel_err(y, ref)
+    assert err <= ROW_TOL
+    # the kernel's own arithmetic (exact products, fp32 sums, one fp16 rounding) is far tighter
+    assert err <= 2e-3
+
+
+@pytest.mark.parametrize("case", inputs.sweep_cases(), ids=lambda c: f"M{c['M']}K{c['K']}N{c['N']}G{c['G']}")
+def test_w4a16_parity_layer_sweep(wql, case):
+    rows = sample_rows(case["M"], 16)
+    y, ref = _w4a16_case(wql, case["M"], case["K"], case["N"], case["G"], rows=rows)
+    assert row_rel_err(y, ref) <= ROW_TOL
+
+
+@pytest.mark.parametrize("case", inputs.prefill_cases(), ids=lambda c: f"M{c['M']}N{c['N']}")
+def test_w4a16_parity_prefill_sampled_rows(wql, case):
+    rows = sample_rows(case["M"], 12)
+    y, ref = _w4a16_case(wql, case["M"], case["K"], case["N"], case["G"], w_out=False, x_out=True, rows=rows)
+    assert row_rel_err(y, ref) <= ROW_TOL
+
+
+def test_w4a16_zero_activations_give_zero(wql):
+    K, N, G = 256, 64, 32
+    W = inputs.weight(K, N, seed=3)
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    y = host(wql.w4a16_gemm(torch.zeros((4, K), dtype=torch.float16, device="cuda"), qw, s, qz, G))
+    assert np.all(y == 0)
+    wql.device_status()
+
+
+# ------------------------------------------------------------------------------------------------
+# QRMSNorm + per-token int8: bit-exact
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K", [(1, 8), (7, 512), (33, 4096), (3, 11008), (2, 16384), (512, 4096)])
+def test_qrmsnorm_quant_bit_exact(wql, M, K):
+    X = inputs.activations(M, K, seed=1, outlier_channels=True)
+    g = inputs.gamma(K, seed=1)
+    if M >= 3:
+        X[1] = 0  # all-zero row
+        X[2] = np.float16(0.375)  # constant row
+    q_r, xs_r = oracle.qrmsnorm_quant_i8(X, g, inputs.EPS)
+    q, xs = wql.qrmsnorm_quant_i8(dev(X), dev(g), inputs.EPS)
+    assert np.array_equal(host(q), q_r)
+    assert np.array_equal(host(xs).view(np.uint32), xs_r.view(np.uint32))
+
+
+# ------------------------------------------------------------------------------------------------
+# SmoothQuant W8A8: prep chain bit-exact, int32 accumulators bit-exact, fp16 output bit-exact
+# ------------------------------------------------------------------------------------------------
+
+def _w8a8_chain(wql, M, K, N, seed=0):
+    X = inputs.activations(M, K, seed=seed, outlier_channels=True)
+    g = inputs.gamma(K, seed=seed)
+    W = inputs.weight(K, N, seed=seed)
+    # oracle
+    a_r = oracle.act_absmax(X, g, inputs.EPS)
+    s_r, g2_r, W2_r = oracle.smooth(a_r, g, W)
+    qW_r, ws_r = oracle.per_channel_quant_i8(W2_r)
+    q_r, xs_r = oracle.qrmsnorm_quant_i8(X, g2_r, inputs.EPS)
+    # CUDA path
+    Xd, gd, Wd = dev(X), dev(g), dev(W)
+    a = wql.act_absmax(Xd, gd, inputs.EPS)
+    s, g2, W2 = wql.smooth(a, gd, Wd)
+    qW, ws = wql.per_channel_quant_i8(W2)
+    q, xs = wql.qrmsnorm_quant_i8(Xd, g2, inputs.EPS)
+    got = dict(a=host(a), s=host(s), g2=host(g2), W2=host(W2), qW=host(qW), ws=host(ws), q=host(q), xs=host(xs))
+    ref = dict(a=a_r, s=s_r, g2=g2_r, W2=W2_r, qW=qW_r, ws=ws_r, q=q_r, xs=xs_r)
+    return got, ref, (q, xs, qW, ws)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 512, 64), (16, 4096, 4096), (37, 1024, 96)])
+def test_w8a8_prep_chain_bit_exact(wql, M, K, N):
+    got, ref, _ = _w8a8_chain(wql, M, K, N)
+    for k in ("a", "s", "W2", "ws", "xs"):
+        assert np.array_equal(got[k].view(np.uint32), ref[k].view(np.uint32)), k
+    assert np.array_equal(got["g2"].view(np.uint16), ref["g2"].view(np.uint16))
+    assert np.array_equal(got["qW"], ref["qW"])
+    assert np.array_equal(got["q"], ref["q"])
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 11008), (5, 512, 96), (33, 1024, 160),
+                                   (512, 4096, 4096)])
+def test_w8a8_gemm_bit_exact(wql, M, K, N):
+    got, ref, (q, xs, qW, ws) = _w8a8_chain(wql, M, K, N, seed=2)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = wql.w8a8_gemm(q, xs, qW, ws, acc_out=acc)
+    rows = sample_rows(M, 24)
+    acc_r = oracle.w8a8_acc(ref["q"], ref["qW"], rows=rows)
+    y_r = oracle.w8a8_epilogue(acc_r, ref["xs"][rows], ref["ws"])
+    assert np.array_equal(host(acc)[rows], acc_r)
+    assert np.array_equal(host(y)[rows].view(np.uint16), y_r.view(np.uint16))
+    y64 = oracle.w8a8_epilogue_f64(acc_r, ref["xs"][rows], ref["ws"])
+    assert row_rel_err(host(y)[rows], y64) <= ROW_TOL
+
+
+@pytest.mark.parametrize("K", [4096, 16384])
+def test_w8a8_int32_exact_beyond_fp32_integer_range(wql, K):
+    # all products at the extreme: |acc| = K * 128 * 127 > 2^24, where plain fp32 sums lose integers
+    M, N = 3, 64
+    q = np.full((M, K), -128, np.int8)
+    q[1] = 127
+    q[2, ::2] = -128
+    q[2, 1::2] = 127
+    qW = np.full((N, K), -127, np.int8)
+    qW[1::2] = 127
+    xs = np.full((M,), 0.01, np.float32)
+    ws = np.full((N,), 0.001, np.float32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), acc_out=acc)
+    assert np.array_equal(host(acc), oracle.w8a8_acc(q, qW))
+
+
+def test_w8a8_random_extremes_bit_exact(wql):
+    rng = np.random.default_rng(5)
+    M, K, N = 9, 8192, 128
+    q = rng.choice(np.array([-128, -127, 127, 0, 1], np.int8), size=(M, K))
+    qW = rng.choice(np.array([-127, 127, 0, -1], np.int8), size=(N, K))
+    xs = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), acc_out=acc)
+    acc_r = oracle.w8a8_acc(q, qW)
+    assert np.array_equal(host(acc), acc_r)
+    assert np.array_equal(host(y).view(np.uint16), oracle.w8a8_epilogue(acc_r, xs, ws).view(np.uint16))
+    wql.device_status()
+
+
+# ------------------------------------------------------------------------------------------------
+# boundary behaviour on the device
+# ------------------------------------------------------------------------------------------------
+
+def test_empty_calls_and_errors(wql):
+    x = torch.empty((0, 256), dtype=torch.float16, device="cuda")
+    W = inputs.weight(256, 64, seed=0)
+    qw, s, qz = wql.awq_pack(dev(W), 32)
+    y = wql.w4a16_gemm(x, qw, s, qz, 32)
+    assert y.shape == (0, 64)
+    with pytest.raises(wql.WQLError):
+        wql.awq_pack(dev(W[:, :48].copy()), 32)  # N not a multiple of 32
+    wql.device_status()

@@ -1,0 +1,25 @@
+"""GB300-native weight-quantized linear layers (AWQ W4A16, SmoothQuant W8A8).
+
+The compute lives in ``libwql.so`` (hand-written CUDA for sm_103a behind the C ABI of
+``include/wql.h``); this package only marshals torch tensors into that ABI.  Build it with
+``weight_quantized_linear_gb300.build.build()``.  Importing the package does not load the library;
+the first call does, and raises if it is missing.
+"""
+from ._lib import (  # noqa: F401
+    WQLError,
+    act_absmax,
+    awq_pack,
+    device_status,
+    load,
+    per_channel_quant_i8,
+    qrmsnorm_quant_i8,
+    smooth,
+    w4a16_gemm,
+    w8a8_gemm,
+    w8a8_workspace_bytes,
+)
+
+__all__ = [
+    "WQLError", "act_absmax", "awq_pack", "device_status", "load", "per_channel_quant_i8",
+    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w8a8_gemm", "w8a8_workspace_bytes",
+]

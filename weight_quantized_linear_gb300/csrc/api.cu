@@ -1,0 +1,225 @@
+// api.cu -- the extern "C" entry points declared in include/wql.h: argument validation, kernel
+// selection by shape, launch-error reporting and the per-device error word of bounded waits.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+#include "wql.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// One error word per device (this module's copy on each device that loads the library).
+__device__ unsigned g_wql_device_error;
+
+unsigned* device_error_word() {
+  static unsigned* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wql_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  return cache[dev];
+}
+
+wql_status fail(wql_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+wql_status cuda_status(cudaError_t e, const char* what, const std::string& extra = std::string()) {
+  if (e == cudaSuccess) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+  if (!extra.empty()) msg += " (" + extra + ")";
+  return fail(WQL_ECUDA, msg);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define WQL_REQUIRE(cond, msg)                      \
+  do {                                              \
+    if (!(cond)) return fail(WQL_EINVAL, (msg));    \
+  } while (0)
+
+#define WQL_REQUIRE_PTR(p) WQL_REQUIRE((p) != nullptr && aligned16(p), #p " must be a non-null 16-byte aligned device pointer")
+
+bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wql_status_string(int status) {
+  switch (status) {
+    case WQL_OK:
+      return "ok";
+    case WQL_EINVAL:
+      return "invalid argument";
+    case WQL_EUNSUPPORTED:
+      return "unsupported request";
+    case WQL_ECUDA:
+      return "CUDA error";
+    case WQL_ETIMEOUT:
+      return "device-side wait timed out";
+    default:
+      return "unknown status";
+  }
+}
+
+const char* wql_last_error(void) { return g_last_error.c_str(); }
+
+int wql_version(void) { return 100; }
+
+wql_status wql_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e, "wql_device_status: stream synchronize");
+  unsigned* w = device_error_word();
+  if (!w) return fail(WQL_ECUDA, "wql_device_status: cannot locate the device error word");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e, "wql_device_status: read error word");
+  if (v != 0) {
+    const unsigned zero = 0;
+    cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    char buf[96];
+    snprintf(buf, sizeof(buf), "a kernel abandoned a bounded wait (error bits 0x%x)", v);
+    return fail(WQL_ETIMEOUT, buf);
+  }
+  g_last_error.clear();
+  return WQL_OK;
+}
+
+wql_status wql_awq_pack(const float* w, int K, int N, int group, uint32_t* qweight, uint16_t* scales,
+                        uint32_t* qzeros, void* stream) {
+  WQL_REQUIRE(valid_group(group), "group must be 32, 64 or 128");
+  WQL_REQUIRE(K >= group && K % group == 0, "K must be a positive multiple of the group size");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE_PTR(w);
+  WQL_REQUIRE_PTR(qweight);
+  WQL_REQUIRE_PTR(scales);
+  WQL_REQUIRE_PTR(qzeros);
+  return cuda_status(wql::launch_awq_pack(w, K, N, group, qweight, scales, qzeros, static_cast<cudaStream_t>(stream)),
+                     "wql_awq_pack");
+}
+
+wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                          const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, void* stream) {
+  WQL_REQUIRE(valid_group(group), "group must be 32, 64 or 128");
+  WQL_REQUIRE(K >= group && K % group == 0, "K must be a positive multiple of the group size");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(x);
+  WQL_REQUIRE_PTR(qweight);
+  WQL_REQUIRE_PTR(scales);
+  WQL_REQUIRE_PTR(qzeros);
+  WQL_REQUIRE_PTR(y);
+  unsigned* dev_err = device_error_word();
+  std::string err;
+  cudaError_t e = wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
+                                           static_cast<cudaStream_t>(stream), &err);
+  if (!err.empty()) return fail(WQL_ECUDA, "wql_w4a16_gemm: " + err);
+  return cuda_status(e, "wql_w4a16_gemm");
+}
+
+wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
+                                 float* xs, void* stream) {
+  WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (K > 16384) return fail(WQL_EUNSUPPORTED, "K > 16384 is not supported by the register-resident row kernel");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(x);
+  WQL_REQUIRE_PTR(gamma);
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  return cuda_status(wql::launch_qrmsnorm_quant_i8(x, gamma, eps, M, K, q, xs, static_cast<cudaStream_t>(stream)),
+                     "wql_qrmsnorm_quant_i8");
+}
+
+size_t wql_w8a8_workspace_bytes(int M, int K, int N) {
+  (void)M;
+  (void)K;
+  (void)N;
+  return 0;
+}
+
+wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K, int N,
+                         uint16_t* y, int32_t* acc_out, void* workspace, size_t workspace_bytes, void* stream) {
+  WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
+  WQL_REQUIRE(K <= 131072, "K must be <= 131072 so that the int32 accumulator cannot overflow");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE_PTR(qw);
+  WQL_REQUIRE_PTR(ws);
+  WQL_REQUIRE_PTR(y);
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  WQL_REQUIRE(acc_out == nullptr || aligned16(acc_out), "acc_out must be NULL or 16-byte aligned");
+  const size_t need = wql_w8a8_workspace_bytes(M, K, N);
+  WQL_REQUIRE(workspace_bytes >= need, "workspace is smaller than wql_w8a8_workspace_bytes()");
+  WQL_REQUIRE(need == 0 || (workspace != nullptr && aligned16(workspace)), "workspace must be 16-byte aligned");
+  unsigned* dev_err = device_error_word();
+  std::string err;
+  cudaError_t e = wql::launch_w8a8_decode(q, xs, qw, ws, M, K, N, y, acc_out, dev_err,
+                                          static_cast<cudaStream_t>(stream), &err);
+  if (!err.empty()) return fail(WQL_ECUDA, "wql_w8a8_gemm: " + err);
+  return cuda_status(e, "wql_w8a8_gemm");
+}
+
+wql_status wql_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,
+                          void* stream) {
+  WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (K > 16384) return fail(WQL_EUNSUPPORTED, "K > 16384 is not supported by the register-resident row kernel");
+  WQL_REQUIRE_PTR(absmax);
+  if (M > 0) {
+    WQL_REQUIRE_PTR(x);
+    WQL_REQUIRE_PTR(gamma);
+  }
+  return cuda_status(wql::launch_act_absmax(x, gamma, eps, M, K, absmax, static_cast<cudaStream_t>(stream)),
+                     "wql_act_absmax");
+}
+
+wql_status wql_smooth(const float* absmax, const uint16_t* gamma, const float* w, int K, int N, float* s,
+                      uint16_t* gamma_out, float* w_out, void* stream) {
+  WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE_PTR(absmax);
+  WQL_REQUIRE_PTR(gamma);
+  WQL_REQUIRE_PTR(w);
+  WQL_REQUIRE_PTR(s);
+  WQL_REQUIRE_PTR(gamma_out);
+  WQL_REQUIRE_PTR(w_out);
+  return cuda_status(wql::launch_smooth(absmax, gamma, w, K, N, s, gamma_out, w_out, static_cast<cudaStream_t>(stream)),
+                     "wql_smooth");
+}
+
+wql_status wql_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws, void* stream) {
+  WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE_PTR(w);
+  WQL_REQUIRE_PTR(qw);
+  WQL_REQUIRE_PTR(ws);
+  return cuda_status(wql::launch_per_channel_quant_i8(w, K, N, qw, ws, static_cast<cudaStream_t>(stream)),
+                     "wql_per_channel_quant_i8");
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// internal.h -- host-side declarations shared by the translation units of libwql.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace wql {
+
+// Encode a 2D tiled TMA descriptor for a row-major matrix [outer, inner] of `elem_bytes`-sized
+// elements with a row pitch of `row_bytes`.  Returns false and fills *err on failure.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+                  uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle, std::string* err);
+
+int num_sms();  // SM count of the current device (cached per device)
+
+// Launchers.  Each returns cudaSuccess or the launch error; *err gets a message for
+// non-CUDA failures (descriptor encoding).  Arguments are already validated by api.cu.
+cudaError_t launch_awq_pack(const float* w, int K, int N, int group, uint32_t* qweight,
+                            uint16_t* scales, uint32_t* qzeros, cudaStream_t s);
+
+cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                                const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                unsigned* dev_err, cudaStream_t s, std::string* err);
+
+cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                                     int8_t* q, float* xs, cudaStream_t s);
+
+cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                              float* absmax, cudaStream_t s);
+
+cudaError_t launch_smooth(const float* absmax, const uint16_t* gamma, const float* w, int K, int N,
+                          float* s_out, uint16_t* gamma_out, float* w_out, cudaStream_t s);
+
+cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws,
+                                        cudaStream_t s);
+
+cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
+                               int M, int K, int N, uint16_t* y, int32_t* acc_out, unsigned* dev_err,
+                               cudaStream_t s, std::string* err);
+
+}  // namespace wql

@@ -1,0 +1,286 @@
+// w8a8_decode.cu -- SmoothQuant W8A8 GEMM for decode-shaped calls ("LMDeploy W8A8 quantisation
+// guide", QLinear.forward / matmul_kernel_dynamic_quant: int8 x int8 products accumulated in
+// int32, then c = c * rms_scale * linear_scale in fp32 and rounded to fp16).
+//
+// GB300 has no int8 path in tcgen05 and its legacy int8 mma.sync runs at a quarter of the fp16
+// rate, so int8 values are converted exactly to fp16 in registers (PRMT places each biased byte in
+// the mantissa of 1024 + b + 128, one f16x2 add removes 1152) and multiplied on the fp16
+// mma.sync.m16n8k16 path with fp32 accumulation.  Products are at most 128 * 127 = 16256 < 2^14;
+// each thread folds its fp32 partial sums into int32 before they can cover more than 1024
+// products (< 2^24), so every partial sum is an integer that fp32 holds exactly and the int32
+// result is exact for every input.
+//
+// Weights are the 16-row MMA operand ("swap AB"), tokens the 8-column operand.  Weight tiles of
+// 128 output channels x 64 k stream once from HBM through a TMA pipeline; split-K across the
+// CTAs of a cluster, reduced through distributed shared memory in int32.
+#include "common.cuh"
+#include "internal.h"
+
+namespace wql {
+namespace {
+
+constexpr int kBK = 64;            // k per stage (bytes of a weight row)
+constexpr int kRows = 128;         // output channels per CTA
+constexpr int kConsumerWarps = 8;  // 4 tile pairs x 2 k16 phases
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kFoldStages = 32;    // each warp sees 32 k per stage: fold to int32 every 1024 k
+
+template <int MT>
+struct Layout8 {
+  static constexpr int kXBytes = 8 * MT * kBK;  // token rows x 64 B
+  static constexpr int kWBytes = kRows * kBK;   // 128 rows x 64 B
+  static constexpr int kStage = (kXBytes + kWBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = 8;
+  static constexpr int kPipe = kStages * kStage;
+  static constexpr int kRed = 2 * 8 * MT * kRows * 4;  // [2 k phases][tokens][128] int32
+  static constexpr int kData = kPipe > kRed ? kPipe : kRed;
+  static constexpr int kBytes = kData + 1024 + 2 * kStages * 8;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Byte offset of 4-byte word t of 16-byte chunk c in row r of a 64-byte-row tile, 64B swizzle.
+__device__ __forceinline__ uint32_t tile64_off(int r, int c, int t) {
+  return r * 64 + (((c ^ (r >> 1)) & 3) << 4) + t * 4;
+}
+
+// Four int8 -> two f16x2 (bytes 0,1 and bytes 2,3), exact.
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = v ^ 0x80808080u;
+  lo = hadd2_u32(prmt(u, 0x64646464u, 0x4140u), 0xE480E480u);
+  hi = hadd2_u32(prmt(u, 0x64646464u, 0x4342u), 0xE480E480u);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] int8, box {64, 8MT}, SW64
+                       const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] int8, box {64, 128}, SW64
+                       const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int kblocks,
+                       __half* __restrict__ y, int32_t* __restrict__ acc_out, unsigned* err) {
+  using L = Layout8<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kData);
+  uint64_t* empty = full + L::kStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int strip = blockIdx.x;
+  const int split = blockIdx.y, nsplit = gridDim.y;
+  const int m0 = blockIdx.z * 8 * MT;
+  const int kb0 = (int)((long long)kblocks * split / nsplit);
+  const int kb1 = (int)((long long)kblocks * (split + 1) / nsplit);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  const int g = lane >> 2, t = lane & 3;
+  const int tp = warp & 3, kp = warp >> 2;  // tile pair (32 channels) and k16 phase
+  int tot[2][MT][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tot[a][mt][i] = 0;
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      const uint64_t pol = policy_evict_first();
+      const uint32_t bytes = L::kXBytes + L::kWBytes;
+      int issued = 0;
+      grid_dependency_wait();
+      for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+        const int s = issued % L::kStages;
+        const uint32_t ph = (issued / L::kStages) & 1;
+        if (issued >= L::kStages && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+          report_error(err, kErrTimeoutEmpty);
+          break;
+        }
+        uint8_t* st = smem + s * L::kStage;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        tma_load_2d(st, &tm_x, &full[s], kb * kBK, m0);
+        tma_load_2d_hint(st + L::kXBytes, &tm_w, &full[s], kb * kBK, strip * kRows, pol);
+      }
+      const int n = issued < L::kStages ? issued : L::kStages;
+      for (int i = issued - n; i < issued; ++i) {
+        if (!mbar_wait_bounded(&full[i % L::kStages], (i / L::kStages) & 1)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+      }
+    }
+  } else {
+    float acc[2][MT][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[a][mt][i] = 0.f;
+
+    auto fold = [&]() {
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            tot[a][mt][i] += __float2int_rn(acc[a][mt][i]);
+            acc[a][mt][i] = 0.f;
+          }
+    };
+
+    int it = 0;
+    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      const int s = it % L::kStages;
+      if (!mbar_wait_bounded(&full[s], (it / L::kStages) & 1)) {
+        report_error(err, kErrTimeoutFull);
+        break;
+      }
+      const uint32_t xt = smem_u32(smem + s * L::kStage);
+      const uint32_t wt = xt + L::kXBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = kp + 2 * h;  // 16-byte chunk = k16 step within the stage
+        uint32_t bx[MT][2];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) i8x4_to_h2x2(lds_u32(xt + tile64_off(8 * mt + g, c, t)), bx[mt][0], bx[mt][1]);
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const int r = 32 * tp + 16 * a + g;
+          uint32_t A[4];
+          i8x4_to_h2x2(lds_u32(wt + tile64_off(r, c, t)), A[0], A[2]);
+          i8x4_to_h2x2(lds_u32(wt + tile64_off(r + 8, c, t)), A[1], A[3]);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) mma_f16_16816(acc[a][mt], A, bx[mt][0], bx[mt][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if ((it + 1) % kFoldStages == 0) fold();
+    }
+    fold();
+  }
+
+  __syncthreads();
+  int* red = reinterpret_cast<int*>(smem);
+  constexpr int kE = 8 * MT * kRows;
+  if (warp < kConsumerWarps) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = 8 * mt + 2 * t + (i & 1);
+          const int col = 32 * tp + 16 * a + g + 8 * (i >> 1);
+          red[kp * kE + row * kRows + col] = tot[a][mt][i];
+        }
+  }
+  cluster_sync();
+  {
+    const uint32_t rank = cluster_ctarank();
+    const int nq = kE / 4;
+    const int f0 = (int)((long long)nq * rank / nsplit), f1 = (int)((long long)nq * (rank + 1) / nsplit);
+    for (int f = f0 + threadIdx.x; f < f1; f += kThreads) {
+      int4 v = make_int4(0, 0, 0, 0);
+      for (int q = 0; q < nsplit; ++q) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const int4 u = ld_cluster_i4(map_cluster(red + p * kE + 4 * f, q));
+          v.x += u.x;
+          v.y += u.y;
+          v.z += u.z;
+          v.w += u.w;
+        }
+      }
+      const int row = (4 * f) / kRows, col = (4 * f) % kRows;
+      const int m = m0 + row, n = strip * kRows + col;
+      if (m < M && n < N) {
+        const float xm = xs[m];
+        const float4 wn = *reinterpret_cast<const float4*>(ws + n);
+        const int iv[4] = {v.x, v.y, v.z, v.w};
+        const float wv[4] = {wn.x, wn.y, wn.z, wn.w};
+        __align__(8) __half hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(iv[e]), xm), wv[e]));
+        *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = *reinterpret_cast<const uint2*>(hv);
+        if (acc_out) *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) = v;
+      }
+    }
+  }
+  cluster_sync();
+}
+
+template <int MT>
+cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* xs, const float* ws, int M, int N,
+                    int kblocks, __half* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream) {
+  using L = Layout8<MT>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(w8a8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int strips = (N + kRows - 1) / kRows;
+  const int mblocks = (M + 8 * MT - 1) / (8 * MT);
+  const int target = 2 * num_sms();
+  int S = (target + strips * mblocks - 1) / (strips * mblocks);
+  if (S > 8) S = 8;
+  if (S > kblocks) S = kblocks;
+  if (S < 1) S = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(strips, S, mblocks);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = S;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, w8a8_decode_kernel<MT>, tx, tw, xs, ws, M, N, kblocks, y, acc_out, dev_err);
+}
+
+}  // namespace
+
+cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
+                               int N, uint16_t* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream,
+                               std::string* err) {
+  const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+  CUtensorMap tx, tw;
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, K, M, (uint64_t)K, kBK, 8 * MT,
+                    CU_TENSOR_MAP_SWIZZLE_64B, err) ||
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kRows,
+                    CU_TENSOR_MAP_SWIZZLE_64B, err)) {
+    return cudaErrorInvalidValue;
+  }
+  const int kblocks = (K + kBK - 1) / kBK;
+  __half* yh = reinterpret_cast<__half*>(y);
+  switch (MT) {
+    case 1:
+      return launch8<1>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+    case 2:
+      return launch8<2>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+    default:
+      return launch8<4>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+  }
+}
+
+}  // namespace wql
