@@ -251,3 +251,70 @@ def test_empty_calls_and_errors(wql):
     with pytest.raises(wql.WQLError):
         wql.awq_pack(dev(W[:, :48].copy()), 32)  # N not a multiple of 32
     wql.device_status()
+
+
+# ------------------------------------------------------------------------------------------------
+# long back-to-back launch chains (programmatic dependent launch, graph replay): the pipelined
+# kernels must stay correct and fault-free over thousands of launches
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 4096, 4096, 128), (16, 4096, 4096, 128), (4, 11008, 4096, 32)])
+def test_w4a16_decode_back_to_back_stress(wql, M, K, N, G):
+    layers, reps = 16, 150
+    W = inputs.weight(K, N, seed=1)
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    stack = [(qw.clone(), s.clone(), qz.clone()) for _ in range(layers)]
+    x = dev(inputs.activations(M, K, seed=1))
+    ref = wql.w4a16_gemm(x, qw, s, qz, G).clone()
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(layers)]
+    stream = torch.cuda.Stream()
+
+    def step():
+        for i, (a, b, c) in enumerate(stack):
+            wql.w4a16_gemm(x, a, b, c, G, out=ys[i])
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    torch.cuda.synchronize()
+    wql.device_status()
+    for y in ys:
+        assert torch.equal(y, ref)  # deterministic: bit-identical to the single call
+
+
+def test_w8a8_decode_back_to_back_stress(wql):
+    M, K, N = 16, 4096, 4096
+    rng = np.random.default_rng(3)
+    q = dev(rng.integers(-128, 128, size=(M, K), dtype=np.int8))
+    xs = dev(rng.uniform(1e-3, 1e-2, M).astype(np.float32))
+    qW = dev(rng.integers(-127, 128, size=(N, K), dtype=np.int8))
+    ws = dev(rng.uniform(1e-4, 1e-3, N).astype(np.float32))
+    ref = wql.w8a8_gemm(q, xs, qW, ws).clone()
+    layers, reps = 16, 150
+    stack = [qW.clone() for _ in range(layers)]
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(layers)]
+    stream = torch.cuda.Stream()
+
+    def step():
+        for i, w in enumerate(stack):
+            wql.w8a8_gemm(q, xs, w, ws, out=ys[i])
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    torch.cuda.synchronize()
+    wql.device_status()
+    for y in ys:
+        assert torch.equal(y, ref)

@@ -139,6 +139,63 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier: a relaxed arrival at kernel start, and the matching wait just before the
+// first access to a peer's shared memory (which must not happen before every peer has started).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_i4(uint32_t addr, int4 v) {
+  asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Asynchronous store of 16 bytes into a peer CTA's shared memory; its completion is counted as 16
+// transaction bytes on the peer's mbarrier (both addresses in the shared::cluster window).
+__device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_i4(uint32_t remote_addr, int4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
+}
+
+// 3D tiled TMA load (coordinates x innermost).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Owner rank of float4 index f when nq float4s are split into `parts` contiguous slices
+// [floor(nq r / parts), floor(nq (r + 1) / parts)).
+__device__ __forceinline__ int slice_owner(int f, int nq, int parts) {
+  int r = (int)(((long long)f * parts) / nq);
+  while (r + 1 < parts && (int)((long long)nq * (r + 1) / parts) <= f) ++r;
+  while (r > 0 && (int)((long long)nq * r / parts) > f) --r;
+  return r;
+}
+
 // Address of the same shared-memory variable in CTA `rank` of this cluster (shared::cluster).
 __device__ __forceinline__ uint32_t map_cluster(const void* p, uint32_t rank) {
   uint32_t out;
@@ -148,10 +205,11 @@ __device__ __forceinline__ uint32_t map_cluster(const void* p, uint32_t rank) {
 
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   float4 v;
+  // volatile keeps these loads after the cluster barrier; no memory clobber, so several can be in
+  // flight before their values are used
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 
@@ -159,8 +217,7 @@ __device__ __forceinline__ int4 ld_cluster_i4(uint32_t addr) {
   int4 v;
   asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 

@@ -15,7 +15,17 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, c
                   uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                   uint32_t box_outer, CUtensorMapSwizzle swizzle, std::string* err);
 
+// Encode a 3D tiled TMA descriptor: element (x, y, z) at base + x*elem + y*stride1 + z*stride2.
+bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                  CUtensorMapSwizzle swizzle, std::string* err);
+
 int num_sms();  // SM count of the current device (cached per device)
+
+// Split factor S (cluster size along k, 1..8) for a split-K launch of `units` independent output
+// tiles: the largest S whose units * S CTAs are all co-resident in one wave (occupancy query with
+// the cluster attribute, cached per kernel and device), bounded by the number of k blocks.
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks);
 
 // Launchers.  Each returns cudaSuccess or the launch error; *err gets a message for
 // non-CUDA failures (descriptor encoding).  Arguments are already validated by api.cu.

@@ -53,6 +53,27 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, c
   return true;
 }
 
+bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                  CUtensorMapSwizzle swizzle, std::string* err) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) {
+    if (err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) *err = "cuTensorMapEncodeTiled (3D) failed (code " + std::to_string((int)r) + ")";
+    return false;
+  }
+  return true;
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -64,6 +85,60 @@ int num_sms() {
     cache[dev] = v > 0 ? v : 148;
   }
   return cache[dev];
+}
+
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks) {
+  struct Entry {
+    const void* k;
+    int dev, smem, cap[9];
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int n_cache = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int cap[9] = {0};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    int found = -1;
+    for (int i = 0; i < n_cache; ++i)
+      if (cache[i].k == kernel && cache[i].dev == dev && cache[i].smem == smem_bytes) found = i;
+    if (found < 0) {
+      Entry e{kernel, dev, smem_bytes, {0}};
+      for (int S = 1; S <= 8; ++S) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, S, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = S;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          clusters = 0;
+        }
+        e.cap[S] = clusters * S;
+      }
+      if (n_cache < 32) cache[n_cache++] = e;
+      for (int S = 0; S <= 8; ++S) cap[S] = e.cap[S];
+    } else {
+      for (int S = 0; S <= 8; ++S) cap[S] = cache[found].cap[S];
+    }
+  }
+  // About one CTA per SM: a decode layer then leaves room on every SM for the next layer's CTAs,
+  // which start streaming their weights early (programmatic dependent launch).
+  const int sms = num_sms();
+  int S = sms / (units > 0 ? units : 1);
+  if (S > 8) S = 8;
+  if (S > kblocks) S = kblocks;
+  if (S < 1) S = 1;
+  while (S > 1 && units * S > cap[S]) --S;
+  return S;
 }
 
 }  // namespace wql

@@ -4,40 +4,67 @@
 // quantisation" tutorial, section 2: per-group asymmetric int4; section 5.1: the engine's fp16 x
 // int4 GEMM).  Design for GB300:
 //   * The packed weight is streamed exactly once from HBM by TMA (one producer thread), in stages
-//     of 64 k-rows x 128 output columns, together with the matching activation, scale and zero
-//     tiles.  L2 eviction hint "evict first" keeps the stream from displacing activations.
-//   * Eight consumer warps dequantise int4 -> fp16 in registers (PRMT to pair rows k and k+1,
-//     LOP3 to splice nibbles into the fp16 pattern 1024 + q, one f16x2 add or fma to subtract
-//     1024 + z exactly) and feed the legacy mma.sync.m16n8k16 tensor-core path with the weights
-//     as the 16-row operand and the tokens as the 8-column operand ("swap AB").
-//   * The per-group scale is applied once per group to fp32 partial sums, not per weight.
-//   * Split-K across the CTAs of a thread-block cluster; partial tiles are reduced through
-//     distributed shared memory in a fixed order, so results are deterministic and no global
-//     scratch is needed.
+//     of 128 k-rows x 128 output columns with the matching scale and zero-point rows.  "Evict
+//     first" L2 hints keep the stream from displacing activations.
+//   * Programmatic dependent launch: each CTA lets the next kernel in the stream launch at once
+//     and issues its weight copies before waiting for the previous kernel; only the activation
+//     copies wait.  Back-to-back layers keep HBM busy across kernel boundaries (weights never
+//     depend on the previous layer's output).  Activations arrive in chunks of 8 stages, one 3D
+//     TMA copy per chunk, into a two-chunk ring.
+//   * Eight consumer warps: two column groups of 64 outputs x four stage lanes (lane l owns every
+//     stage i with i % 4 == l, so every group is reduced by a single warp).  They feed the legacy
+//     mma.sync.m16n8k16 tensor-core path with the weights as the 16-row operand and the tokens as
+//     the 8-column operand ("swap AB").  The int4 codes enter the MMA as the exact fp16 values
+//     1024 + q (or 1024 + 16 q): one PRMT pairs rows k and k+1, one LOP3 per two weights splices
+//     the nibbles into the fp16 bit pattern.  Offset, zero point and scale are applied once per
+//     group to the fp32 partial sums:
+//         sum_k (q - z) x = D - (1024 + z) sum_k x       (D = sum_k (1024 + q) x)
+//         sum_k (q - z) x = D / 16 - (64 + z) sum_k x    (D = sum_k (1024 + 16 q) x)
+//     with sum_k x of each token taken from one extra MMA against an all-ones operand.
+//   * Split-K across the CTAs of a thread-block cluster: every consumer thread sends its partial
+//     sums straight into the owning CTA's receive buffer with st.async, which completes
+//     transaction bytes on the owner's mbarrier; owners add the partials in a fixed order.
+//     Deterministic, no global scratch, one cluster barrier (at start-up).
 #include "common.cuh"
 #include "internal.h"
 
 namespace wql {
 namespace {
 
-constexpr int kBK = 64;            // k rows per stage
+constexpr int kBK = 128;           // k rows per stage (a multiple of every group size)
 constexpr int kStripWords = 16;    // packed words per row of a CTA strip
 constexpr int kStripCols = 128;    // output columns per CTA
-constexpr int kConsumerWarps = 8;  // 2 column groups (64 columns) x 4 k16 steps
+constexpr int kLanes = 4;          // stage lanes
+constexpr int kConsumerWarps = 2 * kLanes;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kChunkStages = 8;    // activation chunk = 8 stages = 16 slabs of 64 k
+constexpr int kChunkSlabs = 2 * kChunkStages;
 
-template <int MT>
+template <int MT, int LG>
 struct Layout {
-  static constexpr int kXBytes = 8 * MT * kBK * 2;          // token rows x 64 k fp16, 128 B rows
-  static constexpr int kWBytes = kBK * kStripWords * 4;     // 64 rows x 64 B
-  static constexpr int kSBytes = 2 * kStripCols * 2;        // <= 2 group rows of 128 fp16
-  static constexpr int kZBytes = 2 * kStripWords * 4;       // <= 2 group rows of 16 words
-  static constexpr int kStage = (kXBytes + kWBytes + kSBytes + kZBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = MT >= 4 ? 6 : 8;
-  static constexpr int kPipe = kStages * kStage;
-  static constexpr int kRed = 4 * 8 * MT * kStripCols * 4;  // [4 k-steps][tokens][128] fp32
-  static constexpr int kData = kPipe > kRed ? kPipe : kRed;
-  static constexpr int kBytes = kData + 1024 + 2 * kStages * 8;
+  static constexpr int G = 1 << LG;
+  static constexpr int kGR = G >= kBK ? 1 : kBK / G;      // groups per stage
+  // Slot s of the weight ring is always served by stage lane s % 4 (so a lane can never lap another
+  // lane on a slot, which the parity-based barrier waits rely on): the depth is a multiple of 4.
+  static constexpr int kStages = 8;
+  static_assert(kStages % kLanes == 0, "weight ring depth must be a multiple of the lane count");
+  static constexpr int kWBytes = kBK * kStripWords * 4;   // 128 rows x 64 B
+  static constexpr int kSBytes = kGR * kStripCols * 2;
+  static constexpr int kZBytes = kGR * kStripWords * 4;
+  static constexpr int kStage = (kWBytes + kSBytes + kZBytes + 511) / 512 * 512;
+  static constexpr int kSlab = 8 * MT * 128;              // token rows x 64 k fp16 (128-byte rows)
+  static constexpr int kXChunk = kChunkSlabs * kSlab;
+  static constexpr int kE = 8 * MT * kStripCols;          // elements of one partial tile
+  static constexpr int kNQ = kE / 4;                      // float4s of one partial tile
+  static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
+  static constexpr uint32_t kXTx = kXChunk;
+  // shared memory map: [X ring (xr chunks, 1024-aligned)] [stages] [receive buffer] [barriers]
+  __host__ __device__ static constexpr int off_stages(int xr) { return xr * kXChunk; }
+  __host__ __device__ static constexpr int off_recv(int xr) { return off_stages(xr) + kStages * kStage; }
+  static int bytes(int S, int xr) {
+    const int lmax = (kNQ + S - 1) / S;
+    return off_recv(xr) + S * kLanes * lmax * 16 + (2 * kStages + 5) * 8 + 1024;
+  }
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -50,54 +77,68 @@ __device__ __forceinline__ uint32_t wtile_off(int r, int j) {
   return r * 64 + ((((j >> 2) ^ (r >> 1)) & 3) << 4) + (j & 3) * 4;
 }
 
-// Zero-point constants for the 8 columns of one packed zero word: even columns are extracted as
-// 1024 + q and need -(1024 + z); odd columns as 1024 + 16 q, scaled by 1/16, and need -(64 + z).
-__device__ __forceinline__ void zero_consts(uint32_t zw, uint32_t zc[8]) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t z = (zw >> (4 * c)) & 15u;
-    zc[c] = (c & 1) ? (0xD400D400u | (z << 4) | (z << 20)) : (0xE400E400u | z | (z << 16));
-  }
-}
-
-// Four f16x2 registers (q - z) for the 4 columns held in the nibbles of T, exact.
-__device__ __forceinline__ void dequant4(uint32_t T, const uint32_t* zc, uint32_t out[4]) {
-  const uint32_t kMagic = 0x64006400u, kSixteenth = 0x2C002C00u;
+// The four f16x2 MMA operands held in the nibbles of T: columns 0 and 2 as 1024 + q, columns 1 and
+// 3 as 1024 + 16 q (both exact).
+__device__ __forceinline__ void splice4(uint32_t T, uint32_t out[4]) {
+  const uint32_t kMagic = 0x64006400u;
   const uint32_t T8 = T >> 8;
-  out[0] = hadd2_u32(and_or(T, 0x000F000Fu, kMagic), zc[0]);
-  out[1] = hfma2_u32(and_or(T, 0x00F000F0u, kMagic), kSixteenth, zc[1]);
-  out[2] = hadd2_u32(and_or(T8, 0x000F000Fu, kMagic), zc[2]);
-  out[3] = hfma2_u32(and_or(T8, 0x00F000F0u, kMagic), kSixteenth, zc[3]);
+  out[0] = and_or(T, 0x000F000Fu, kMagic);
+  out[1] = and_or(T, 0x00F000F0u, kMagic);
+  out[2] = and_or(T8, 0x000F000Fu, kMagic);
+  out[3] = and_or(T8, 0x00F000F0u, kMagic);
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
-    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x [M][K] fp16, box {64, 8MT}, SW128
-                        const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 64}, SW64
+template <int MT, int LG>
+__global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
+    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x: 3D {64, M, K/64} box {64, 8MT, 16}, or
+                                                                    //    2D {K, M} box {64, 8MT} (x3d == 0)
+                        const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 128}, SW64
                         const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
-                        int M, int N, int G, int kblocks, __half* __restrict__ y, unsigned* err) {
-  using L = Layout<MT>;
+                        int M, int N, int kblocks, int x3d, int xr, __half* __restrict__ y, unsigned* err) {
+  using L = Layout<MT, LG>;
+  constexpr int G = L::G;
+  constexpr int kGR = L::kGR;
+  constexpr int kStages = L::kStages;
+  constexpr int kStepsPerGroup = (G >= kBK ? kBK : G) / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kData);
-  uint64_t* empty = full + L::kStages;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int strip = blockIdx.x;
-  const int split = blockIdx.y, nsplit = gridDim.y;
+  const int nsplit = gridDim.y;
   const int m0 = blockIdx.z * 8 * MT;
-  const int kb0 = (int)((long long)kblocks * split / nsplit);
-  const int kb1 = (int)((long long)kblocks * (split + 1) / nsplit);
-  const int GR = G >= kBK ? 1 : kBK / G;
+  const int kb0 = (int)((long long)kblocks * blockIdx.y / nsplit);
+  const int kb1 = (int)((long long)kblocks * (blockIdx.y + 1) / nsplit);
+  const int nkb = kb1 - kb0;
+  const int lmax = (L::kNQ + nsplit - 1) / nsplit;  // owner r holds float4s [r lmax, min((r+1) lmax, nq))
+  const uint32_t rank = cluster_ctarank();
+
+  const int off_stages = L::off_stages(xr);  // xr = activation ring depth (1 or 2 chunks)
+  float4* recv = reinterpret_cast<float4*>(smem + L::off_recv(xr));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::off_recv(xr) + nsplit * kLanes * lmax * 16);
+  uint64_t* empty = full + kStages;
+  uint64_t* x_full = empty + kStages;  // [2]
+  uint64_t* x_empty = x_full + 2;      // [2]
+  uint64_t* recv_full = x_empty + 2;   // [1]
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], 2);  // the two column-group warps of the stage's lane
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&x_full[b], 1);
+      mbar_init(&x_empty[b], kConsumerWarps);
+    }
+    mbar_init(recv_full, 1);
     fence_mbarrier_init();
+    const int own0 = (int)rank * lmax, own1 = own0 + lmax < L::kNQ ? own0 + lmax : L::kNQ;
+    // the owner's slice arrives from every (CTA, lane) pair as st.async transaction bytes
+    mbar_arrive_expect_tx(recv_full, (uint32_t)(nsplit * kLanes * (own1 > own0 ? own1 - own0 : 0) * 16));
+    grid_dependents_launch();  // the next kernel may start streaming its own weights now
   }
+  __syncwarp();
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
   __syncthreads();
 
   float tot[4][MT][4];
@@ -120,172 +161,233 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_s);
       tma_prefetch_desc(&tm_z);
       const uint64_t pol = policy_evict_first();
-      const uint32_t bytes = L::kXBytes + L::kWBytes + GR * (kStripCols * 2 + kStripWords * 4);
-      int issued = 0;
+      auto issue_weights = [&](int i) {
+        const int s = i % kStages, kb = kb0 + i;
+        uint8_t* st = smem + off_stages + s * L::kStage;
+        const int grow = (kb * kBK) >> LG;
+        mbar_arrive_expect_tx(&full[s], L::kWTx);
+        tma_load_2d_hint(st, &tm_qw, &full[s], strip * kStripWords, kb * kBK, pol);
+        tma_load_2d_hint(st + L::kWBytes, &tm_s, &full[s], strip * kStripCols, grow, pol);
+        tma_load_2d_hint(st + L::kWBytes + L::kSBytes, &tm_z, &full[s], strip * kStripWords, grow, pol);
+      };
+      auto issue_x = [&](int c) {
+        const int b = c & 1;
+        uint8_t* dst = smem + b * L::kXChunk;
+        const int slab0 = 2 * (kb0 + kChunkStages * c);
+        mbar_arrive_expect_tx(&x_full[b], L::kXTx);
+        if (x3d) {
+          tma_load_3d(dst, &tm_x, &x_full[b], 0, m0, slab0);
+        } else {
+          for (int q = 0; q < kChunkSlabs; ++q) tma_load_2d(dst + q * L::kSlab, &tm_x, &x_full[b], 64 * (slab0 + q), m0);
+        }
+      };
       bool ok = true;
+      int nx_issued = 0;
+      // prologue: weights first (independent of the previous kernel), then activations
+      const int pro = nkb < kStages ? nkb : kStages;
+      for (int i = 0; i < pro; ++i) issue_weights(i);
       grid_dependency_wait();  // activations may come from the preceding kernel
-      for (int kb = kb0; kb < kb1; ++kb, ++issued) {
-        const int s = issued % L::kStages;
-        const uint32_t ph = (issued / L::kStages) & 1;
-        if (issued >= L::kStages && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+      const int nxc = (nkb + kChunkStages - 1) / kChunkStages;
+      for (int c = 0; c < nxc && c < xr; ++c, ++nx_issued) issue_x(c);
+      int issued = pro;
+      for (; issued < nkb && ok; ++issued) {
+        if (issued % kChunkStages == 0 && issued / kChunkStages >= 2) {
+          const int c = issued / kChunkStages;
+          if (!mbar_wait_bounded(&x_empty[c & 1], ((c >> 1) & 1) ^ 1)) {
+            report_error(err, kErrTimeoutEmpty);
+            ok = false;
+            break;
+          }
+          issue_x(c);
+          ++nx_issued;
+        }
+        const int s = issued % kStages;
+        if (!mbar_wait_bounded(&empty[s], ((issued / kStages) & 1) ^ 1)) {
           report_error(err, kErrTimeoutEmpty);
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const int grow = kb * kBK / G;
-        tma_load_2d(st, &tm_x, &full[s], kb * kBK, m0);
-        tma_load_2d_hint(st + L::kXBytes, &tm_qw, &full[s], strip * kStripWords, kb * kBK, pol);
-        tma_load_2d(st + L::kXBytes + L::kWBytes, &tm_s, &full[s], strip * kStripCols, grow);
-        tma_load_2d(st + L::kXBytes + L::kWBytes + L::kSBytes, &tm_z, &full[s], strip * kStripWords, grow);
+        issue_weights(issued);
       }
       // Drain: every issued copy must have landed before shared memory is reused or released.
-      const int n = issued < L::kStages ? issued : L::kStages;
+      const int n = issued < kStages ? issued : kStages;
       for (int i = issued - n; i < issued; ++i) {
-        if (!mbar_wait_bounded(&full[i % L::kStages], (i / L::kStages) & 1)) {
+        if (!mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1)) {
           report_error(err, kErrTimeoutDrain);
           break;
         }
       }
-      (void)ok;
+      for (int c = nx_issued - 2 < 0 ? 0 : nx_issued - 2; c < nx_issued; ++c) {
+        if (!mbar_wait_bounded(&x_full[c & 1], (c >> 1) & 1)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+      }
     }
   } else {
-    // ---------------- consumers: dequantise + tensor-core dot products ----------------
-    float acc[4][MT][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[j][mt][i] = 0.f;
-    uint32_t zc[8];
-    float sc[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      zc[c] = 0u;
-      sc[c] = 0.f;
-    }
-    int cur_group = -1;
+    // ---------------- consumers: splice codes + tensor-core dot products ----------------
     const uint32_t sel_lo = (t & 1) ? 0x1054u : 0x5410u;
     const uint32_t sel_hi = (t & 1) ? 0x3276u : 0x7632u;
-    const int ra = 16 * kq + 2 * t + (t & 1);      // rows of this thread's k pairs, ordered so that
-    const int rb = 16 * kq + 2 * t + 1 - (t & 1);  // the four t lanes hit distinct banks
+    const uint32_t kOnes[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+    // rows 2t, 2t+1, 2t+8, 2t+9 of k16 step 0, ordered so that the four t lanes hit distinct banks;
+    // step u sits 16 rows = 1024 bytes further
+    const int ra = 2 * t + (t & 1), rb = 2 * t + 1 - (t & 1);
     const uint32_t offa = wtile_off(ra, wc), offb = wtile_off(rb, wc);
     const uint32_t offc = wtile_off(ra + 8, wc), offd = wtile_off(rb + 8, wc);
-    // ldmatrix row addresses for the activation tile (128-byte rows, 128B swizzle)
-    uint32_t xoff[(MT + 1) / 2];
+    // ldmatrix row addresses for chunk pair u2 (k16 step) within one activation slab (128-byte rows,
+    // 128B swizzle); matrices: (tokens 0-7, chunks 2u2, 2u2+1), then the next token tile
+    uint32_t xoff[4][(MT + 1) / 2];
 #pragma unroll
-    for (int p = 0; p < (MT + 1) / 2; ++p) {
-      const int mat = lane >> 3;
-      const int row = 8 * (2 * p + (mat >> 1)) + (lane & 7);
-      const int chunk = 2 * kq + (mat & 1);
-      xoff[p] = row * 128 + ((chunk ^ (row & 7)) << 4);
-    }
+    for (int u2 = 0; u2 < 4; ++u2)
+#pragma unroll
+      for (int p = 0; p < (MT + 1) / 2; ++p) {
+        const int mat = lane >> 3;
+        const int row = 8 * (2 * p + (mat >> 1)) + (lane & 7);
+        const int chunk = 2 * u2 + (mat & 1);
+        xoff[u2][p] = row * 128 + ((chunk ^ (row & 7)) << 4);
+      }
+    const uint32_t xbase = smem_u32(smem);
+    int xc_held = -1;
 
-    auto flush = [&]() {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          tot[j][mt][0] += sc[j] * acc[j][mt][0];
-          tot[j][mt][1] += sc[j] * acc[j][mt][1];
-          tot[j][mt][2] += sc[j + 4] * acc[j][mt][2];
-          tot[j][mt][3] += sc[j + 4] * acc[j][mt][3];
-          acc[j][mt][0] = acc[j][mt][1] = acc[j][mt][2] = acc[j][mt][3] = 0.f;
+    for (int i = kq; i < nkb; i += kLanes) {
+      const int c = i / kChunkStages;
+      if (c != xc_held) {
+        if (xc_held >= 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&x_empty[xc_held & 1]);
         }
-    };
-
-    int it = 0;
-    for (int kb = kb0; kb < kb1; ++kb, ++it) {
-      const int s = it % L::kStages;
-      if (!mbar_wait_bounded(&full[s], (it / L::kStages) & 1)) {
+        if (!mbar_wait_bounded(&x_full[c & 1], (c >> 1) & 1)) {
+          report_error(err, kErrTimeoutFull);
+          break;
+        }
+        xc_held = c;
+      }
+      const int s = i % kStages;
+      if (!mbar_wait_bounded(&full[s], (i / kStages) & 1)) {
         report_error(err, kErrTimeoutFull);
         break;
       }
-      const uint32_t st = smem_u32(smem + s * L::kStage);
-      const uint32_t wt = st + L::kXBytes;
-      const int k0 = kb * kBK + 16 * kq;
-      const int grp = k0 / G;
-      if (grp != cur_group) {
-        if (cur_group >= 0) flush();
-        cur_group = grp;
-        const int grow = grp - (kb * kBK) / G;
-        const uint32_t sbase = wt + L::kWBytes + grow * (kStripCols * 2);
-        const uint32_t zbase = wt + L::kWBytes + L::kSBytes + grow * (kStripWords * 4);
-        zero_consts(lds_u32(zbase + wc * 4), zc);
-        const uint4 sv = lds_u128(sbase + wc * 16);
+      const uint32_t wt = smem_u32(smem + off_stages + s * L::kStage);
+      const uint32_t sbase = wt + L::kWBytes, zbase = sbase + L::kSBytes;
+      const uint32_t xt = xbase + (c & 1) * L::kXChunk + (2 * (i - c * kChunkStages)) * L::kSlab;
+#pragma unroll
+      for (int gi = 0; gi < kGR; ++gi) {
+        float acc[4][MT][4];
+        float sx[MT][4];
+#pragma unroll
+        for (int uu = 0; uu < kStepsPerGroup; ++uu) {
+          const int u = gi * kStepsPerGroup + uu;  // k16 step within the stage (0..7)
+          const int hb = u >> 2, u2 = u & 3;       // activation slab and chunk pair
+          uint32_t bx[MT][2];
+#pragma unroll
+          for (int p = 0; p < (MT + 1) / 2; ++p) {
+            if (2 * p + 1 < MT)
+              ldmatrix_x4(xt + hb * L::kSlab + xoff[u2][p], bx[2 * p][0], bx[2 * p][1], bx[2 * p + 1][0],
+                          bx[2 * p + 1][1]);
+            else
+              ldmatrix_x2(xt + hb * L::kSlab + xoff[u2][p], bx[2 * p][0], bx[2 * p][1]);
+          }
+          const uint32_t w0 = lds_u32(wt + u * 1024 + offa), w1 = lds_u32(wt + u * 1024 + offb);
+          const uint32_t w2 = lds_u32(wt + u * 1024 + offc), w3 = lds_u32(wt + u * 1024 + offd);
+          uint32_t lo[4], hi[4], lo2[4], hi2[4];
+          splice4(prmt(w0, w1, sel_lo), lo);
+          splice4(prmt(w0, w1, sel_hi), hi);
+          splice4(prmt(w2, w3, sel_lo), lo2);
+          splice4(prmt(w2, w3, sel_hi), hi2);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a[4] = {lo[j], hi[j], lo2[j], hi2[j]};
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              if (uu == 0) acc[j][mt][0] = acc[j][mt][1] = acc[j][mt][2] = acc[j][mt][3] = 0.f;
+              mma_f16_16816(acc[j][mt], a, bx[mt][0], bx[mt][1]);
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            if (uu == 0) sx[mt][0] = sx[mt][1] = sx[mt][2] = sx[mt][3] = 0.f;
+            mma_f16_16816(sx[mt], kOnes, bx[mt][0], bx[mt][1]);
+          }
+        }
+        // group epilogue: tot += ca * acc - cb * sx per column
+        const uint32_t zw = lds_u32(zbase + gi * (kStripWords * 4) + wc * 4);
+        const uint4 sv = lds_u128(sbase + gi * (kStripCols * 2) + wc * 16);
         const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+        float ca[8], cb[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[c]));
-          sc[2 * c] = f.x;
-          sc[2 * c + 1] = f.y;
-        }
-      }
-      // activation fragments (B operand), one pair of registers per token tile
-      uint32_t bx[MT][2];
+        for (int c2 = 0; c2 < 4; ++c2) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[c2]));
 #pragma unroll
-      for (int p = 0; p < (MT + 1) / 2; ++p) {
-        if (2 * p + 1 < MT) {
-          ldmatrix_x4(st + xoff[p], bx[2 * p][0], bx[2 * p][1], bx[2 * p + 1][0], bx[2 * p + 1][1]);
-        } else {
-          ldmatrix_x2(st + xoff[p], bx[2 * p][0], bx[2 * p][1]);
+          for (int e = 0; e < 2; ++e) {
+            const int cc = 2 * c2 + e;
+            const float sc = e ? f.y : f.x;
+            // 1024 + z (even columns) or 64 + z (odd columns) built directly as fp32 bit patterns
+            const uint32_t zb = (cc & 1) ? (0x42800000u | (((zw >> (4 * cc)) & 15u) << 17))
+                                         : (0x44800000u | (((zw >> (4 * cc)) & 15u) << 13));
+            ca[cc] = (cc & 1) ? sc * 0.0625f : sc;
+            cb[cc] = sc * __uint_as_float(zb);
+          }
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = j + 4 * (e >> 1);
+              tot[j][mt][e] = fmaf(ca[cc], acc[j][mt][e], fmaf(-cb[cc], sx[mt][e & 1], tot[j][mt][e]));
+            }
       }
-      // weight fragments (A operand): rows 2t, 2t+1 and 2t+8, 2t+9 of this k16 step
-      const uint32_t w0 = lds_u32(wt + offa), w1 = lds_u32(wt + offb);
-      const uint32_t w2 = lds_u32(wt + offc), w3 = lds_u32(wt + offd);
-      uint32_t lo[4], hi[4], lo2[4], hi2[4];
-      dequant4(prmt(w0, w1, sel_lo), zc, lo);
-      dequant4(prmt(w0, w1, sel_hi), zc + 4, hi);
-      dequant4(prmt(w2, w3, sel_lo), zc, lo2);
-      dequant4(prmt(w2, w3, sel_hi), zc + 4, hi2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t a[4] = {lo[j], hi[j], lo2[j], hi2[j]};
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) mma_f16_16816(acc[j][mt], a, bx[mt][0], bx[mt][1]);
-      }
     }
-    if (cur_group >= 0) flush();
+    if (xc_held >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&x_empty[xc_held & 1]);
+    }
   }
 
-  // ---------------- reduction over the 4 k-step warps and the cluster's k splits ----------------
-  __syncthreads();  // all stages consumed and drained: the pipeline memory is free
-  float* red = reinterpret_cast<float*>(smem);
-  constexpr int kE = 8 * MT * kStripCols;  // elements of one partial tile
+  // ---------------- split-K reduction: push partials to the owners, owners add ----------------
+  __syncwarp();
+  cluster_wait();  // every peer has started: its receive buffer and barrier are initialised
   if (warp < kConsumerWarps) {
+    const uint32_t recv_base = smem_u32(recv);
+    const uint32_t bar_local = smem_u32(recv_full);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = 8 * mt + 2 * t + (i & 1);
-          const int col = 8 * wc + j + 4 * (i >> 1);
-          red[kq * kE + row * kStripCols + col] = tot[j][mt][i];
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int row = 8 * mt + 2 * t + (e & 1);
+        const int col = 8 * wc + 4 * (e >> 1);
+        const int f = (row * kStripCols + col) >> 2;
+        const int owner = f / lmax;
+        const uint32_t slot = recv_base + (uint32_t)((((int)rank * kLanes + kq) * lmax + (f - owner * lmax)) * 16);
+        uint32_t raddr, rbar;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(slot), "r"(owner));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_local), "r"(owner));
+        st_async_f4(raddr, make_float4(tot[0][mt][e], tot[1][mt][e], tot[2][mt][e], tot[3][mt][e]), rbar);
+      }
   }
-  cluster_sync();
-  {
-    const uint32_t rank = cluster_ctarank();
-    const int nq = kE / 4;
-    const int f0 = (int)((long long)nq * rank / nsplit), f1 = (int)((long long)nq * (rank + 1) / nsplit);
+  const bool received = mbar_wait_bounded(recv_full, 0);
+  if (!received) report_error(err, kErrTimeoutMma);
+  // Second cluster phase: a CTA arrives once its own slice is complete and waits for every peer
+  // before exiting, so no CTA leaves while st.async stores it issued may still be in flight.
+  __syncwarp();
+  cluster_arrive_release();
+  if (received) {
+    const int f0 = (int)rank * lmax;
+    const int f1 = f0 + lmax < L::kNQ ? f0 + lmax : L::kNQ;
     for (int f = f0 + threadIdx.x; f < f1; f += kThreads) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < nsplit; ++q) {
+      for (int q = 0; q < nsplit; ++q)
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float4 p = ld_cluster_f4(map_cluster(red + w * kE + 4 * f, q));
+        for (int l = 0; l < kLanes; ++l) {
+          const float4 p = recv[(q * kLanes + l) * lmax + (f - f0)];
           v.x += p.x;
           v.y += p.y;
           v.z += p.z;
           v.w += p.w;
         }
-      }
       const int row = (4 * f) / kStripCols, col = (4 * f) % kStripCols;
       const int m = m0 + row, n = strip * kStripCols + col;
       if (m < M && n < N) {
@@ -297,48 +399,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  cluster_sync();  // keep this CTA's partial tile alive until every peer has read it
+  __syncwarp();
+  cluster_wait();
 }
 
-template <int MT>
-cudaError_t launch_mt(const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts,
-                      const CUtensorMap& tz, int M, int N, int G, int kblocks, __half* y, unsigned* dev_err,
+template <int MT, int LG>
+cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, const CUtensorMap& ts,
+                      const CUtensorMap& tz, int M, int N, int kblocks, __half* y, unsigned* dev_err,
                       cudaStream_t stream) {
-  using L = Layout<MT>;
+  using L = Layout<MT, LG>;
+  auto kern = w4a16_decode_kernel<MT, LG>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
+  int max_bytes = 0;  // the receive buffer size depends on the cluster size
+  for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S, 2) > max_bytes ? L::bytes(S, 2) : max_bytes;
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w4a16_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int strips = (N + kStripCols - 1) / kStripCols;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
-  const int target = 2 * num_sms();
-  int S = (target + strips * mblocks - 1) / (strips * mblocks);
-  if (S > 8) S = 8;
-  if (S > kblocks) S = kblocks;
-  if (S < 1) S = 1;
+  const int S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, max_bytes, strips * mblocks, kblocks);
+
+  // activation ring depth: one chunk of 8 stages suffices when no CTA gets more than 8 stages
+  const int nkb_max = (kblocks + S - 1) / S;
+  const int xr = nkb_max > kChunkStages ? 2 : 1;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.dynamicSmemBytes = L::bytes(S, xr);
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
-  int na = 0;
-  attrs[na].id = cudaLaunchAttributeClusterDimension;
-  attrs[na].val.clusterDim.x = 1;
-  attrs[na].val.clusterDim.y = S;
-  attrs[na].val.clusterDim.z = 1;
-  ++na;
-  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = S;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, w4a16_decode_kernel<MT>, tx, tq, ts, tz, M, N, G, kblocks, y, dev_err);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, kblocks, x3d, xr, y, dev_err);
+}
+
+template <int MT>
+cudaError_t launch_g(int group, const CUtensorMap& tx, int x3d, const CUtensorMap& tq, const CUtensorMap& ts,
+                     const CUtensorMap& tz, int M, int N, int kblocks, __half* y, unsigned* dev_err, cudaStream_t s) {
+  switch (group) {
+    case 32:
+      return launch_mt<MT, 5>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+    case 64:
+      return launch_mt<MT, 6>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+    default:
+      return launch_mt<MT, 7>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+  }
 }
 
 }  // namespace
@@ -346,11 +462,17 @@ cudaError_t launch_mt(const CUtensorMap& tx, const CUtensorMap& tq, const CUtens
 cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
                                 unsigned* dev_err, cudaStream_t stream, std::string* err) {
-  const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+  const int MT = M <= 8 ? 1 : 2;  // larger M runs as several 16-token blocks
   const int GR = group >= kBK ? 1 : kBK / group;
   CUtensorMap tx, tq, ts, tz;
-  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, kBK, 8 * MT,
-                    CU_TENSOR_MAP_SWIZZLE_128B, err) ||
+  // Activations: 64-k slabs of 8 MT token rows, 128-byte rows with the 128B swizzle.  With K a
+  // multiple of 64, one 3D copy fetches 16 slabs; otherwise one 2D copy per slab.
+  const int x3d = (K % 64 == 0) ? 1 : 0;
+  const bool okx = x3d ? make_tmap_3d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, 64, M, K / 64, (uint64_t)K * 2, 128, 64,
+                                      8 * MT, kChunkSlabs, CU_TENSOR_MAP_SWIZZLE_128B, err)
+                       : make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, 8 * MT,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, err);
+  if (!okx ||
       !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords, kBK,
                     CU_TENSOR_MAP_SWIZZLE_64B, err) ||
       !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / group, (uint64_t)N * 2, kStripCols, GR,
@@ -361,14 +483,8 @@ cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, cons
   }
   const int kblocks = (K + kBK - 1) / kBK;
   __half* yh = reinterpret_cast<__half*>(y);
-  switch (MT) {
-    case 1:
-      return launch_mt<1>(tx, tq, ts, tz, M, N, group, kblocks, yh, dev_err, stream);
-    case 2:
-      return launch_mt<2>(tx, tq, ts, tz, M, N, group, kblocks, yh, dev_err, stream);
-    default:
-      return launch_mt<4>(tx, tq, ts, tz, M, N, group, kblocks, yh, dev_err, stream);
-  }
+  if (MT == 1) return launch_g<1>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, dev_err, stream);
+  return launch_g<2>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, dev_err, stream);
 }
 
 }  // namespace wql

@@ -23,6 +23,7 @@ constexpr int kBK = 64;            // k per stage (bytes of a weight row)
 constexpr int kRows = 128;         // output channels per CTA
 constexpr int kConsumerWarps = 8;  // 4 tile pairs x 2 k16 phases
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxCluster = 8;
 constexpr int kFoldStages = 32;    // each warp sees 32 k per stage: fold to int32 every 1024 k
 
 template <int MT>
@@ -34,7 +35,8 @@ struct Layout8 {
   static constexpr int kPipe = kStages * kStage;
   static constexpr int kRed = 2 * 8 * MT * kRows * 4;  // [2 k phases][tokens][128] int32
   static constexpr int kData = kPipe > kRed ? kPipe : kRed;
-  static constexpr int kBytes = kData + 1024 + 2 * kStages * 8;
+  static constexpr int kRecv = (8 * MT * kRows / 4 + kMaxCluster) * 16;  // owner's receive slots, dedicated
+  static constexpr int kBytes = kData + kRecv + 1024 + 2 * kStages * 8;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -54,7 +56,7 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t v, uint32_t& lo, uint32_t&
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
     w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] int8, box {64, 8MT}, SW64
                        const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] int8, box {64, 128}, SW64
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int kblocks,
@@ -62,7 +64,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout8<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kData);
+  int4* recv = reinterpret_cast<int4*>(smem + L::kData);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kData + L::kRecv);
   uint64_t* empty = full + L::kStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -78,7 +81,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_mbarrier_init();
+    grid_dependents_launch();  // the next kernel may start streaming its own weights now
   }
+  __syncwarp();
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
   __syncthreads();
 
   const int g = lane >> 2, t = lane & 3;
@@ -97,19 +103,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol = policy_evict_first();
       const uint32_t bytes = L::kXBytes + L::kWBytes;
-      int issued = 0;
+      const int nkb = kb1 - kb0;
+      // prologue: weight tiles first (independent of the previous kernel), activations after the
+      // programmatic dependency resolves
+      const int pro = nkb < L::kStages ? nkb : L::kStages;
+      for (int i = 0; i < pro; ++i) {
+        mbar_arrive_expect_tx(&full[i], bytes);
+        tma_load_2d_hint(smem + i * L::kStage + L::kXBytes, &tm_w, &full[i], (kb0 + i) * kBK, strip * kRows, pol);
+      }
       grid_dependency_wait();
-      for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+      for (int i = 0; i < pro; ++i) tma_load_2d(smem + i * L::kStage, &tm_x, &full[i], (kb0 + i) * kBK, m0);
+      int issued = pro;
+      for (; issued < nkb; ++issued) {
         const int s = issued % L::kStages;
-        const uint32_t ph = (issued / L::kStages) & 1;
-        if (issued >= L::kStages && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+        const int kb = kb0 + issued;
+        if (!mbar_wait_bounded(&empty[s], ((issued / L::kStages) & 1) ^ 1)) {
           report_error(err, kErrTimeoutEmpty);
           break;
         }
         uint8_t* st = smem + s * L::kStage;
         mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d(st, &tm_x, &full[s], kb * kBK, m0);
         tma_load_2d_hint(st + L::kXBytes, &tm_w, &full[s], kb * kBK, strip * kRows, pol);
+        tma_load_2d(st, &tm_x, &full[s], kb * kBK, m0);
       }
       const int n = issued < L::kStages ? issued : L::kStages;
       for (int i = issued - n; i < issued; ++i) {
@@ -187,22 +202,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           red[kp * kE + row * kRows + col] = tot[a][mt][i];
         }
   }
-  cluster_sync();
+  __syncthreads();
+  __syncwarp();
+  cluster_wait();  // every peer has started: its receive buffer may be written
+  const uint32_t rank = cluster_ctarank();
+  const int nq = kE / 4;
+  const int lmax = (nq + nsplit - 1) / nsplit;
+  {  // fold the two k-phase partials and push each slice to its owner
+    const int4* r4 = reinterpret_cast<const int4*>(red);
+    for (int f = threadIdx.x; f < nq; f += kThreads) {
+      const int4 a = r4[f], b = r4[nq + f];
+      const int owner = slice_owner(f, nq, nsplit);
+      const int f0 = (int)((long long)nq * owner / nsplit);
+      st_cluster_i4(map_cluster(recv + rank * lmax + (f - f0), owner), make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // all slices delivered
   {
-    const uint32_t rank = cluster_ctarank();
-    const int nq = kE / 4;
     const int f0 = (int)((long long)nq * rank / nsplit), f1 = (int)((long long)nq * (rank + 1) / nsplit);
     for (int f = f0 + threadIdx.x; f < f1; f += kThreads) {
-      int4 v = make_int4(0, 0, 0, 0);
-      for (int q = 0; q < nsplit; ++q) {
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          const int4 u = ld_cluster_i4(map_cluster(red + p * kE + 4 * f, q));
-          v.x += u.x;
-          v.y += u.y;
-          v.z += u.z;
-          v.w += u.w;
-        }
+      int4 v = recv[f - f0];
+      for (int q = 1; q < nsplit; ++q) {
+        const int4 p = recv[q * lmax + (f - f0)];
+        v.x += p.x;
+        v.y += p.y;
+        v.z += p.z;
+        v.w += p.w;
       }
       const int row = (4 * f) / kRows, col = (4 * f) % kRows;
       const int m = m0 + row, n = strip * kRows + col;
@@ -219,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  cluster_sync();
 }
 
 template <int MT>
@@ -236,11 +261,7 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   }
   const int strips = (N + kRows - 1) / kRows;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
-  const int target = 2 * num_sms();
-  int S = (target + strips * mblocks - 1) / (strips * mblocks);
-  if (S > 8) S = 8;
-  if (S > kblocks) S = kblocks;
-  if (S < 1) S = 1;
+  const int S = pick_k_split(reinterpret_cast<const void*>(w8a8_decode_kernel<MT>), kThreads, L::kBytes, strips * mblocks, kblocks);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
   cfg.blockDim = dim3(kThreads, 1, 1);
