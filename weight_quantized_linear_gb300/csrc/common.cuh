@@ -196,6 +196,13 @@ __device__ __forceinline__ int slice_owner(int f, int nq, int parts) {
   return r;
 }
 
+// shared::cta address -> the same offset in CTA `rank` of this cluster (shared::cluster window).
+__device__ __forceinline__ uint32_t map_cluster_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr), "r"(rank));
+  return out;
+}
+
 // Address of the same shared-memory variable in CTA `rank` of this cluster (shared::cluster).
 __device__ __forceinline__ uint32_t map_cluster(const void* p, uint32_t rank) {
   uint32_t out;
@@ -219,6 +226,11 @@ __device__ __forceinline__ int4 ld_cluster_i4(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+// Named barrier over `count` threads (a multiple of 32) of this CTA; id 0 is __syncthreads.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------

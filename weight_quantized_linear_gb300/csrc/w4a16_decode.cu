@@ -4,13 +4,12 @@
 // quantisation" tutorial, section 2: per-group asymmetric int4; section 5.1: the engine's fp16 x
 // int4 GEMM).  Design for GB300:
 //   * The packed weight is streamed exactly once from HBM by TMA (one producer thread), in stages
-//     of 128 k-rows x 128 output columns with the matching scale and zero-point rows.  "Evict
-//     first" L2 hints keep the stream from displacing activations.
+//     of 128 k-rows x 128 output columns with the matching scale and zero-point rows and the
+//     stage's activation slab (one 3D copy).  "Evict first" L2 hints on the weight stream.
 //   * Programmatic dependent launch: each CTA lets the next kernel in the stream launch at once
 //     and issues its weight copies before waiting for the previous kernel; only the activation
 //     copies wait.  Back-to-back layers keep HBM busy across kernel boundaries (weights never
-//     depend on the previous layer's output).  Activations arrive in chunks of 8 stages, one 3D
-//     TMA copy per chunk, into a two-chunk ring.
+//     depend on the previous layer's output).
 //   * Eight consumer warps: two column groups of 64 outputs x four stage lanes (lane l owns every
 //     stage i with i % 4 == l, so every group is reduced by a single warp).  They feed the legacy
 //     mma.sync.m16n8k16 tensor-core path with the weights as the 16-row operand and the tokens as
@@ -24,7 +23,9 @@
 //   * Split-K across the CTAs of a thread-block cluster: every consumer thread sends its partial
 //     sums straight into the owning CTA's receive buffer with st.async, which completes
 //     transaction bytes on the owner's mbarrier; owners add the partials in a fixed order.
-//     Deterministic, no global scratch, one cluster barrier (at start-up).
+//     Deterministic and free of global scratch.  Cluster barrier phase 0 (arrive at start, wait
+//     before the first remote store) guarantees every peer is initialised; phase 1 (arrive once
+//     the own slice is complete, wait before exit) keeps every CTA alive until all stores landed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,33 +38,29 @@ constexpr int kStripCols = 128;    // output columns per CTA
 constexpr int kLanes = 4;          // stage lanes
 constexpr int kConsumerWarps = 2 * kLanes;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kChunkStages = 8;    // activation chunk = 8 stages = 16 slabs of 64 k
-constexpr int kChunkSlabs = 2 * kChunkStages;
 
 template <int MT, int LG>
 struct Layout {
   static constexpr int G = 1 << LG;
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;      // groups per stage
-  // Slot s of the weight ring is always served by stage lane s % 4 (so a lane can never lap another
-  // lane on a slot, which the parity-based barrier waits rely on): the depth is a multiple of 4.
+  // Slot s of the ring is always served by stage lane s % 4, so a lane can never lap another lane
+  // on a slot (the parity-based barrier waits rely on it): the depth is a multiple of 4.
   static constexpr int kStages = 8;
-  static_assert(kStages % kLanes == 0, "weight ring depth must be a multiple of the lane count");
+  static_assert(kStages % kLanes == 0, "ring depth must be a multiple of the lane count");
+  static constexpr int kSlab = 8 * MT * 128;              // token rows x 64 k fp16 (128-byte rows)
+  static constexpr int kXBytes = 2 * kSlab;               // two 64-k slabs per stage
   static constexpr int kWBytes = kBK * kStripWords * 4;   // 128 rows x 64 B
   static constexpr int kSBytes = kGR * kStripCols * 2;
   static constexpr int kZBytes = kGR * kStripWords * 4;
-  static constexpr int kStage = (kWBytes + kSBytes + kZBytes + 511) / 512 * 512;
-  static constexpr int kSlab = 8 * MT * 128;              // token rows x 64 k fp16 (128-byte rows)
-  static constexpr int kXChunk = kChunkSlabs * kSlab;
+  static constexpr int kStage = (kXBytes + kWBytes + kSBytes + kZBytes + 1023) / 1024 * 1024;
   static constexpr int kE = 8 * MT * kStripCols;          // elements of one partial tile
   static constexpr int kNQ = kE / 4;                      // float4s of one partial tile
-  static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
-  static constexpr uint32_t kXTx = kXChunk;
-  // shared memory map: [X ring (xr chunks, 1024-aligned)] [stages] [receive buffer] [barriers]
-  __host__ __device__ static constexpr int off_stages(int xr) { return xr * kXChunk; }
-  __host__ __device__ static constexpr int off_recv(int xr) { return off_stages(xr) + kStages * kStage; }
-  static int bytes(int S, int xr) {
+  static constexpr uint32_t kTx = kXBytes + kWBytes + kSBytes + kZBytes;
+  // shared memory map: [stages (1024-aligned)] [receive buffer] [barriers]
+  static constexpr int kOffRecv = kStages * kStage;
+  static int bytes(int S) {
     const int lmax = (kNQ + S - 1) / S;
-    return off_recv(xr) + S * kLanes * lmax * 16 + (2 * kStages + 5) * 8 + 1024;
+    return kOffRecv + S * lmax * 16 + (2 * kStages + 1) * 8 + 1024;
   }
 };
 
@@ -90,12 +87,12 @@ __device__ __forceinline__ void splice4(uint32_t T, uint32_t out[4]) {
 
 template <int MT, int LG>
 __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
-    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x: 3D {64, M, K/64} box {64, 8MT, 16}, or
+    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x: 3D {64, M, K/64} box {64, 8MT, 2}, or
                                                                     //    2D {K, M} box {64, 8MT} (x3d == 0)
                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 128}, SW64
                         const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
-                        int M, int N, int kblocks, int x3d, int xr, __half* __restrict__ y, unsigned* err) {
+                        int M, int N, int kblocks, int x3d, __half* __restrict__ y, unsigned* err) {
   using L = Layout<MT, LG>;
   constexpr int G = L::G;
   constexpr int kGR = L::kGR;
@@ -113,41 +110,26 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
   const int lmax = (L::kNQ + nsplit - 1) / nsplit;  // owner r holds float4s [r lmax, min((r+1) lmax, nq))
   const uint32_t rank = cluster_ctarank();
 
-  const int off_stages = L::off_stages(xr);  // xr = activation ring depth (1 or 2 chunks)
-  float4* recv = reinterpret_cast<float4*>(smem + L::off_recv(xr));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::off_recv(xr) + nsplit * kLanes * lmax * 16);
+  float4* recv = reinterpret_cast<float4*>(smem + L::kOffRecv);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffRecv + nsplit * lmax * 16);
   uint64_t* empty = full + kStages;
-  uint64_t* x_full = empty + kStages;  // [2]
-  uint64_t* x_empty = x_full + 2;      // [2]
-  uint64_t* recv_full = x_empty + 2;   // [1]
+  uint64_t* recv_full = empty + kStages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // the two column-group warps of the stage's lane
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&x_full[b], 1);
-      mbar_init(&x_empty[b], kConsumerWarps);
+      mbar_init(&empty[s], 2);  // the two column-group warps of the slot's lane
     }
     mbar_init(recv_full, 1);
     fence_mbarrier_init();
     const int own0 = (int)rank * lmax, own1 = own0 + lmax < L::kNQ ? own0 + lmax : L::kNQ;
-    // the owner's slice arrives from every (CTA, lane) pair as st.async transaction bytes
-    mbar_arrive_expect_tx(recv_full, (uint32_t)(nsplit * kLanes * (own1 > own0 ? own1 - own0 : 0) * 16));
+    // the owner's slice arrives once from every CTA of the cluster as st.async transaction bytes
+    mbar_arrive_expect_tx(recv_full, (uint32_t)(nsplit * (own1 > own0 ? own1 - own0 : 0) * 16));
     grid_dependents_launch();  // the next kernel may start streaming its own weights now
   }
   __syncwarp();
-  cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
+  cluster_arrive_relaxed();  // phase 0: this CTA's receive buffer and barriers are initialised
   __syncthreads();
-
-  float tot[4][MT][4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tot[j][mt][i] = 0.f;
 
   const int cg = warp & 1, kq = warp >> 1;
   const int g = lane >> 2, t = lane & 3;
@@ -163,51 +145,37 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
       const uint64_t pol = policy_evict_first();
       auto issue_weights = [&](int i) {
         const int s = i % kStages, kb = kb0 + i;
-        uint8_t* st = smem + off_stages + s * L::kStage;
+        uint8_t* st = smem + s * L::kStage + L::kXBytes;
         const int grow = (kb * kBK) >> LG;
-        mbar_arrive_expect_tx(&full[s], L::kWTx);
+        mbar_arrive_expect_tx(&full[s], L::kTx);
         tma_load_2d_hint(st, &tm_qw, &full[s], strip * kStripWords, kb * kBK, pol);
         tma_load_2d_hint(st + L::kWBytes, &tm_s, &full[s], strip * kStripCols, grow, pol);
         tma_load_2d_hint(st + L::kWBytes + L::kSBytes, &tm_z, &full[s], strip * kStripWords, grow, pol);
       };
-      auto issue_x = [&](int c) {
-        const int b = c & 1;
-        uint8_t* dst = smem + b * L::kXChunk;
-        const int slab0 = 2 * (kb0 + kChunkStages * c);
-        mbar_arrive_expect_tx(&x_full[b], L::kXTx);
+      auto issue_x = [&](int i) {
+        const int s = i % kStages, kb = kb0 + i;
+        uint8_t* st = smem + s * L::kStage;
         if (x3d) {
-          tma_load_3d(dst, &tm_x, &x_full[b], 0, m0, slab0);
+          tma_load_3d(st, &tm_x, &full[s], 0, m0, 2 * kb);
         } else {
-          for (int q = 0; q < kChunkSlabs; ++q) tma_load_2d(dst + q * L::kSlab, &tm_x, &x_full[b], 64 * (slab0 + q), m0);
+          tma_load_2d(st, &tm_x, &full[s], kb * kBK, m0);
+          tma_load_2d(st + L::kSlab, &tm_x, &full[s], kb * kBK + 64, m0);
         }
       };
-      bool ok = true;
-      int nx_issued = 0;
       // prologue: weights first (independent of the previous kernel), then activations
       const int pro = nkb < kStages ? nkb : kStages;
       for (int i = 0; i < pro; ++i) issue_weights(i);
       grid_dependency_wait();  // activations may come from the preceding kernel
-      const int nxc = (nkb + kChunkStages - 1) / kChunkStages;
-      for (int c = 0; c < nxc && c < xr; ++c, ++nx_issued) issue_x(c);
+      for (int i = 0; i < pro; ++i) issue_x(i);
       int issued = pro;
-      for (; issued < nkb && ok; ++issued) {
-        if (issued % kChunkStages == 0 && issued / kChunkStages >= 2) {
-          const int c = issued / kChunkStages;
-          if (!mbar_wait_bounded(&x_empty[c & 1], ((c >> 1) & 1) ^ 1)) {
-            report_error(err, kErrTimeoutEmpty);
-            ok = false;
-            break;
-          }
-          issue_x(c);
-          ++nx_issued;
-        }
+      for (; issued < nkb; ++issued) {
         const int s = issued % kStages;
         if (!mbar_wait_bounded(&empty[s], ((issued / kStages) & 1) ^ 1)) {
           report_error(err, kErrTimeoutEmpty);
-          ok = false;
           break;
         }
         issue_weights(issued);
+        issue_x(issued);
       }
       // Drain: every issued copy must have landed before shared memory is reused or released.
       const int n = issued < kStages ? issued : kStages;
@@ -217,15 +185,19 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
           break;
         }
       }
-      for (int c = nx_issued - 2 < 0 ? 0 : nx_issued - 2; c < nx_issued; ++c) {
-        if (!mbar_wait_bounded(&x_full[c & 1], (c >> 1) & 1)) {
-          report_error(err, kErrTimeoutDrain);
-          break;
-        }
-      }
     }
+    __syncwarp();
+    cluster_wait();  // phase 0
   } else {
     // ---------------- consumers: splice codes + tensor-core dot products ----------------
+    cluster_wait();  // phase 0, while the first activations are still in flight
+    float tot[4][MT][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[j][mt][i] = 0.f;
     const uint32_t sel_lo = (t & 1) ? 0x1054u : 0x5410u;
     const uint32_t sel_hi = (t & 1) ? 0x3276u : 0x7632u;
     const uint32_t kOnes[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
@@ -246,30 +218,16 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
         const int chunk = 2 * u2 + (mat & 1);
         xoff[u2][p] = row * 128 + ((chunk ^ (row & 7)) << 4);
       }
-    const uint32_t xbase = smem_u32(smem);
-    int xc_held = -1;
 
     for (int i = kq; i < nkb; i += kLanes) {
-      const int c = i / kChunkStages;
-      if (c != xc_held) {
-        if (xc_held >= 0) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&x_empty[xc_held & 1]);
-        }
-        if (!mbar_wait_bounded(&x_full[c & 1], (c >> 1) & 1)) {
-          report_error(err, kErrTimeoutFull);
-          break;
-        }
-        xc_held = c;
-      }
       const int s = i % kStages;
       if (!mbar_wait_bounded(&full[s], (i / kStages) & 1)) {
         report_error(err, kErrTimeoutFull);
         break;
       }
-      const uint32_t wt = smem_u32(smem + off_stages + s * L::kStage);
+      const uint32_t xt = smem_u32(smem + s * L::kStage);
+      const uint32_t wt = xt + L::kXBytes;
       const uint32_t sbase = wt + L::kWBytes, zbase = sbase + L::kSBytes;
-      const uint32_t xt = xbase + (c & 1) * L::kXChunk + (2 * (i - c * kChunkStages)) * L::kSlab;
 #pragma unroll
       for (int gi = 0; gi < kGR; ++gi) {
         float acc[4][MT][4];
@@ -341,53 +299,54 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (xc_held >= 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&x_empty[xc_held & 1]);
-    }
-  }
 
-  // ---------------- split-K reduction: push partials to the owners, owners add ----------------
-  __syncwarp();
-  cluster_wait();  // every peer has started: its receive buffer and barrier are initialised
-  if (warp < kConsumerWarps) {
-    const uint32_t recv_base = smem_u32(recv);
-    const uint32_t bar_local = smem_u32(recv_full);
+    // Fold the four lanes' partials in shared memory first.  Once all consumer warps pass this
+    // named barrier every stage has been consumed and every issued copy has landed (each one was
+    // waited for by its lane), so the pipeline memory is free for staging.
+    named_barrier_sync(1, kConsumerWarps * 32);
+    float4* stage4 = reinterpret_cast<float4*>(smem);  // [lane][float4 index]
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = 8 * mt + 2 * t + (e & 1);
         const int col = 8 * wc + 4 * (e >> 1);
-        const int f = (row * kStripCols + col) >> 2;
-        const int owner = f / lmax;
-        const uint32_t slot = recv_base + (uint32_t)((((int)rank * kLanes + kq) * lmax + (f - owner * lmax)) * 16);
-        uint32_t raddr, rbar;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(slot), "r"(owner));
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_local), "r"(owner));
-        st_async_f4(raddr, make_float4(tot[0][mt][e], tot[1][mt][e], tot[2][mt][e], tot[3][mt][e]), rbar);
+        stage4[kq * L::kNQ + ((row * kStripCols + col) >> 2)] =
+            make_float4(tot[0][mt][e], tot[1][mt][e], tot[2][mt][e], tot[3][mt][e]);
       }
+    named_barrier_sync(1, kConsumerWarps * 32);
+    // split-K: send each folded float4 to its owner CTA
+    const uint32_t recv_base = smem_u32(recv);
+    const uint32_t bar_local = smem_u32(recv_full);
+    for (int f = threadIdx.x; f < L::kNQ; f += kConsumerWarps * 32) {
+      const float4 a = stage4[f], b = stage4[L::kNQ + f], c = stage4[2 * L::kNQ + f], d = stage4[3 * L::kNQ + f];
+      const float4 v = make_float4(((a.x + b.x) + c.x) + d.x, ((a.y + b.y) + c.y) + d.y, ((a.z + b.z) + c.z) + d.z,
+                                   ((a.w + b.w) + c.w) + d.w);
+      const int owner = f / lmax;
+      const uint32_t slot = recv_base + (uint32_t)(((int)rank * lmax + (f - owner * lmax)) * 16);
+      st_async_f4(map_cluster_addr(slot, owner), v, map_cluster_addr(bar_local, owner));
+    }
   }
+
+  // ---------------- owners: add the partials of their slice in a fixed order ----------------
   const bool received = mbar_wait_bounded(recv_full, 0);
   if (!received) report_error(err, kErrTimeoutMma);
-  // Second cluster phase: a CTA arrives once its own slice is complete and waits for every peer
-  // before exiting, so no CTA leaves while st.async stores it issued may still be in flight.
   __syncwarp();
-  cluster_arrive_release();
+  // phase 1: this CTA's slice is complete (an execution barrier only: the receive barrier has
+  // already ordered the data, so no release fence is needed)
+  cluster_arrive_relaxed();
   if (received) {
     const int f0 = (int)rank * lmax;
     const int f1 = f0 + lmax < L::kNQ ? f0 + lmax : L::kNQ;
     for (int f = f0 + threadIdx.x; f < f1; f += kThreads) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < nsplit; ++q)
-#pragma unroll
-        for (int l = 0; l < kLanes; ++l) {
-          const float4 p = recv[(q * kLanes + l) * lmax + (f - f0)];
-          v.x += p.x;
-          v.y += p.y;
-          v.z += p.z;
-          v.w += p.w;
-        }
+      float4 v = recv[f - f0];
+      for (int q = 1; q < nsplit; ++q) {
+        const float4 p = recv[q * lmax + (f - f0)];
+        v.x += p.x;
+        v.y += p.y;
+        v.z += p.z;
+        v.w += p.w;
+      }
       const int row = (4 * f) / kStripCols, col = (4 * f) % kStripCols;
       const int m = m0 + row, n = strip * kStripCols + col;
       if (m < M && n < N) {
@@ -400,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
     }
   }
   __syncwarp();
-  cluster_wait();
+  cluster_wait();  // phase 1: no CTA exits before every slice in the cluster is complete
 }
 
 template <int MT, int LG>
@@ -413,7 +372,7 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   int dev = 0;
   cudaGetDevice(&dev);
   int max_bytes = 0;  // the receive buffer size depends on the cluster size
-  for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S, 2) > max_bytes ? L::bytes(S, 2) : max_bytes;
+  for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S) > max_bytes ? L::bytes(S) : max_bytes;
   if (dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
     if (e != cudaSuccess) return e;
@@ -423,14 +382,10 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
   const int S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, max_bytes, strips * mblocks, kblocks);
 
-  // activation ring depth: one chunk of 8 stages suffices when no CTA gets more than 8 stages
-  const int nkb_max = (kblocks + S - 1) / S;
-  const int xr = nkb_max > kChunkStages ? 2 : 1;
-
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::bytes(S, xr);
+  cfg.dynamicSmemBytes = L::bytes(S);
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -441,7 +396,7 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, kblocks, x3d, xr, y, dev_err);
+  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, kblocks, x3d, y, dev_err);
 }
 
 template <int MT>
@@ -466,10 +421,10 @@ cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, cons
   const int GR = group >= kBK ? 1 : kBK / group;
   CUtensorMap tx, tq, ts, tz;
   // Activations: 64-k slabs of 8 MT token rows, 128-byte rows with the 128B swizzle.  With K a
-  // multiple of 64, one 3D copy fetches 16 slabs; otherwise one 2D copy per slab.
+  // multiple of 64, one 3D copy fetches both slabs of a stage; otherwise one 2D copy per slab.
   const int x3d = (K % 64 == 0) ? 1 : 0;
   const bool okx = x3d ? make_tmap_3d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, 64, M, K / 64, (uint64_t)K * 2, 128, 64,
-                                      8 * MT, kChunkSlabs, CU_TENSOR_MAP_SWIZZLE_128B, err)
+                                      8 * MT, 2, CU_TENSOR_MAP_SWIZZLE_128B, err)
                        : make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, 8 * MT,
                                       CU_TENSOR_MAP_SWIZZLE_128B, err);
   if (!okx ||
