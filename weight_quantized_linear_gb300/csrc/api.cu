@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points declared in include/wql.h: argument validation, kernel
 // selection by shape, launch-error reporting and the per-device error word of bounded waits.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -127,8 +128,14 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
   WQL_REQUIRE_PTR(y);
   unsigned* dev_err = device_error_word();
   std::string err;
-  cudaError_t e = wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
-                                           static_cast<cudaStream_t>(stream), &err);
+  const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode" or "prefill"
+  const bool prefill = force && strcmp(force, "decode") == 0   ? false
+                       : force && strcmp(force, "prefill") == 0 ? true
+                                                                : M >= wql::kW4A16PrefillMinM;
+  cudaError_t e = prefill ? wql::launch_w4a16_prefill(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
+                                                      static_cast<cudaStream_t>(stream), &err)
+                          : wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
+                                                     static_cast<cudaStream_t>(stream), &err);
   if (!err.empty()) return fail(WQL_ECUDA, "wql_w4a16_gemm: " + err);
   return cuda_status(e, "wql_w4a16_gemm");
 }

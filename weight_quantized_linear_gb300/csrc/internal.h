@@ -36,6 +36,13 @@ cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, cons
                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
                                 unsigned* dev_err, cudaStream_t s, std::string* err);
 
+cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                 unsigned* dev_err, cudaStream_t s, std::string* err);
+
+// Token count from which w4a16_gemm uses the tcgen05 kernel instead of the streaming decode kernel.
+constexpr int kW4A16PrefillMinM = 17;
+
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                                      int8_t* q, float* xs, cudaStream_t s);
 

@@ -1,0 +1,337 @@
+// w4a16_prefill.cu -- AWQ W4A16 GEMM for prefill-shaped calls on the tcgen05 tensor cores.
+//
+// y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n] ("LMDeploy ... INT4 quantisation"
+// tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  A persistent kernel, one
+// CTA per SM, tiles of 128 output channels x BN tokens, K walked in blocks of 64:
+//   * warp 0, one thread: TMA copies of the activation tile (K-major, 128B swizzle), the packed
+//     weight tile, and its scale / zero-point rows into a ring of stages;
+//   * warps 2-9: dequantise the packed tile straight into the MMA's A operand: each packed word
+//     (8 output channels at one k) becomes one 16-byte chunk of fp16 (q - z) * s (exact q - z via
+//     the 1024 + q bit-splice trick, one rounding for the scale) in an MN-major 128B-swizzled layout;
+//   * warp 1: allocates TMEM; one thread issues tcgen05.mma.kind::f16 (M = 128 channels,
+//     N = BN tokens, K = 16) into a double-buffered fp32 accumulator and commits stage releases;
+//   * warps 10-13: tcgen05.ld the accumulator (lane = channel, column = token), round to fp16, store.
+// Swapping A and B puts the dequantised weights (not the activations) in the 128-row operand, so
+// the converter writes 128 x 64 fp16 per stage whatever the token count.
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace wql {
+namespace {
+
+constexpr int kBK = 64;          // k per stage
+constexpr int kBM = 128;         // output channels per tile (MMA M)
+constexpr int kStripWords = 16;  // packed words per tile row
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kDqWarp0 = 2, kDqWarps = 8, kEpiWarp0 = 10, kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+
+template <int BN, int LG>
+struct PLayout {
+  static constexpr int G = 1 << LG;
+  static constexpr int kGR = G >= kBK ? 1 : kBK / G;
+  static constexpr int kXBytes = BN * 128;               // BN token rows x 64 k fp16
+  static constexpr int kABytes = kBK * kBM * 2;          // 64 k rows x 128 channels fp16
+  static constexpr int kWBytes = kBK * kStripWords * 4;  // 64 rows x 16 packed words
+  static constexpr int kSBytes = kGR * kBM * 2;
+  static constexpr int kZBytes = kGR * kStripWords * 4;
+  static constexpr int kOffA = kXBytes;                  // both 1024-aligned
+  static constexpr int kOffW = kOffA + kABytes;
+  static constexpr int kOffS = kOffW + kWBytes;
+  static constexpr int kOffZ = kOffS + kSBytes;
+  static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 5 : 6);
+  static constexpr uint32_t kTx = kXBytes + kWBytes + kSBytes + kZBytes;
+  static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
+  static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
+  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int BN, int LG>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,   // x [M][K] fp16, box {64, BN}, SW128
+                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 64}
+                         const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
+                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
+                         int M, int N, int K, __half* __restrict__ y, unsigned* err) {
+  using L = PLayout<BN, LG>;
+  constexpr int kStages = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
+  uint64_t* empty = full + kStages;
+  uint64_t* afull = empty + kStages;
+  uint64_t* accfull = afull + kStages;  // [2]
+  uint64_t* accempty = accfull + 2;     // [2]
+  uint64_t* finalbar = accempty + 2;    // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntn = (N + kBM - 1) / kBM;
+  const int ntm = (M + BN - 1) / BN;
+  const int ntiles = ntn * ntm;
+  const int nkb = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);                // tcgen05.commit of the MMAs reading the stage
+      mbar_init(&afull[s], kDqWarps * 32);    // every dequantising thread
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kEpiWarps);
+    }
+    mbar_init(finalbar, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_qw);
+      tma_prefetch_desc(&tm_s);
+      tma_prefetch_desc(&tm_z);
+      grid_dependency_wait();
+      int stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int nt = tile % ntn, mt = tile / ntn;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+            report_error(err, kErrTimeoutEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * L::kStage;
+          mbar_arrive_expect_tx(&full[stage], L::kTx);
+          tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
+          tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
+          tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
+          tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: wait for the copies of the last (up to kStages) issued stages.
+      for (int i = 0; i < kStages && i < issued; ++i) {
+        stage = stage == 0 ? kStages - 1 : stage - 1;
+        if (stage == kStages - 1) phase ^= 1;
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A MN-major*/ 1, /*B K-major*/ 0);
+      int stage = 0, phase = 0, it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (!mbar_wait_bounded(&accempty[b], ((it >> 1) & 1) ^ 1)) {
+          report_error(err, kErrTimeoutMma);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&afull[stage], phase) || !mbar_wait_bounded(&full[stage], phase)) {
+            report_error(err, kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t xs = smem_u32(smem + stage * L::kStage);
+          const uint32_t as = xs + L::kOffA;
+#pragma unroll
+          for (int s = 0; s < kBK / 16; ++s) {
+            // A: MN-major, 2 channel atoms of 64 (8 KB apart), k groups of 8 rows 1 KB apart;
+            // a k16 step spans two k groups.  B: K-major rows of 128 bytes, 8-row groups 1 KB apart.
+            const uint64_t adesc = umma_sdesc_sw128(as + s * 2048, 8192, 1024);
+            const uint64_t bdesc = umma_sdesc_sw128(xs + s * 32, 16, 1024);
+            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | s) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&accfull[b]);
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      umma_commit(finalbar);
+      if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ---------------- dequantisers: packed int4 -> fp16 A operand ----------------
+    const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
+    const int j = d & 15, r0 = d >> 4;          // packed word column, first row (rows r0 + 16 i)
+    const uint32_t aoff_col = (j >> 3) * 8192;
+    int stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          report_error(err, kErrTimeoutFull);
+          ok = false;
+          break;
+        }
+        const uint32_t st = smem_u32(smem + stage * L::kStage);
+        // per-group constants: -(1024+z) / -(64+z) pairs and (s_c, s_c+4) pairs in chunk order
+        uint32_t zc[L::kGR][4], sp[L::kGR][4];
+#pragma unroll
+        for (int gi = 0; gi < L::kGR; ++gi) {
+          const uint32_t zw = lds_u32(st + L::kOffZ + gi * (kStripWords * 4) + j * 4);
+          const uint32_t zw8 = zw >> 8;
+          zc[gi][0] = and_or(zw, 0x000F000Fu, 0xE400E400u);
+          zc[gi][1] = and_or(zw, 0x00F000F0u, 0xD400D400u);
+          zc[gi][2] = and_or(zw8, 0x000F000Fu, 0xE400E400u);
+          zc[gi][3] = and_or(zw8, 0x00F000F0u, 0xD400D400u);
+          const uint4 sv = lds_u128(st + L::kOffS + gi * (kBM * 2) + j * 16);
+          sp[gi][0] = prmt(sv.x, sv.z, 0x5410u);  // (s0, s4)
+          sp[gi][1] = prmt(sv.x, sv.z, 0x7632u);  // (s1, s5)
+          sp[gi][2] = prmt(sv.y, sv.w, 0x5410u);  // (s2, s6)
+          sp[gi][3] = prmt(sv.y, sv.w, 0x7632u);  // (s3, s7)
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + 16 * i;
+          const int gi = L::kGR == 1 ? 0 : (r >> LG);
+          const uint32_t w = lds_u32(st + L::kOffW + r * 64 + j * 4);
+          const uint32_t w8 = w >> 8;
+          const uint32_t kMagic = 0x64006400u, kSixteenth = 0x2C002C00u;
+          uint4 o;
+          o.x = hmul2_u32(hadd2_u32(and_or(w, 0x000F000Fu, kMagic), zc[gi][0]), sp[gi][0]);
+          o.y = hmul2_u32(hfma2_u32(and_or(w, 0x00F000F0u, kMagic), kSixteenth, zc[gi][1]), sp[gi][1]);
+          o.z = hmul2_u32(hadd2_u32(and_or(w8, 0x000F000Fu, kMagic), zc[gi][2]), sp[gi][2]);
+          o.w = hmul2_u32(hfma2_u32(and_or(w8, 0x00F000F0u, kMagic), kSixteenth, zc[gi][3]), sp[gi][3]);
+          const int rr = r & 7;
+          const uint32_t dst = st + L::kOffA + aoff_col + (r >> 3) * 1024 + rr * 128 + ((((j & 7) ^ rr)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        mbar_arrive(&afull[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> fp16 -> global ----------------
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int i = quad * 32 + lane;
+    const int col_in_tile = 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);  // chunk order n0 n4 n1 n5 ...
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int nt = tile % ntn, mt = tile / ntn;
+      const int b = it & 1;
+      if (!mbar_wait_bounded(&accfull[b], (it >> 1) & 1)) {
+        report_error(err, kErrTimeoutMma);
+        break;
+      }
+      tc_fence_after_sync();
+      const int n = nt * kBM + col_in_tile;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + b * BN;
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + cc, r);
+        tmem_ld_wait();
+        const int mbase = mt * BN + cc;
+        if (n < N) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (mbase + k < M) y[(size_t)(mbase + k) * N + n] = __float2half_rn(__uint_as_float(r[k]));
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+template <int BN, int LG>
+cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
+                     int M, int N, int K, __half* y, unsigned* dev_err, cudaStream_t stream) {
+  using L = PLayout<BN, LG>;
+  auto kern = w4a16_prefill_kernel<BN, LG>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tq, ts, tz, M, N, K, y, dev_err);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_pg(int group, const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts,
+                      const CUtensorMap& tz, int M, int N, int K, __half* y, unsigned* dev_err, cudaStream_t s) {
+  switch (group) {
+    case 32:
+      return launch_p<BN, 5>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+    case 64:
+      return launch_p<BN, 6>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+    default:
+      return launch_p<BN, 7>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                 unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  const int BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  const int GR = group >= kBK ? 1 : kBK / group;
+  CUtensorMap tx, tq, ts, tz;
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B, err) ||
+      !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords, kBK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
+      !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / group, (uint64_t)N * 2, kBM, GR,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
+      !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qzeros, N / 8, K / group, (uint64_t)N / 2, kStripWords, GR,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, err)) {
+    return cudaErrorInvalidValue;
+  }
+  __half* yh = reinterpret_cast<__half*>(y);
+  if (BN == 64) return launch_pg<64>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
+  if (BN == 128) return launch_pg<128>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
+  return launch_pg<256>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
+}
+
+}  // namespace wql
