@@ -1,0 +1,108 @@
+"""GPU parity of the tcgen05 prefill kernels (token counts from 17 up), through the C ABI.
+
+W4A16: fp16 output within 1e-2 of the fp64 oracle (row-relative L2), on ragged tiles.
+W8A8: int32 accumulators and fp16 outputs bit-exact, including adversarial extremes whose sums
+leave the range where fp32 holds integers exactly (checks the 1024-k chunk folding).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from weight_quantized_linear_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wql(wql_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return wql_lib
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def row_rel_err(y, ref):
+    num = np.linalg.norm(y.astype(np.float64) - ref, axis=1)
+    return float((num / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)).max())
+
+
+@pytest.mark.parametrize("M,K,N,G", [(17, 256, 128, 32), (64, 512, 96, 64), (65, 4096, 4096, 128),
+                                     (128, 4096, 12288, 64), (200, 11008, 4096, 128), (257, 4096, 160, 32),
+                                     (300, 96, 4096, 32)])
+def test_w4a16_prefill_ragged(wql, M, K, N, G):
+    W = inputs.weight(K, N, seed=2, outliers=True)
+    X = inputs.activations(M, K, seed=2, outlier_channels=True)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    rows = np.unique(np.linspace(0, M - 1, min(M, 24)).astype(np.int64))
+    y = host(wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G))
+    ref = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
+    assert np.isfinite(y).all()
+    assert row_rel_err(y[rows], ref) <= 1e-2
+    wql.device_status()
+
+
+@pytest.mark.parametrize("M,K,N", [(17, 64, 32), (64, 1024, 128), (130, 4096, 256), (512, 4096, 4096),
+                                   (96, 3008, 160)])
+def test_w8a8_prefill_bit_exact(wql, M, K, N):
+    rng = np.random.default_rng(M + K + N)
+    q = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    qW = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    xs = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), acc_out=acc)
+    rows = np.unique(np.linspace(0, M - 1, min(M, 32)).astype(np.int64))
+    acc_r = oracle.w8a8_acc(q, qW, rows=rows)
+    assert np.array_equal(host(acc)[rows], acc_r)
+    assert np.array_equal(host(y)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xs[rows], ws).view(np.uint16))
+    wql.device_status()
+
+
+@pytest.mark.parametrize("K", [4096, 8192])
+def test_w8a8_prefill_exact_beyond_fp32_integer_range(wql, K):
+    M, N = 40, 256
+    q = np.full((M, K), -128, np.int8)
+    q[1::3] = 127
+    q[2::3, ::2] = -128
+    q[2::3, 1::2] = 127
+    qW = np.full((N, K), -127, np.int8)
+    qW[1::2] = 127
+    qW[::5, : K // 2] = -128
+    xs = np.full((M,), 0.01, np.float32)
+    ws = np.full((N,), 0.001, np.float32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), acc_out=acc)
+    ref = oracle.w8a8_acc(q, qW)
+    assert np.abs(ref.astype(np.int64)).max() > 2 ** 24
+    assert np.array_equal(host(acc), ref)
+    wql.device_status()
+
+
+def test_w8a8_smoothquant_block_full_size_sampled(wql):
+    # the W8A8 block at a full prefill size: prep chain on the GPU, GEMM through the tcgen05 path
+    M, K, N = 4096, 4096, 11008
+    X = inputs.activations(M, K, seed=5, outlier_channels=True)
+    g = inputs.gamma(K, seed=5)
+    W = inputs.weight(K, N, seed=5)
+    Xd, gd, Wd = dev(X), dev(g), dev(W)
+    a = wql.act_absmax(Xd, gd, inputs.EPS)
+    s, g2, W2 = wql.smooth(a, gd, Wd)
+    qW, ws = wql.per_channel_quant_i8(W2)
+    q, xs = wql.qrmsnorm_quant_i8(Xd, g2, inputs.EPS)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = wql.w8a8_gemm(q, xs, qW, ws, acc_out=acc)
+    rows = np.array([0, 1, 777, 2048, 4095], dtype=np.int64)
+    qh, qWh, xsh, wsh = host(q), host(qW), host(xs), host(ws)
+    acc_r = oracle.w8a8_acc(qh, qWh, rows=rows)
+    assert np.array_equal(host(acc)[rows], acc_r)
+    assert np.array_equal(host(y)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xsh[rows], wsh).view(np.uint16))
+    wql.device_status()

@@ -158,10 +158,9 @@ wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float
 }
 
 size_t wql_w8a8_workspace_bytes(int M, int K, int N) {
-  (void)M;
-  (void)K;
   (void)N;
-  return 0;
+  if (M < wql::kW8A8PrefillMinM || K <= 0) return 0;  // the streaming decode kernel needs no scratch
+  return wql::w8a8_prefill_workspace_bytes(M, K);      // fp16 copy of the activation codes
 }
 
 wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K, int N,
@@ -185,8 +184,12 @@ wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, con
   WQL_REQUIRE(need == 0 || (workspace != nullptr && aligned16(workspace)), "workspace must be 16-byte aligned");
   unsigned* dev_err = device_error_word();
   std::string err;
-  cudaError_t e = wql::launch_w8a8_decode(q, xs, qw, ws, M, K, N, y, acc_out, dev_err,
-                                          static_cast<cudaStream_t>(stream), &err);
+  const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode" or "prefill"
+  const bool prefill = force && strcmp(force, "decode") == 0 ? false : M >= wql::kW8A8PrefillMinM;
+  cudaError_t e = prefill ? wql::launch_w8a8_prefill(q, xs, qw, ws, M, K, N, y, acc_out, workspace, dev_err,
+                                                     static_cast<cudaStream_t>(stream), &err)
+                          : wql::launch_w8a8_decode(q, xs, qw, ws, M, K, N, y, acc_out, dev_err,
+                                                    static_cast<cudaStream_t>(stream), &err);
   if (!err.empty()) return fail(WQL_ECUDA, "wql_w8a8_gemm: " + err);
   return cuda_status(e, "wql_w8a8_gemm");
 }

@@ -55,6 +55,13 @@ cudaError_t launch_smooth(const float* absmax, const uint16_t* gamma, const floa
 cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws,
                                         cudaStream_t s);
 
+// Token count from which w8a8_gemm uses the tcgen05 kernel (which needs the workspace).
+constexpr int kW8A8PrefillMinM = 17;
+size_t w8a8_prefill_workspace_bytes(int M, int K);
+cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
+                                int N, uint16_t* y, int32_t* acc_out, void* workspace, unsigned* dev_err,
+                                cudaStream_t stream, std::string* err);
+
 cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
                                int M, int K, int N, uint16_t* y, int32_t* acc_out, unsigned* dev_err,
                                cudaStream_t s, std::string* err);

@@ -1,0 +1,342 @@
+// w8a8_prefill.cu -- SmoothQuant W8A8 GEMM for prefill-shaped calls on the tcgen05 tensor cores
+// ("LMDeploy W8A8 quantisation guide", QLinear.forward / matmul_kernel_dynamic_quant: int8 x int8
+// products summed in int32, then c = c * rms_scale * linear_scale in fp32, rounded to fp16).
+//
+// GB300's tcgen05 has no int8 kind, and int8 values are exact in fp16, so both operands run on
+// kind::f16 as exact fp16 integers:
+//   * a pre-pass converts the activation codes q [M, K] to fp16 in the caller's workspace (TMA then
+//     reads them like any fp16 operand);
+//   * warps 2-9 convert each 128 x 64 int8 weight tile to fp16 directly into a K-major 128B-swizzled
+//     UMMA operand (weights are the 128-row operand: "swap AB");
+//   * exactness: products are at most 128 * 127 < 2^14 and each accumulator covers at most 1024 k,
+//     so every partial sum is an integer below 2^24 that fp32 holds exactly.  The MMA thread
+//     alternates two TMEM chunk accumulators; the epilogue warps turn each finished chunk into
+//     int32 and add it to an int32 running sum kept in TMEM, so the MMAs never wait for them.
+//     The tile's last chunk yields acc (written to acc_out if requested) and
+//     y = fp16((float(acc) * xs[m]) * ws[n]).
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace wql {
+namespace {
+
+constexpr int kBK = 64;         // k per stage (bytes of a weight row)
+constexpr int kBM = 128;        // output channels per tile (MMA M)
+constexpr int kChunkKB = 16;    // stages per exact chunk: 16 x 64 = 1024 k
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kCvWarp0 = 2, kCvWarps = 8, kEpiWarp0 = 10, kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+
+template <int BN>
+struct QLayout {
+  static constexpr int kXBytes = BN * 128;       // BN token rows x 64 k fp16 (from the workspace)
+  static constexpr int kABytes = kBM * 128;      // 128 channel rows x 64 k fp16
+  static constexpr int kWBytes = kBM * kBK;      // 128 rows x 64 int8
+  static constexpr int kOffA = kXBytes;
+  static constexpr int kOffW = kOffA + kABytes;
+  static constexpr int kStage = (kOffW + kWBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = BN >= 128 ? 5 : 6;
+  static constexpr uint32_t kTx = kXBytes + kWBytes;
+  static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
+  static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
+  static constexpr uint32_t kTmemCols = 4 * BN;  // 2 chunk accumulators + int32 sum (+ spare), power of 2
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// int8 [n] -> fp16 [n], exact; n a multiple of 16, both pointers 16-byte aligned.
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ q, __half* __restrict__ out,
+                                                        long long n16) {
+  const uint4* src = reinterpret_cast<const uint4*>(q);
+  uint4* dst = reinterpret_cast<uint4*>(out);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    uint4 a, b;
+    i8x4_to_f16x2x2(v.x, a.x, a.y);
+    i8x4_to_f16x2x2(v.y, a.z, a.w);
+    i8x4_to_f16x2x2(v.z, b.x, b.y);
+    i8x4_to_f16x2x2(v.w, b.z, b.w);
+    dst[2 * i] = a;
+    dst[2 * i + 1] = b;
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // fp16 codes [M][K], box {64, BN}, SW128
+                        const __grid_constant__ CUtensorMap tm_w,  // qw int8 [N][K], box {64, 128}
+                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
+                        __half* __restrict__ y, int32_t* __restrict__ acc_out, unsigned* err) {
+  using L = QLayout<BN>;
+  constexpr int kStages = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
+  uint64_t* empty = full + kStages;
+  uint64_t* afull = empty + kStages;
+  uint64_t* accfull = afull + kStages;  // [2] chunk accumulators
+  uint64_t* accempty = accfull + 2;     // [2]
+  uint64_t* finalbar = accempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntn = (N + kBM - 1) / kBM;
+  const int ntm = (M + BN - 1) / BN;
+  const int ntiles = ntn * ntm;
+  const int nkb = (K + kBK - 1) / kBK;
+  const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&afull[s], kCvWarps * 32);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kEpiWarps);
+    }
+    mbar_init(finalbar, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      grid_dependency_wait();
+      int stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int nt = tile % ntn, mt = tile / ntn;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+            report_error(err, kErrTimeoutEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * L::kStage;
+          mbar_arrive_expect_tx(&full[stage], L::kTx);
+          tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
+          tma_load_2d(st + L::kOffW, &tm_w, &full[stage], kb * kBK, nt * kBM);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      for (int i = 0; i < kStages && i < issued; ++i) {
+        stage = stage == 0 ? kStages - 1 : stage - 1;
+        if (stage == kStages - 1) phase ^= 1;
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A K-major*/ 0, /*B K-major*/ 0);
+      int stage = 0, phase = 0, cseq = 0;  // cseq counts chunks over all tiles
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int c = 0; c < nchunks && ok; ++c, ++cseq) {
+          const int b = cseq & 1;
+          if (!mbar_wait_bounded(&accempty[b], ((cseq >> 1) & 1) ^ 1)) {
+            report_error(err, kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + b * BN;
+          const int kb1 = (c + 1) * kChunkKB < nkb ? (c + 1) * kChunkKB : nkb;
+          for (int kb = c * kChunkKB; kb < kb1; ++kb) {
+            if (!mbar_wait_bounded(&afull[stage], phase) || !mbar_wait_bounded(&full[stage], phase)) {
+              report_error(err, kErrTimeoutMma);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t xs_s = smem_u32(smem + stage * L::kStage);
+            const uint32_t as = xs_s + L::kOffA;
+#pragma unroll
+            for (int s = 0; s < kBK / 16; ++s) {
+              const uint64_t adesc = umma_sdesc_sw128(as + s * 32, 16, 1024);
+              const uint64_t bdesc = umma_sdesc_sw128(xs_s + s * 32, 16, 1024);
+              umma_f16(d_tmem, adesc, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&accfull[b]);
+        }
+      }
+      umma_commit(finalbar);
+      if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ---------------- converters: int8 weight tile -> fp16 K-major A operand ----------------
+    const int d = threadIdx.x - kCvWarp0 * 32;  // 0..255; 16-byte pieces d and d + 256
+    int stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          report_error(err, kErrTimeoutFull);
+          ok = false;
+          break;
+        }
+        const uint32_t st = smem_u32(smem + stage * L::kStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int piece = d + 256 * h;          // 128 rows x 4 pieces of 16 int8
+          const int row = piece >> 2, part = piece & 3;
+          const uint4 v = lds_u128(st + L::kOffW + row * kBK + part * 16);
+          uint4 a, bb;
+          i8x4_to_f16x2x2(v.x, a.x, a.y);
+          i8x4_to_f16x2x2(v.y, a.z, a.w);
+          i8x4_to_f16x2x2(v.z, bb.x, bb.y);
+          i8x4_to_f16x2x2(v.w, bb.z, bb.w);
+          const int rr = row & 7;
+          const uint32_t rbase = st + L::kOffA + (row >> 3) * 1024 + rr * 128;
+          const int c0 = 2 * part, c1 = 2 * part + 1;  // 16-byte chunks (8 k each) of the 128-byte row
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + ((c0 ^ rr) << 4)), "r"(a.x), "r"(a.y),
+                       "r"(a.z), "r"(a.w)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + ((c1 ^ rr) << 4)), "r"(bb.x),
+                       "r"(bb.y), "r"(bb.z), "r"(bb.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&afull[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: exact int32 from the chunk accumulators ----------------
+    const int quad = warp & 3;
+    const int n_in_tile = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    const uint32_t sum_col = 2 * BN;
+    int cseq = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int nt = tile % ntn, mt = tile / ntn;
+      const int n = nt * kBM + n_in_tile;
+      const float wn = n < N ? ws[n] : 0.f;
+      for (int c = 0; c < nchunks; ++c, ++cseq) {
+        const int b = cseq & 1;
+        if (!mbar_wait_bounded(&accfull[b], (cseq >> 1) & 1)) {
+          report_error(err, kErrTimeoutMma);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool first = c == 0, last = c == nchunks - 1;
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 32) {
+          uint32_t r[32], sacc[32];
+          tmem_ld_32x32b_x32(lane_base + b * BN + cc, r);
+          if (!first) tmem_ld_32x32b_x32(lane_base + sum_col + cc, sacc);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int v = __float2int_rn(__uint_as_float(r[k]));  // an exact integer below 2^24
+            sacc[k] = first ? (uint32_t)v : (uint32_t)((int)sacc[k] + v);
+          }
+          if (!last) {
+            tmem_st_32x32b_x32(lane_base + sum_col + cc, sacc);
+            tmem_st_wait();
+          } else if (n < N) {
+            const int mbase = mt * BN + cc;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int m = mbase + k;
+              if (m < M) {
+                const int a = (int)sacc[k];
+                y[(size_t)m * N + n] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(a), xs[m]), wn));
+                if (acc_out) acc_out[(size_t)m * N + n] = a;
+              }
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[b]);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+template <int BN>
+cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const float* xs, const float* ws, int M, int N,
+                     int K, __half* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream) {
+  using L = QLayout<BN>;
+  auto kern = w8a8_prefill_kernel<BN>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, y, acc_out, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t w8a8_prefill_workspace_bytes(int M, int K) { return (size_t)M * (size_t)K * 2; }
+
+cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
+                                int N, uint16_t* y, int32_t* acc_out, void* workspace, unsigned* dev_err,
+                                cudaStream_t stream, std::string* err) {
+  // 1. activation codes -> exact fp16 in the workspace
+  __half* xh = reinterpret_cast<__half*>(workspace);
+  const long long n16 = (long long)M * K / 16;
+  const long long blocks = (n16 + 255) / 256;
+  const int grid = (int)(blocks < 4L * num_sms() ? blocks : 4L * num_sms());
+  i8_to_f16_kernel<<<grid, 256, 0, stream>>>(q, xh, n16);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. the GEMM
+  const int BN = M <= 64 ? 64 : 128;
+  CUtensorMap tx, tw;
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, K, M, (uint64_t)K * 2, 64, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B, err) ||
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    err)) {
+    return cudaErrorInvalidValue;
+  }
+  __half* yh = reinterpret_cast<__half*>(y);
+  if (BN == 64) return launch_q<64>(tx, tw, xs, ws, M, N, K, yh, acc_out, dev_err, stream);
+  return launch_q<128>(tx, tw, xs, ws, M, N, K, yh, acc_out, dev_err, stream);
+}
+
+}  // namespace wql
