@@ -128,6 +128,27 @@ wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, con
                          size_t workspace_bytes, void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * w8a8_gemm_noalloc -- the same operation as wql_w8a8_gemm (same kernels, same results) for
+ * callers that cannot allocate device memory at call time: an engine that has already handed
+ * its whole memory budget to its own pool, a plugin whose host framework owns every allocation,
+ * or a latency-critical loop that must not pay for the allocator's synchronisation.  The source
+ * pages have no counterpart to this entry point; it exists for such callers only.
+ * Instead of a caller workspace it uses a scratch array built into the library:
+ *   - 32 MiB, so M * K * 2 <= 33554432 (e.g. M = K = 4096); larger calls return
+ *     WQL_EUNSUPPORTED with a message in wql_last_error() and launch nothing;
+ *   - one array per GPU that loads the library, held until the process exits;
+ *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture;
+ *   - every call on a device shares the one array.  Calls that may overlap on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the caller.  Nothing in it
+ *     needs to start at zero: each call overwrites every byte it later reads.
+ * The library allocates and frees nothing in this call.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_w8a8_gemm_noalloc(const int8_t* q, const float* xs, const int8_t* qw,
+                                 const float* ws, int M, int K, int N, uint16_t* y,
+                                 int32_t* acc_out, void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * Offline preparation for W8A8 ([W8A8] "weight smoothing" and QLinear.from_float).
  *
  * wql_act_absmax: calibration statistic a_j = max_m |RMSNorm_gamma(x)[m, j]| over x [M, K]

@@ -16,10 +16,11 @@ from ._lib import (  # noqa: F401
     smooth,
     w4a16_gemm,
     w8a8_gemm,
+    w8a8_gemm_noalloc,
     w8a8_workspace_bytes,
 )
 
 __all__ = [
     "WQLError", "act_absmax", "awq_pack", "device_status", "load", "per_channel_quant_i8",
-    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w8a8_gemm", "w8a8_workspace_bytes",
+    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w8a8_gemm", "w8a8_gemm_noalloc", "w8a8_workspace_bytes",
 ]

@@ -34,6 +34,7 @@ SIGNATURES = {
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_w8a8_workspace_bytes": (_SZ, [_I, _I, _I]),
     "wql_w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "wql_w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "wql_act_absmax": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "wql_smooth": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P]),
     "wql_per_channel_quant_i8": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -180,6 +181,27 @@ def w8a8_gemm(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch.Ten
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().wql_w8a8_gemm(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), M, K, N, _ptr(out), _ptr(acc_out),
                                 _ptr(workspace), ws_bytes, _stream(q.device)), "wql_w8a8_gemm")
+    return out
+
+
+def w8a8_gemm_noalloc(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch.Tensor,
+                      out: torch.Tensor, acc_out: torch.Tensor | None = None) -> torch.Tensor:
+    """w8a8_gemm for callers that cannot allocate: the library uses its built-in scratch array.
+
+    The caller passes every input and output (``out`` is required); the call itself allocates
+    nothing.  Limits and sharing rules: see wql_w8a8_gemm_noalloc in include/wql.h.
+    """
+    M, K = q.shape
+    N = qw.shape[0]
+    _need(q, "q", torch.int8, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _need(qw, "qw", torch.int8, (N, K))
+    _need(ws, "ws", torch.float32, (N,))
+    _need(out, "out", torch.float16, (M, N))
+    if acc_out is not None:
+        _need(acc_out, "acc_out", torch.int32, (M, N))
+    _check(load().wql_w8a8_gemm_noalloc(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), M, K, N, _ptr(out), _ptr(acc_out),
+                                        _stream(q.device)), "wql_w8a8_gemm_noalloc")
     return out
 
 

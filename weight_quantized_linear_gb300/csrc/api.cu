@@ -56,6 +56,8 @@ bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
 
 }  // namespace
 
+void wql::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 extern "C" {
 
 const char* wql_status_string(int status) {

@@ -22,6 +22,9 @@ bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// Sets the message returned by wql_last_error() on this host thread.
+void set_last_error(const std::string& msg);
+
 // Split factor S (cluster size along k, 1..8) for a split-K launch of `units` independent output
 // tiles: the largest S whose units * S CTAs are all co-resident in one wave (occupancy query with
 // the cluster attribute, cached per kernel and device), bounded by the number of k blocks.
