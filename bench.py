@@ -518,7 +518,7 @@ def run_sweep(args):
         reps = 20 if flops * len(stack) < 5e12 else 3
         sec = timed(fn, len(stack), reps)
         bound = "hbm" if M <= 32 else "tensor"
-        row = "a2_w4a16_decode" if M < 17 else "a3_w4a16_prefill"
+        row = "a2_w4a16_decode" if M < 33 else "a3_w4a16_prefill"
         emit(row, f"{fam}:M{M}K{K}N{N}G{G}", sec, nbytes, flops, bound, {"copies": len(stack)})
         del x, y
     packed.clear()

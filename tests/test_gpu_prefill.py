@@ -37,7 +37,11 @@ def row_rel_err(y, ref):
 
 @pytest.mark.parametrize("M,K,N,G", [(17, 256, 128, 32), (64, 512, 96, 64), (65, 4096, 4096, 128),
                                      (128, 4096, 12288, 64), (200, 11008, 4096, 128), (257, 4096, 160, 32),
-                                     (300, 96, 4096, 32)])
+                                     (300, 96, 4096, 32),
+                                     # split-K over clusters of 2, 4 and 8 CTAs, with uneven k splits,
+                                     # owner column ranges down to 4 tokens, and ragged token tails
+                                     (20, 4096, 256, 32), (31, 4160, 2048, 64), (64, 4096, 8192, 128),
+                                     (33, 8192, 1024, 128)])
 def test_w4a16_prefill_ragged(wql, M, K, N, G):
     W = inputs.weight(K, N, seed=2, outliers=True)
     X = inputs.activations(M, K, seed=2, outlier_channels=True)
@@ -105,4 +109,35 @@ def test_w8a8_smoothquant_block_full_size_sampled(wql):
     acc_r = oracle.w8a8_acc(qh, qWh, rows=rows)
     assert np.array_equal(host(acc)[rows], acc_r)
     assert np.array_equal(host(y)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xsh[rows], wsh).view(np.uint16))
+    wql.device_status()
+
+
+@pytest.mark.parametrize("M,K,N,G", [(32, 11008, 4096, 32), (256, 11008, 4096, 128)])
+def test_w4a16_prefill_split_k_is_deterministic(wql, M, K, N, G):
+    # the cluster split-K path adds the partial sums in a fixed order: repeated calls agree bit for bit
+    W = inputs.weight(K, N, seed=4)
+    X = inputs.activations(M, K, seed=4, outlier_channels=True)
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    x = dev(X)
+    y0 = host(wql.w4a16_gemm(x, qw, s, qz, G))
+    for _ in range(3):
+        assert np.array_equal(host(wql.w4a16_gemm(x, qw, s, qz, G)).view(np.uint16), y0.view(np.uint16))
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    rows = np.array([0, M // 2, M - 1], dtype=np.int64)
+    assert row_rel_err(y0[rows], oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)) <= 1e-2
+    wql.device_status()
+
+
+@pytest.mark.parametrize("kernel,M,K,N,G", [("prefill", 17, 4096, 256, 32), ("prefill", 20, 4096, 1024, 64),
+                                            ("prefill", 32, 4160, 4096, 64), ("decode", 17, 4096, 512, 128),
+                                            ("decode", 32, 2048, 1024, 32), ("decode", 64, 4096, 256, 64)])
+def test_w4a16_both_kernels_across_the_dispatch_threshold(wql, monkeypatch, kernel, M, K, N, G):
+    # w4a16_gemm picks the kernel by token count; each kernel must be correct on either side of it
+    monkeypatch.setenv("WQL_FORCE_KERNEL", kernel)
+    W = inputs.weight(K, N, seed=3, outliers=True)
+    X = inputs.activations(M, K, seed=3, outlier_channels=True)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    y = host(wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G))
+    rows = np.unique(np.linspace(0, M - 1, min(M, 16)).astype(np.int64))
+    assert row_rel_err(y[rows], oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)) <= 1e-2
     wql.device_status()

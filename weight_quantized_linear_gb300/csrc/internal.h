@@ -27,8 +27,9 @@ void set_last_error(const std::string& msg);
 
 // Split factor S (cluster size along k, 1..8) for a split-K launch of `units` independent output
 // tiles: the largest S whose units * S CTAs are all co-resident in one wave (occupancy query with
-// the cluster attribute, cached per kernel and device), bounded by the number of k blocks.
-int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks);
+// the cluster attribute, cached per kernel and device), bounded by the number of k blocks.  With
+// `pow2`, S is restricted to powers of two.  The kernel is queried with a (1, S, 1) cluster.
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2 = false);
 
 // Launchers.  Each returns cudaSuccess or the launch error; *err gets a message for
 // non-CUDA failures (descriptor encoding).  Arguments are already validated by api.cu.
@@ -44,7 +45,7 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
                                  unsigned* dev_err, cudaStream_t s, std::string* err);
 
 // Token count from which w4a16_gemm uses the tcgen05 kernel instead of the streaming decode kernel.
-constexpr int kW4A16PrefillMinM = 17;
+constexpr int kW4A16PrefillMinM = 33;
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                                      int8_t* q, float* xs, cudaStream_t s);

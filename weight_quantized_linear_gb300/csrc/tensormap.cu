@@ -87,7 +87,7 @@ int num_sms() {
   return cache[dev];
 }
 
-int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks) {
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2) {
   struct Entry {
     const void* k;
     int dev, smem, cap[9];
@@ -137,7 +137,9 @@ int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int
   if (S > 8) S = 8;
   if (S > kblocks) S = kblocks;
   if (S < 1) S = 1;
-  while (S > 1 && units * S > cap[S]) --S;
+  if (pow2)
+    while (S & (S - 1)) S &= S - 1;
+  while (S > 1 && units * S > cap[S]) S = pow2 ? S / 2 : S - 1;
   return S;
 }
 

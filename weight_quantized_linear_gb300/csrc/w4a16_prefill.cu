@@ -1,18 +1,28 @@
 // w4a16_prefill.cu -- AWQ W4A16 GEMM for prefill-shaped calls on the tcgen05 tensor cores.
 //
 // y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n] ("LMDeploy ... INT4 quantisation"
-// tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  A persistent kernel, one
-// CTA per SM, tiles of 128 output channels x BN tokens, K walked in blocks of 64:
+// tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  Tiles of 128 output
+// channels x BN tokens, K walked in blocks of 64, one ring of stages [x tile | A | packed | s | z]:
 //   * warp 0, one thread: TMA copies of the activation tile (K-major, 128B swizzle), the packed
-//     weight tile, and its scale / zero-point rows into a ring of stages;
-//   * warps 2-9: dequantise the packed tile straight into the MMA's A operand: each packed word
-//     (8 output channels at one k) becomes one 16-byte chunk of fp16 (q - z) * s (exact q - z via
-//     the 1024 + q bit-splice trick, one rounding for the scale) in an MN-major 128B-swizzled layout;
+//     weight tile, and its scale / zero-point rows;
+//   * warps 2-9: dequantise the packed tile into the MMA's A operand: each packed word (8 output
+//     channels at one k) becomes one 16-byte chunk of fp16 (q - z) * s (exact q - z via the
+//     1024 + q bit-splice trick, one rounding for the scale) in an MN-major 128B-swizzled layout;
 //   * warp 1: allocates TMEM; one thread issues tcgen05.mma.kind::f16 (M = 128 channels,
 //     N = BN tokens, K = 16) into a double-buffered fp32 accumulator and commits stage releases;
 //   * warps 10-13: tcgen05.ld the accumulator (lane = channel, column = token), round to fp16, store.
 // Swapping A and B puts the dequantised weights (not the activations) in the 128-row operand, so
 // the converter writes 128 x 64 fp16 per stage whatever the token count.
+//
+// Two launch shapes:
+//   * persistent (gridDim.y == 1): one CTA per SM walks the tiles;
+//   * split-K (gridDim.y == S in {2, 4, 8}, clusters of S CTAs along y): when the tiles are fewer
+//     than half the SMs, the S CTAs of a cluster each take 1/S of K for one tile.  After their
+//     main loops they exchange partial sums through distributed shared memory (the stage ring is
+//     reused as the receive buffer): CTA r owns token columns [r BN/S, (r+1) BN/S) and adds the S
+//     partials in split order, so the result does not depend on timing.
+// Launched with programmatic dependent launch: the packed weights of the first stages are
+// requested before waiting for the preceding kernel, whose output may be x.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -45,10 +55,28 @@ struct PLayout {
   static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
   static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  // split-K receive buffer (aliases the ring once every main loop of the cluster has ended):
+  // [source split][channel][BN / S + 4] fp32, largest for S = 8
+  static constexpr int kRecvBytesMax = 8 * kBM * (BN / 8 + 4) * 4;
+  static_assert(kRecvBytesMax <= kStages * kStage, "split-K receive buffer must fit in the ring");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+// Every thread of every warp calls this the same number of times (cluster barrier, release/acquire).
+__device__ __forceinline__ void cluster_phase() {
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait();
 }
 
 template <int BN, int LG>
@@ -75,12 +103,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntm = (M + BN - 1) / BN;
   const int ntiles = ntn * ntm;
   const int nkb = (K + kBK - 1) / kBK;
+  const int S = gridDim.y, split = blockIdx.y;  // split-K: cluster (1, S, 1), rank = blockIdx.y
+  const int kb0 = (int)(((long long)split * nkb) / S), kb1 = (int)(((long long)(split + 1) * nkb) / S);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);                // tcgen05.commit of the MMAs reading the stage
-      mbar_init(&afull[s], kDqWarps * 32);    // every dequantising thread
+      mbar_init(&empty[s], 1);              // tcgen05.commit of the MMAs reading the stage
+      mbar_init(&afull[s], kDqWarps * 32);  // every dequantising thread
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
@@ -97,6 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // A grid of at most one tile per CTA leaves SMs free for most of its run: let the next kernel be
+  // scheduled on them now and start its own weight prefetch (its consumers still wait for this
+  // grid to complete).  A persistent grid over many tiles triggers only when it exits.
+  if (threadIdx.x == 0 && ntiles <= (int)gridDim.x) grid_dependents_launch();
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -104,23 +138,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_qw);
       tma_prefetch_desc(&tm_s);
       tma_prefetch_desc(&tm_z);
+      // The packed weights do not depend on the preceding kernel: fill the first stages with them
+      // before waiting for it, then add the activation tiles.
+      int pre = 0;
+      if ((int)blockIdx.x < ntiles) {
+        const int nt = blockIdx.x % ntn;
+        for (int kb = kb0; kb < kb1 && pre < kStages; ++kb, ++pre) {
+          uint8_t* st = smem + pre * L::kStage;
+          mbar_arrive_expect_tx(&full[pre], L::kTx);
+          tma_load_2d(st + L::kOffW, &tm_qw, &full[pre], nt * kStripWords, kb * kBK);
+          tma_load_2d(st + L::kOffS, &tm_s, &full[pre], nt * kBM, (kb * kBK) >> LG);
+          tma_load_2d(st + L::kOffZ, &tm_z, &full[pre], nt * kStripWords, (kb * kBK) >> LG);
+        }
+      }
       grid_dependency_wait();
       int stage = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int nt = tile % ntn, mt = tile / ntn;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
-            report_error(err, kErrTimeoutEmpty);
-            ok = false;
-            break;
-          }
+        for (int kb = kb0; kb < kb1; ++kb) {
           uint8_t* st = smem + stage * L::kStage;
-          mbar_arrive_expect_tx(&full[stage], L::kTx);
+          if (issued >= pre) {  // stages not armed before the dependency wait
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+              report_error(err, kErrTimeoutEmpty);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], L::kTx);
+            tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
+            tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
+            tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
+          }
           tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
-          tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
-          tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
-          tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -151,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * BN;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&afull[stage], phase) || !mbar_wait_bounded(&full[stage], phase)) {
             report_error(err, kErrTimeoutMma);
             ok = false;
@@ -159,14 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t xs = smem_u32(smem + stage * L::kStage);
-          const uint32_t as = xs + L::kOffA;
 #pragma unroll
           for (int s = 0; s < kBK / 16; ++s) {
-            // A: MN-major, 2 channel atoms of 64 (8 KB apart), k groups of 8 rows 1 KB apart;
-            // a k16 step spans two k groups.  B: K-major rows of 128 bytes, 8-row groups 1 KB apart.
-            const uint64_t adesc = umma_sdesc_sw128(as + s * 2048, 8192, 1024);
-            const uint64_t bdesc = umma_sdesc_sw128(xs + s * 32, 16, 1024);
-            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | s) != 0 ? 1u : 0u);
+            // A: MN-major, 2 channel atoms of 64 (8 KB apart), k groups of 8 rows 1 KB apart; a k16
+            // step spans two k groups (2048 bytes).  B: K-major rows of 128 bytes, 8-row groups 1 KB
+            // apart; a k16 step is 32 bytes along the row.
+            umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, 8192, 1024),
+                     umma_sdesc_sw128(xs + s * 32, 16, 1024), idesc, (kb != kb0 || s != 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == kStages) {
@@ -189,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(&full[stage], phase)) {
           report_error(err, kErrTimeoutFull);
           ok = false;
@@ -215,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = r0 + 16 * i;
-          const int gi = L::kGR == 1 ? 0 : (r >> LG);
+          // rows [16 i, 16 i + 16) lie in one quantisation group (G >= 32): a compile-time index
+          const int gi = L::kGR == 1 ? 0 : ((16 * i) >> LG);
           const uint32_t w = lds_u32(st + L::kOffW + r * 64 + j * 4);
           const uint32_t w8 = w >> 8;
           const uint32_t kMagic = 0x64006400u, kSixteenth = 0x2C002C00u;
@@ -242,36 +291,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int i = quad * 32 + lane;
     const int col_in_tile = 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);  // chunk order n0 n4 n1 n5 ...
-    int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-      const int nt = tile % ntn, mt = tile / ntn;
-      const int b = it & 1;
-      if (!mbar_wait_bounded(&accfull[b], (it >> 1) & 1)) {
-        report_error(err, kErrTimeoutMma);
-        break;
+    grid_dependency_wait();  // y may still be read by the preceding kernel
+    if (S == 1) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int nt = tile % ntn, mt = tile / ntn;
+        const int b = it & 1;
+        if (!mbar_wait_bounded(&accfull[b], (it >> 1) & 1)) {
+          report_error(err, kErrTimeoutMma);
+          break;
+        }
+        tc_fence_after_sync();
+        const int n = nt * kBM + col_in_tile;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + b * BN;
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + cc, r);
+          tmem_ld_wait();
+          const int mbase = mt * BN + cc;
+          if (n < N) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (mbase + k < M) y[(size_t)(mbase + k) * N + n] = __float2half_rn(__uint_as_float(r[k]));
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[b]);
       }
+    } else {
+      // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
+      const int tile = blockIdx.x;
+      const int nt = tile % ntn, mt = tile / ntn;
+      if (!mbar_wait_bounded(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
       tc_fence_after_sync();
-      const int n = nt * kBM + col_in_tile;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + b * BN;
+      const int CW = BN / S;       // token columns owned by each CTA of the cluster
+      const int rstride = CW + 4;  // floats per receive row (16 bytes of padding)
+      cluster_phase();             // (1) every main loop of the cluster is over: the ring is free
+      const uint32_t recv = smem_u32(smem);
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + cc, r);
         tmem_ld_wait();
-        const int mbase = mt * BN + cc;
-        if (n < N) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (mbase + k < M) y[(size_t)(mbase + k) * N + n] = __float2half_rn(__uint_as_float(r[k]));
-          }
+        for (int g = 0; g < 8; ++g) {
+          const int col = cc + 4 * g;
+          const int owner = col / CW, cl = col - owner * CW;
+          const uint32_t off = (uint32_t)(((split * kBM + i) * rstride + cl) * 4);
+          st_cluster_f4(map_cluster_addr(recv + off, (uint32_t)owner),
+                        make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                    __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
         }
       }
       tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&accempty[b]);
+      cluster_phase();  // (2) every partial has landed in its owner's receive buffer
+      const int n = nt * kBM + col_in_tile;
+      if (n < N) {
+#pragma unroll 1
+        for (int cl = 0; cl < CW; cl += 4) {
+          float4 acc = lds_f4(recv + (uint32_t)((i * rstride + cl) * 4));
+          for (int src = 1; src < S; ++src) {
+            const float4 p = lds_f4(recv + (uint32_t)(((src * kBM + i) * rstride + cl) * 4));
+            acc.x = __fadd_rn(acc.x, p.x);
+            acc.y = __fadd_rn(acc.y, p.y);
+            acc.z = __fadd_rn(acc.z, p.z);
+            acc.w = __fadd_rn(acc.w, p.w);
+          }
+          const int m = mt * BN + split * CW + cl;
+          const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
+        }
+      }
     }
   }
 
+  if (S > 1 && warp < kEpiWarp0) {
+    // the other warps take part in the two cluster barriers of the split-K exchange
+    cluster_phase();
+    cluster_phase();
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -292,9 +396,29 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
     attr_set[dev] = true;
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tq, ts, tz, M, N, K, y, dev_err);
-  return cudaGetLastError();
+  const int nkb = (K + kBK - 1) / kBK;
+  const int sms = num_sms();
+  int S = 1;
+  // Few tiles: split K over a cluster so that (nearly) every SM streams weights.  Each split keeps
+  // at least 8 k blocks; S is a power of two dividing BN into owner column ranges of >= 4.
+  if (2 * ntiles <= sms)
+    S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, L::kBytes, ntiles, nkb / 8, /*pow2=*/true);
+  while (S > 1 && BN / S < 4) S >>= 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = S == 1 ? dim3(ntiles < sms ? ntiles : sms, 1, 1) : dim3(ntiles, S, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = S;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = S == 1 ? 1 : 2;
+  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, K, y, dev_err);
 }
 
 template <int BN>
@@ -315,7 +439,7 @@ cudaError_t launch_pg(int group, const CUtensorMap& tx, const CUtensorMap& tq, c
 cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
                                  const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
                                  unsigned* dev_err, cudaStream_t stream, std::string* err) {
-  const int BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  const int BN = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   const int GR = group >= kBK ? 1 : kBK / group;
   CUtensorMap tx, tq, ts, tz;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
@@ -329,6 +453,7 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
     return cudaErrorInvalidValue;
   }
   __half* yh = reinterpret_cast<__half*>(y);
+  if (BN == 32) return launch_pg<32>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
   if (BN == 64) return launch_pg<64>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
   if (BN == 128) return launch_pg<128>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
   return launch_pg<256>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
