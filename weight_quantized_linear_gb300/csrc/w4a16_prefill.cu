@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int nt = tile % ntn, mt = tile / ntn;
         const int b = it & 1;
-        if (!mbar_wait_bounded(&accfull[b], (it >> 1) & 1)) {
+        if (!mbar_wait_warp(&accfull[b], (it >> 1) & 1)) {
           report_error(err, kErrTimeoutMma);
           break;
         }
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
       const int tile = blockIdx.x;
       const int nt = tile % ntn, mt = tile / ntn;
-      if (!mbar_wait_bounded(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
+      if (!mbar_wait_warp(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
       tc_fence_after_sync();
       const int CW = BN / S;       // token columns owned by each CTA of the cluster
       const int rstride = CW + 4;  // floats per receive row (16 bytes of padding)

@@ -6,8 +6,12 @@
 // kind::f16 as exact fp16 integers:
 //   * a pre-pass converts the activation codes q [M, K] to fp16 in the caller's workspace (TMA then
 //     reads them like any fp16 operand);
-//   * warps 2-9 convert each 128 x 64 int8 weight tile to fp16 directly into a K-major 128B-swizzled
-//     UMMA operand (weights are the 128-row operand: "swap AB");
+//   * warps 2-9 convert each 128 x 64 int8 weight tile to fp16 and write it straight into tensor
+//     memory, which the MMA reads as its A operand (weights are the 128-row operand: "swap AB").
+//     A thread owns one output channel, i.e. one TMEM lane, and half of the tile's 64 k: the int8
+//     weight rows are K-contiguous, so its 32 codes are two 16-byte shared-memory loads (the tile
+//     arrives with a 64-byte swizzle, which spreads a warp's rows over all banks).  Keeping the
+//     fp16 operand out of shared memory removes two thirds of the shared-memory traffic per stage;
 //   * exactness: products are at most 128 * 127 < 2^14 and each accumulator covers at most 1024 k,
 //     so every partial sum is an integer below 2^24 that fp32 holds exactly.  The MMA thread
 //     alternates two TMEM chunk accumulators; the epilogue warps turn each finished chunk into
@@ -30,16 +34,22 @@ constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 template <int BN>
 struct QLayout {
   static constexpr int kXBytes = BN * 128;       // BN token rows x 64 k fp16 (from the workspace)
-  static constexpr int kABytes = kBM * 128;      // 128 channel rows x 64 k fp16
-  static constexpr int kWBytes = kBM * kBK;      // 128 rows x 64 int8
-  static constexpr int kOffA = kXBytes;
-  static constexpr int kOffW = kOffA + kABytes;
+  static constexpr int kWBytes = kBM * kBK;      // 128 rows x 64 int8, 64-byte swizzle
+  static constexpr int kOffW = kXBytes;
   static constexpr int kStage = (kOffW + kWBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN >= 128 ? 5 : 6;
+  static constexpr int kStages = 8;
   static constexpr uint32_t kTx = kXBytes + kWBytes;
-  static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
+  // TMEM columns: [0, BN) and [BN, 2 BN) chunk accumulators, [2 BN, 3 BN) int32 running sum,
+  // [3 BN, 4 BN) the fp16 A operand, kASlots slots of 32 columns (64 k) each
+  static constexpr uint32_t kTmemCols = 4 * BN;
+  static constexpr uint32_t kAColBase = 3 * BN;
+  static constexpr int kASlots = BN / 32;
+  static constexpr int kBarBytes = (2 * kStages + kASlots + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
-  static constexpr uint32_t kTmemCols = 4 * BN;  // 2 chunk accumulators + int32 sum (+ spare), power of 2
+  // a converter waits for the stage release of block i - kASlots before reusing its A slot: that
+  // barrier is then never a phase ahead
+  static_assert(kStages >= kASlots, "ring depths");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -74,9 +84,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
-  uint64_t* empty = full + kStages;
-  uint64_t* afull = empty + kStages;
-  uint64_t* accfull = afull + kStages;  // [2] chunk accumulators
+  uint64_t* empty = full + kStages;     // MMAs done with the stage (and with the blocks before it)
+  uint64_t* afull = empty + kStages;    // [kASlots] A slot written to TMEM
+  uint64_t* accfull = afull + L::kASlots;  // [2] chunk accumulators
   uint64_t* accempty = accfull + 2;     // [2]
   uint64_t* finalbar = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
@@ -92,8 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&afull[s], kCvWarps * 32);
     }
+    for (int a = 0; a < L::kASlots; ++a) mbar_init(&afull[a], kCvWarps * 32);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], kEpiWarps);
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A K-major*/ 0, /*B K-major*/ 0);
-      int stage = 0, phase = 0, cseq = 0;  // cseq counts chunks over all tiles
+      int stage = 0, phase = 0, aslot = 0, aph = 0, cseq = 0;  // cseq counts chunks over all tiles
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         for (int c = 0; c < nchunks && ok; ++c, ++cseq) {
@@ -162,24 +172,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem_base + b * BN;
           const int kb1 = (c + 1) * kChunkKB < nkb ? (c + 1) * kChunkKB : nkb;
           for (int kb = c * kChunkKB; kb < kb1; ++kb) {
-            if (!mbar_wait_bounded(&afull[stage], phase) || !mbar_wait_bounded(&full[stage], phase)) {
+            if (!mbar_wait_bounded(&afull[aslot], aph) || !mbar_wait_bounded(&full[stage], phase)) {
               report_error(err, kErrTimeoutMma);
               ok = false;
               break;
             }
             tc_fence_after_sync();
             const uint32_t xs_s = smem_u32(smem + stage * L::kStage);
-            const uint32_t as = xs_s + L::kOffA;
+            const uint32_t a_tmem = tmem_base + L::kAColBase + aslot * 32;
 #pragma unroll
             for (int s = 0; s < kBK / 16; ++s) {
-              const uint64_t adesc = umma_sdesc_sw128(as + s * 32, 16, 1024);
               const uint64_t bdesc = umma_sdesc_sw128(xs_s + s * 32, 16, 1024);
-              umma_f16(d_tmem, adesc, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
+              umma_f16_ta(d_tmem, a_tmem + s * 8, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
             }
-            umma_commit(&empty[stage]);
+            umma_commit(&empty[stage]);  // the stage and this block's A slot are free again
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
+            }
+            if (++aslot == L::kASlots) {
+              aslot = 0;
+              aph ^= 1;
             }
           }
           if (!ok) break;
@@ -190,44 +203,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
     }
   } else if (warp < kEpiWarp0) {
-    // ---------------- converters: int8 weight tile -> fp16 K-major A operand ----------------
-    const int d = threadIdx.x - kCvWarp0 * 32;  // 0..255; 16-byte pieces d and d + 256
-    int stage = 0, phase = 0;
+    // ---------------- converters: int8 weight tile -> fp16 A operand in TMEM ----------------
+    const int quad = warp & 3;                // TMEM lane quadrant this warp may access
+    const int half = (warp - kCvWarp0) >> 2;  // k half of the tile: bytes [32 half, 32 half + 32)
+    const int row = quad * 32 + lane;         // output channel within the tile = TMEM lane
+    const int sw = (row >> 1) & 3;            // 64-byte swizzle: 16-byte chunk c sits at c ^ sw
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + L::kAColBase + 16 * half;
+    int stage = 0, phase = 0, aslot = 0, kbi = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase)) {
+      for (int kb = 0; kb < nkb; ++kb, ++kbi) {
+        // the A slot was last used by block kbi - kASlots: wait until its MMAs have completed
+        const int prev = kbi - L::kASlots;
+        const bool okf = mbar_wait_warp(&full[stage], phase);
+        const bool oke = prev < 0 || mbar_wait_warp(&empty[prev % kStages], (prev / kStages) & 1);
+        if (!okf || !oke) {
           report_error(err, kErrTimeoutFull);
           ok = false;
           break;
         }
-        const uint32_t st = smem_u32(smem + stage * L::kStage);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int piece = d + 256 * h;          // 128 rows x 4 pieces of 16 int8
-          const int row = piece >> 2, part = piece & 3;
-          const uint4 v = lds_u128(st + L::kOffW + row * kBK + part * 16);
-          uint4 a, bb;
-          i8x4_to_f16x2x2(v.x, a.x, a.y);
-          i8x4_to_f16x2x2(v.y, a.z, a.w);
-          i8x4_to_f16x2x2(v.z, bb.x, bb.y);
-          i8x4_to_f16x2x2(v.w, bb.z, bb.w);
-          const int rr = row & 7;
-          const uint32_t rbase = st + L::kOffA + (row >> 3) * 1024 + rr * 128;
-          const int c0 = 2 * part, c1 = 2 * part + 1;  // 16-byte chunks (8 k each) of the 128-byte row
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + ((c0 ^ rr) << 4)), "r"(a.x), "r"(a.y),
-                       "r"(a.z), "r"(a.w)
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + ((c1 ^ rr) << 4)), "r"(bb.x),
-                       "r"(bb.y), "r"(bb.z), "r"(bb.w)
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&afull[stage]);
+        const uint32_t wrow = smem_u32(smem + stage * L::kStage + L::kOffW) + row * kBK;
+        const uint4 v0 = lds_u128(wrow + (((2 * half) ^ sw) << 4));
+        const uint4 v1 = lds_u128(wrow + (((2 * half + 1) ^ sw) << 4));
+        uint32_t a[16];
+        i8x4_to_f16x2x2(v0.x, a[0], a[1]);
+        i8x4_to_f16x2x2(v0.y, a[2], a[3]);
+        i8x4_to_f16x2x2(v0.z, a[4], a[5]);
+        i8x4_to_f16x2x2(v0.w, a[6], a[7]);
+        i8x4_to_f16x2x2(v1.x, a[8], a[9]);
+        i8x4_to_f16x2x2(v1.y, a[10], a[11]);
+        i8x4_to_f16x2x2(v1.z, a[12], a[13]);
+        i8x4_to_f16x2x2(v1.w, a[14], a[15]);
+        tmem_st_32x32b_x16(lane_addr + aslot * 32, a);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&afull[aslot]);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
         }
+        if (++aslot == L::kASlots) aslot = 0;
       }
     }
   } else {
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float wn = n < N ? ws[n] : 0.f;
       for (int c = 0; c < nchunks; ++c, ++cseq) {
         const int b = cseq & 1;
-        if (!mbar_wait_bounded(&accfull[b], (cseq >> 1) & 1)) {
+        if (!mbar_wait_warp(&accfull[b], (cseq >> 1) & 1)) {
           report_error(err, kErrTimeoutMma);
           ok = false;
           break;
@@ -330,7 +345,7 @@ cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* 
   CUtensorMap tx, tw;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, K, M, (uint64_t)K * 2, 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B, err) ||
-      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE,
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B,
                     err)) {
     return cudaErrorInvalidValue;
   }
