@@ -28,8 +28,11 @@ void set_last_error(const std::string& msg);
 // Split factor S (cluster size along k, 1..8) for a split-K launch of `units` independent output
 // tiles: the largest S whose units * S CTAs are all co-resident in one wave (occupancy query with
 // the cluster attribute, cached per kernel and device), bounded by the number of k blocks.  With
-// `pow2`, S is restricted to powers of two.  The kernel is queried with a (1, S, 1) cluster.
-int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2 = false);
+// `pow2`, S is restricted to powers of two.  With `balanced`, S instead minimises the load of the
+// busiest SM (several co-resident CTAs per SM and several rounds allowed).  The kernel is queried
+// with a (1, S, 1) cluster.
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2 = false,
+                 bool balanced = false);
 
 // Launchers.  Each returns cudaSuccess or the launch error; *err gets a message for
 // non-CUDA failures (descriptor encoding).  Arguments are already validated by api.cu.

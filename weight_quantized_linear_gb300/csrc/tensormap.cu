@@ -87,7 +87,7 @@ int num_sms() {
   return cache[dev];
 }
 
-int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2) {
+int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2, bool balanced) {
   struct Entry {
     const void* k;
     int dev, smem, cap[9];
@@ -130,9 +130,33 @@ int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int
       for (int S = 0; S <= 8; ++S) cap[S] = cache[found].cap[S];
     }
   }
+  const int sms = num_sms();
+  if (balanced) {
+    // Weight streaming is bound by each SM's copy rate, so the time is set by the busiest SM: the
+    // co-resident CTAs of an SM share it.  Model: rounds = ceil(CTAs / co-resident capacity); an SM
+    // runs ceil(CTAs in a round / SMs) CTAs of kblocks / S blocks each, plus a fixed cost per CTA
+    // (launch, activation fetch, reduction) of about kFixed blocks.  Smallest cost wins; ties go
+    // to the smaller S, which also leaves room on the SMs for the next layer's early start.
+    constexpr double kFixed = 4.0;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int S = 1; S <= 8 && S <= (kblocks > 0 ? kblocks : 1); ++S) {
+      if (pow2 && (S & (S - 1))) continue;
+      if (cap[S] <= 0) continue;
+      const long long ctas = (long long)units * S;
+      const long long rounds = (ctas + cap[S] - 1) / cap[S];
+      const long long per_round = ctas < cap[S] ? ctas : cap[S];
+      const long long per_sm = (per_round + sms - 1) / sms;
+      const double cost = (double)(rounds * per_sm) * ((double)((kblocks + S - 1) / S) + kFixed);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = S;
+      }
+    }
+    return best;
+  }
   // About one CTA per SM: a decode layer then leaves room on every SM for the next layer's CTAs,
   // which start streaming their weights early (programmatic dependent launch).
-  const int sms = num_sms();
   int S = sms / (units > 0 ? units : 1);
   if (S > 8) S = 8;
   if (S > kblocks) S = kblocks;

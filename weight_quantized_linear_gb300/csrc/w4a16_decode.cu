@@ -380,7 +380,8 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   }
   const int strips = (N + kStripCols - 1) / kStripCols;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
-  const int S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, max_bytes, strips * mblocks, kblocks);
+  const int S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, max_bytes, strips * mblocks, kblocks,
+                             /*pow2=*/false, /*balanced=*/true);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);

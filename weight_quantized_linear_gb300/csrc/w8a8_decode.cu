@@ -261,7 +261,8 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   }
   const int strips = (N + kRows - 1) / kRows;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
-  const int S = pick_k_split(reinterpret_cast<const void*>(w8a8_decode_kernel<MT>), kThreads, L::kBytes, strips * mblocks, kblocks);
+  const int S = pick_k_split(reinterpret_cast<const void*>(w8a8_decode_kernel<MT>), kThreads, L::kBytes, strips * mblocks,
+                             kblocks, /*pow2=*/false, /*balanced=*/true);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
   cfg.blockDim = dim3(kThreads, 1, 1);
