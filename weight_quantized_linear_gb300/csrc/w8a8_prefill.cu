@@ -9,8 +9,8 @@
 //   * warps 2-9 convert each 128 x 64 int8 weight tile to fp16 and write it straight into tensor
 //     memory, which the MMA reads as its A operand (weights are the 128-row operand: "swap AB").
 //     A thread owns one output channel, i.e. one TMEM lane, and half of the tile's 64 k: the int8
-//     weight rows are K-contiguous, so its 32 codes are two 16-byte shared-memory loads (the tile
-//     arrives with a 64-byte swizzle, which spreads a warp's rows over all banks).  Keeping the
+//     weight rows are K-contiguous, so its 64 codes are four 16-byte shared-memory loads (the tile
+//     arrives with a 128-byte swizzle, which spreads a warp's rows over all banks).  Keeping the
 //     fp16 operand out of shared memory removes two thirds of the shared-memory traffic per stage;
 //   * exactness: products are at most 128 * 127 < 2^14 and each accumulator covers at most 1024 k,
 //     so every partial sum is an integer below 2^24 that fp32 holds exactly.  The MMA thread
@@ -25,25 +25,27 @@
 namespace wql {
 namespace {
 
-constexpr int kBK = 64;         // k per stage (bytes of a weight row)
+constexpr int kBK = 128;        // k per stage (bytes of a weight row): 8 MMAs per barrier round trip
 constexpr int kBM = 128;        // output channels per tile (MMA M)
-constexpr int kChunkKB = 16;    // stages per exact chunk: 16 x 64 = 1024 k
+constexpr int kChunkKB = 8;     // stages per exact chunk: 8 x 128 = 1024 k
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kCvWarp0 = 2, kCvWarps = 8, kEpiWarp0 = 10, kEpiWarps = 4;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 
 template <int BN>
 struct QLayout {
-  static constexpr int kXBytes = BN * 128;       // BN token rows x 64 k fp16 (from the workspace)
-  static constexpr int kWBytes = kBM * kBK;      // 128 rows x 64 int8, 64-byte swizzle
+  static constexpr int kXBox = BN * 128;         // BN token rows x 64 k fp16 (from the workspace)
+  static constexpr int kXBytes = 2 * kXBox;      // two 64-k boxes per stage
+  static constexpr int kWBytes = kBM * kBK;      // 128 rows x 128 int8, 128-byte swizzle
   static constexpr int kOffW = kXBytes;
   static constexpr int kStage = (kOffW + kWBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = 8;
+  static constexpr int kStages = BN >= 128 ? 4 : 6;
   static constexpr uint32_t kTx = kXBytes + kWBytes;
-  // TMEM columns: [0, BN) and [BN, 2 BN) chunk accumulators, [2 BN, 3 BN) int32 running sum,
-  // [3 BN, 4 BN) the fp16 A operand, kASlots slots of 32 columns (64 k) each
-  static constexpr uint32_t kTmemCols = 4 * BN;
+  // TMEM columns: [0, BN) and [BN, 2 BN) chunk accumulators, [2 BN, 3 BN) int32 running sum, then
+  // the fp16 A operand: kASlots slots of 64 columns (128 k) each
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kAColBase = 3 * BN;
-  static constexpr int kASlots = BN / 32;
+  static constexpr int kASlots = BN >= 128 ? 2 : 4;
+  static_assert(kAColBase + 64 * kASlots <= kTmemCols, "TMEM budget");
   static constexpr int kBarBytes = (2 * kStages + kASlots + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
   // a converter waits for the stage release of block i - kASlots before reusing its A slot: that
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * L::kStage;
           mbar_arrive_expect_tx(&full[stage], L::kTx);
           tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
+          tma_load_2d(st + L::kXBox, &tm_x, &full[stage], kb * kBK + 64, mt * BN);
           tma_load_2d(st + L::kOffW, &tm_w, &full[stage], kb * kBK, nt * kBM);
           ++issued;
           if (++stage == kStages) {
@@ -179,10 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t xs_s = smem_u32(smem + stage * L::kStage);
-            const uint32_t a_tmem = tmem_base + L::kAColBase + aslot * 32;
+            const uint32_t a_tmem = tmem_base + L::kAColBase + aslot * 64;
 #pragma unroll
             for (int s = 0; s < kBK / 16; ++s) {
-              const uint64_t bdesc = umma_sdesc_sw128(xs_s + s * 32, 16, 1024);
+              // k16 step s: x box s / 4, 32 bytes per step along its 128-byte rows
+              const uint64_t bdesc = umma_sdesc_sw128(xs_s + (s >> 2) * L::kXBox + (s & 3) * 32, 16, 1024);
               umma_f16_ta(d_tmem, a_tmem + s * 8, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
             }
             umma_commit(&empty[stage]);  // the stage and this block's A slot are free again
@@ -205,10 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ---------------- converters: int8 weight tile -> fp16 A operand in TMEM ----------------
     const int quad = warp & 3;                // TMEM lane quadrant this warp may access
-    const int half = (warp - kCvWarp0) >> 2;  // k half of the tile: bytes [32 half, 32 half + 32)
+    const int half = (warp - kCvWarp0) >> 2;  // k half of the tile: bytes [64 half, 64 half + 64)
     const int row = quad * 32 + lane;         // output channel within the tile = TMEM lane
-    const int sw = (row >> 1) & 3;            // 64-byte swizzle: 16-byte chunk c sits at c ^ sw
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + L::kAColBase + 16 * half;
+    const int sw = row & 7;                   // 128-byte swizzle: 16-byte chunk c sits at c ^ sw
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + L::kAColBase + 32 * half;
     int stage = 0, phase = 0, aslot = 0, kbi = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -223,18 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t wrow = smem_u32(smem + stage * L::kStage + L::kOffW) + row * kBK;
-        const uint4 v0 = lds_u128(wrow + (((2 * half) ^ sw) << 4));
-        const uint4 v1 = lds_u128(wrow + (((2 * half + 1) ^ sw) << 4));
-        uint32_t a[16];
-        i8x4_to_f16x2x2(v0.x, a[0], a[1]);
-        i8x4_to_f16x2x2(v0.y, a[2], a[3]);
-        i8x4_to_f16x2x2(v0.z, a[4], a[5]);
-        i8x4_to_f16x2x2(v0.w, a[6], a[7]);
-        i8x4_to_f16x2x2(v1.x, a[8], a[9]);
-        i8x4_to_f16x2x2(v1.y, a[10], a[11]);
-        i8x4_to_f16x2x2(v1.z, a[12], a[13]);
-        i8x4_to_f16x2x2(v1.w, a[14], a[15]);
-        tmem_st_32x32b_x16(lane_addr + aslot * 32, a);
+        uint32_t a[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = lds_u128(wrow + (((4 * half + c) ^ sw) << 4));
+          i8x4_to_f16x2x2(v.x, a[8 * c + 0], a[8 * c + 1]);
+          i8x4_to_f16x2x2(v.y, a[8 * c + 2], a[8 * c + 3]);
+          i8x4_to_f16x2x2(v.z, a[8 * c + 4], a[8 * c + 5]);
+          i8x4_to_f16x2x2(v.w, a[8 * c + 6], a[8 * c + 7]);
+        }
+        tmem_st_32x32b_x32(lane_addr + aslot * 64, a);
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&afull[aslot]);
@@ -345,7 +347,7 @@ cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* 
   CUtensorMap tx, tw;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, K, M, (uint64_t)K * 2, 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B, err) ||
-      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B,
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
                     err)) {
     return cudaErrorInvalidValue;
   }
