@@ -536,7 +536,12 @@ def run_sweep(args):
             del W2
             q, xs = wql.qrmsnorm_quant_i8(X, g2, inputs.EPS)
             if N == 4096:
-                sec = timed(lambda: wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs), 1, 50)
+                # 24 calls per graph, so that graph launch overhead does not count as kernel time
+                def norms(X=X, g2=g2, q=q, xs=xs):
+                    for _ in range(24):
+                        wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
+
+                sec = timed(norms, 24, 20)
                 emit("a4_qrmsnorm_quant_i8", f"M{M}K{K}", sec, qrmsnorm_bytes(M, K), 0, "hbm")
             per = N * K
             copies = int(max(2, min(64, -(-3 * l2 // per))))
@@ -555,10 +560,11 @@ def run_sweep(args):
                  {"copies": copies, "tensor_peak_note": "int8 run as exact fp16 on kind::f16; peak = measured bf16"})
 
             def block(stack=stack, X=X, g2=g2, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
-                wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
-                wql.w8a8_gemm(q, xs, stack[0], ws, out=y, workspace=wsp)
+                for w in stack:
+                    wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
+                    wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
 
-            secb = timed(block, 1, reps)
+            secb = timed(block, copies, reps)
             emit("a4+a6_w8a8_block", f"M{M}K{K}N{N}", secb, qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N), flops,
                  "hbm" if M <= 16 else "tensor")
             del stack, y, wsp, X, q, xs, qW, ws, a, s_, g2
