@@ -98,6 +98,11 @@ TINY_AND_EDGE = [
     (33, 512, 64, 64),    # M just above a 32-token block
     (8, 4096, 4096, 128),
     (5, 11008, 4096, 128),  # K with 172 stages of 64 rows
+    # K % 128 == 64: the last 128-row stage is half past K (activations loaded by the consumer
+    # warps must be zero there), with zero token rows past M inside a 16-token block
+    (1, 4160, 1024, 64),
+    (13, 4160, 512, 32),
+    (20, 192, 256, 64),
 ]
 
 

@@ -33,8 +33,11 @@ namespace {
 constexpr int kBK = 64;          // k per stage
 constexpr int kBM = 128;         // output channels per tile (MMA M)
 constexpr int kStripWords = 16;  // packed words per tile row
+// Warp 0 issues the weight copies and warp 14 the activation copies: copies issued by one thread
+// complete one after another, so two issuing warps keep twice as many in progress.
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kDqWarp0 = 2, kDqWarps = 8, kEpiWarp0 = 10, kEpiWarps = 4;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kXProducerWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kThreads = (kXProducerWarp + 1) * 32;
 
 template <int BN, int LG>
 struct PLayout {
@@ -51,7 +54,7 @@ struct PLayout {
   static constexpr int kOffZ = kOffS + kSBytes;
   static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
   static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 5 : 6);
-  static constexpr uint32_t kTx = kXBytes + kWBytes + kSBytes + kZBytes;
+  static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
   static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
   static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);               // the weight and the activation producer
       mbar_init(&empty[s], 1);              // tcgen05.commit of the MMAs reading the stage
       mbar_init(&afull[s], kDqWarps * 32);  // every dequantising thread
     }
@@ -132,44 +135,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // grid to complete).  A persistent grid over many tiles triggers only when it exits.
   if (threadIdx.x == 0 && ntiles <= (int)gridDim.x) grid_dependents_launch();
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp == kXProducerWarp) {
+    // ---------------- producers: weights (warp 0) and activations (warp 14) ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_qw);
-      tma_prefetch_desc(&tm_s);
-      tma_prefetch_desc(&tm_z);
-      // The packed weights do not depend on the preceding kernel: fill the first stages with them
-      // before waiting for it, then add the activation tiles.
-      int pre = 0;
-      if ((int)blockIdx.x < ntiles) {
-        const int nt = blockIdx.x % ntn;
-        for (int kb = kb0; kb < kb1 && pre < kStages; ++kb, ++pre) {
-          uint8_t* st = smem + pre * L::kStage;
-          mbar_arrive_expect_tx(&full[pre], L::kTx);
-          tma_load_2d(st + L::kOffW, &tm_qw, &full[pre], nt * kStripWords, kb * kBK);
-          tma_load_2d(st + L::kOffS, &tm_s, &full[pre], nt * kBM, (kb * kBK) >> LG);
-          tma_load_2d(st + L::kOffZ, &tm_z, &full[pre], nt * kStripWords, (kb * kBK) >> LG);
-        }
+      const bool wprod = warp == kProducerWarp;
+      if (wprod) {
+        tma_prefetch_desc(&tm_qw);
+        tma_prefetch_desc(&tm_s);
+        tma_prefetch_desc(&tm_z);
+      } else {
+        tma_prefetch_desc(&tm_x);
+        grid_dependency_wait();  // the activations may come from the preceding kernel
       }
-      grid_dependency_wait();
+      // The packed weights do not depend on the preceding kernel: the weight producer never waits
+      // for it, so its first stages stream while the preceding kernel is still running.
       int stage = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int nt = tile % ntn, mt = tile / ntn;
         for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+            report_error(err, kErrTimeoutEmpty);
+            ok = false;
+            break;
+          }
           uint8_t* st = smem + stage * L::kStage;
-          if (issued >= pre) {  // stages not armed before the dependency wait
-            if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
-              report_error(err, kErrTimeoutEmpty);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[stage], L::kTx);
+          if (wprod) {
+            mbar_arrive_expect_tx(&full[stage], L::kWTx);
             tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
             tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
             tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], L::kXBytes);
+            tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
           }
-          tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -286,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: TMEM -> fp16 -> global ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int i = quad * 32 + lane;
@@ -371,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (S > 1 && warp < kEpiWarp0) {
+  if (S > 1 && (warp < kEpiWarp0 || warp >= kEpiWarp0 + kEpiWarps)) {
     // the other warps take part in the two cluster barriers of the split-K exchange
     cluster_phase();
     cluster_phase();
