@@ -2,7 +2,8 @@
 //
 // y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n] ("LMDeploy ... INT4 quantisation"
 // tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  Tiles of 128 output
-// channels x BN tokens, K walked in blocks of 64, one ring of stages [x tile | A | packed | s | z]:
+// channels x BN tokens, K walked in blocks of 128 (64 for the widest tile), one ring of stages
+// [x tile | A | packed | s | z]:
 //   * warp 0, one thread: TMA copies of the activation tile (K-major, 128B swizzle), the packed
 //     weight tile, and its scale / zero-point rows;
 //   * warps 2-9: dequantise the packed tile into the MMA's A operand: each packed word (8 output
@@ -30,7 +31,9 @@
 namespace wql {
 namespace {
 
-constexpr int kBK = 64;          // k per stage
+// k per stage: 128 for token tiles up to 128 (eight MMAs per barrier round trip of the MMA thread),
+// 64 for the widest tile, whose stages would not fit twice in shared memory otherwise
+__host__ __device__ constexpr int bk_for(int bn) { return bn <= 128 ? 128 : 64; }
 constexpr int kBM = 128;         // output channels per tile (MMA M)
 constexpr int kStripWords = 16;  // packed words per tile row
 // Warp 0 issues the weight copies and warp 14 the activation copies: copies issued by one thread
@@ -42,10 +45,14 @@ constexpr int kThreads = (kXProducerWarp + 1) * 32;
 template <int BN, int LG>
 struct PLayout {
   static constexpr int G = 1 << LG;
+  static constexpr int kBK = bk_for(BN);
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;
-  static constexpr int kXBytes = BN * 128;               // BN token rows x 64 k fp16
-  static constexpr int kABytes = kBK * kBM * 2;          // 64 k rows x 128 channels fp16
-  static constexpr int kWBytes = kBK * kStripWords * 4;  // 64 rows x 16 packed words
+  static constexpr int kXBox = BN * 128;                 // BN token rows x 64 k fp16
+  static constexpr int kXBoxes = kBK / 64;
+  static constexpr int kXBytes = kXBoxes * kXBox;
+  static constexpr int kAAtom = kBK * 128;               // 64 channels x kBK k fp16, MN-major
+  static constexpr int kABytes = 2 * kAAtom;             // kBK k rows x 128 channels fp16
+  static constexpr int kWBytes = kBK * kStripWords * 4;  // kBK rows x 16 packed words
   static constexpr int kSBytes = kGR * kBM * 2;
   static constexpr int kZBytes = kGR * kStripWords * 4;
   static constexpr int kOffA = kXBytes;                  // both 1024-aligned
@@ -53,7 +60,7 @@ struct PLayout {
   static constexpr int kOffS = kOffW + kWBytes;
   static constexpr int kOffZ = kOffS + kSBytes;
   static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 5 : 6);
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 64 ? 3 : 4);
   static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
   static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
@@ -90,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                          int M, int N, int K, __half* __restrict__ y, unsigned* err) {
   using L = PLayout<BN, LG>;
-  constexpr int kStages = L::kStages;
+  constexpr int kStages = L::kStages, kBK = L::kBK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
@@ -167,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
           } else {
             mbar_arrive_expect_tx(&full[stage], L::kXBytes);
-            tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mt * BN);
+#pragma unroll
+            for (int b = 0; b < L::kXBoxes; ++b)
+              tma_load_2d(st + b * L::kXBox, &tm_x, &full[stage], kb * kBK + 64 * b, mt * BN);
           }
           ++issued;
           if (++stage == kStages) {
@@ -209,11 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t xs = smem_u32(smem + stage * L::kStage);
 #pragma unroll
           for (int s = 0; s < kBK / 16; ++s) {
-            // A: MN-major, 2 channel atoms of 64 (8 KB apart), k groups of 8 rows 1 KB apart; a k16
-            // step spans two k groups (2048 bytes).  B: K-major rows of 128 bytes, 8-row groups 1 KB
-            // apart; a k16 step is 32 bytes along the row.
-            umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, 8192, 1024),
-                     umma_sdesc_sw128(xs + s * 32, 16, 1024), idesc, (kb != kb0 || s != 0) ? 1u : 0u);
+            // A: MN-major, 2 channel atoms of 64 (kAAtom apart), k groups of 8 rows 1 KB apart; a
+            // k16 step spans two k groups (2048 bytes).  B: 64-k boxes of K-major 128-byte rows,
+            // 8-row groups 1 KB apart; a k16 step is 32 bytes along the row.
+            umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, L::kAAtom, 1024),
+                     umma_sdesc_sw128(xs + (s >> 2) * L::kXBox + (s & 3) * 32, 16, 1024), idesc,
+                     (kb != kb0 || s != 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == kStages) {
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- dequantisers: packed int4 -> fp16 A operand ----------------
     const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
     const int j = d & 15, r0 = d >> 4;          // packed word column, first row (rows r0 + 16 i)
-    const uint32_t aoff_col = (j >> 3) * 8192;
+    const uint32_t aoff_col = (j >> 3) * L::kAAtom;
     int stage = 0, phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sp[gi][3] = prmt(sv.y, sv.w, 0x7632u);  // (s3, s7)
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kBK / 16; ++i) {
           const int r = r0 + 16 * i;
           // rows [16 i, 16 i + 16) lie in one quantisation group (G >= 32): a compile-time index
           const int gi = L::kGR == 1 ? 0 : ((16 * i) >> LG);
@@ -395,13 +405,14 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
     attr_set[dev] = true;
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int nkb = (K + kBK - 1) / kBK;
+  const int nkb = (K + L::kBK - 1) / L::kBK;
   const int sms = num_sms();
   int S = 1;
   // Few tiles: split K over a cluster so that (nearly) every SM streams weights.  Each split keeps
-  // at least 8 k blocks; S is a power of two dividing BN into owner column ranges of >= 4.
+  // at least 512 k; S is a power of two dividing BN into owner column ranges of >= 4.
   if (2 * ntiles <= sms)
-    S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, L::kBytes, ntiles, nkb / 8, /*pow2=*/true);
+    S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, L::kBytes, ntiles, nkb * L::kBK / 512,
+                     /*pow2=*/true);
   while (S > 1 && BN / S < 4) S >>= 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = S == 1 ? dim3(ntiles < sms ? ntiles : sms, 1, 1) : dim3(ntiles, S, 1);
@@ -439,11 +450,12 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
                                  const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
                                  unsigned* dev_err, cudaStream_t stream, std::string* err) {
   const int BN = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
-  const int GR = group >= kBK ? 1 : kBK / group;
+  const int BK = bk_for(BN);
+  const int GR = group >= BK ? 1 : BK / group;
   CUtensorMap tx, tq, ts, tz;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B, err) ||
-      !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords, kBK,
+      !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords, BK,
                     CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
       !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / group, (uint64_t)N * 2, kBM, GR,
                     CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
