@@ -68,86 +68,102 @@ __device__ __forceinline__ float quant_code(float y, float s, float inv) {
 }
 
 // MODE 0: quantise (q, xs); MODE 1: per-channel absmax of the norm output (atomic max into absmax).
-template <int CPT, int MODE>
+// A CTA normalises R consecutive rows (R = 1 as launched); every row's 16-byte loads are issued
+// before the first reduction.
+template <int CPT, int R, int MODE>
 __global__ void __launch_bounds__(kNormThreads)
-    qrmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma, float eps, int K,
+    qrmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma, float eps, int M, int K,
                     int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax) {
   __shared__ float red[272];  // [0, 256) lane partials, 256 row sum, [264, 272) warp maxima
-  const int m = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   // programmatic dependent launch: the next kernel (typically the int8 GEMM) may start fetching its
   // weights now; this kernel's input comes from the preceding kernel
   if (tid == 0) grid_dependents_launch();
   grid_dependency_wait();
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)m * K);
   const int nchunks = K >> 3;
+  const int m0 = blockIdx.x * R;
 
-  uint4 xv[CPT];
-  float p = 0.f;
+  uint4 xv[R][CPT];
 #pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int c = tid + kNormThreads * i;
-    if (c < nchunks) {
-      xv[i] = __ldg(xr + c);
-      const __half* h = reinterpret_cast<const __half*>(&xv[i]);
+  for (int rr = 0; rr < R; ++rr) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(m0 + rr) * K);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float v = __half2float(h[e]);
-        p = __fadd_rn(p, __fmul_rn(v, v));
-      }
-    }
-  }
-  const float ss = block_sum_fixed(p, red);
-  const float mean = __fdiv_rn(ss, (float)K);
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-
-  float yv[CPT][8];
-  float amax = 0.f;
-  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int c = tid + kNormThreads * i;
-    if (c < nchunks) {
-      const uint4 gv = __ldg(gr + c);
-      const __half* h = reinterpret_cast<const __half*>(&xv[i]);
-      const __half* gh = reinterpret_cast<const __half*>(&gv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float yy = __fmul_rn(__fmul_rn(__half2float(h[e]), r), __half2float(gh[e]));
-        yv[i][e] = yy;
-        amax = fmaxf(amax, fabsf(yy));
-      }
+    for (int i = 0; i < CPT; ++i) {
+      const int c = tid + kNormThreads * i;
+      if (m0 + rr < M && c < nchunks) xv[rr][i] = __ldg(xr + c);
     }
   }
 
-  if (MODE == 1) {
+#pragma unroll
+  for (int rr = 0; rr < R; ++rr) {
+    const int m = m0 + rr;
+    if (m >= M) break;  // uniform over the CTA
+    float p = 0.f;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
+        const __half* h = reinterpret_cast<const __half*>(&xv[rr][i]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          atomicMax(reinterpret_cast<int*>(absmax) + 8 * c + e, __float_as_int(fabsf(yv[i][e])));
+        for (int e = 0; e < 8; ++e) {
+          const float v = __half2float(h[e]);
+          p = __fadd_rn(p, __fmul_rn(v, v));
+        }
       }
     }
-    return;
-  }
+    const float ss = block_sum_fixed(p, red);
+    const float mean = __fdiv_rn(ss, (float)K);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 
-  const float rowmax = block_max(amax, red);
-  const float scale = rowmax == 0.f ? 1.0f : __fdiv_rn(rowmax, 127.0f);
-  const float inv = __fdiv_rn(1.0f, scale);
-  if (tid == 0) xs[m] = scale;
-  int8_t* qr = q + (size_t)m * K;
+    float yv[CPT][8];
+    float amax = 0.f;
+    const uint4* gr = reinterpret_cast<const uint4*>(gamma);
 #pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int c = tid + kNormThreads * i;
-    if (c < nchunks) {
-      uint32_t packed[2] = {0u, 0u};
+    for (int i = 0; i < CPT; ++i) {
+      const int c = tid + kNormThreads * i;
+      if (c < nchunks) {
+        const uint4 gv = __ldg(gr + c);
+        const __half* h = reinterpret_cast<const __half*>(&xv[rr][i]);
+        const __half* gh = reinterpret_cast<const __half*>(&gv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float v = quant_code(yv[i][e], scale, inv);
-        packed[e >> 2] |= (uint32_t)(uint8_t)(int8_t)(int)v << (8 * (e & 3));
+        for (int e = 0; e < 8; ++e) {
+          const float yy = __fmul_rn(__fmul_rn(__half2float(h[e]), r), __half2float(gh[e]));
+          yv[i][e] = yy;
+          amax = fmaxf(amax, fabsf(yy));
+        }
       }
-      *reinterpret_cast<uint2*>(qr + 8 * c) = make_uint2(packed[0], packed[1]);
+    }
+
+    if (MODE == 1) {
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = tid + kNormThreads * i;
+        if (c < nchunks) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicMax(reinterpret_cast<int*>(absmax) + 8 * c + e, __float_as_int(fabsf(yv[i][e])));
+        }
+      }
+      continue;
+    }
+
+    const float rowmax = block_max(amax, red);
+    const float scale = rowmax == 0.f ? 1.0f : __fdiv_rn(rowmax, 127.0f);
+    const float inv = __fdiv_rn(1.0f, scale);
+    if (tid == 0) xs[m] = scale;
+    int8_t* qr = q + (size_t)m * K;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = tid + kNormThreads * i;
+      if (c < nchunks) {
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float v = quant_code(yv[i][e], scale, inv);
+          packed[e >> 2] |= (uint32_t)(uint8_t)(int8_t)(int)v << (8 * (e & 3));
+        }
+        *reinterpret_cast<uint2*>(qr + 8 * c) = make_uint2(packed[0], packed[1]);
+      }
     }
   }
 }
@@ -175,14 +191,12 @@ cudaError_t launch_norm(const uint16_t* x, const uint16_t* gamma, float eps, int
   const __half* xh = reinterpret_cast<const __half*>(x);
   const __half* gh = reinterpret_cast<const __half*>(gamma);
   const int cpt = (K + 2047) / 2048;
-  dim3 grid(M), block(kNormThreads);
-  if (cpt <= 1)
-    return launch_pdl(qrmsnorm_kernel<1, MODE>, grid, block, s, xh, gh, eps, K, q, xs, absmax);
-  if (cpt <= 2)
-    return launch_pdl(qrmsnorm_kernel<2, MODE>, grid, block, s, xh, gh, eps, K, q, xs, absmax);
-  if (cpt <= 4)
-    return launch_pdl(qrmsnorm_kernel<4, MODE>, grid, block, s, xh, gh, eps, K, q, xs, absmax);
-  return launch_pdl(qrmsnorm_kernel<8, MODE>, grid, block, s, xh, gh, eps, K, q, xs, absmax);
+  // one row per CTA (two rows per CTA measured slower at M = 4096)
+  const dim3 grid(M), block(kNormThreads);
+  if (cpt <= 1) return launch_pdl(qrmsnorm_kernel<1, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
+  if (cpt <= 2) return launch_pdl(qrmsnorm_kernel<2, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
+  if (cpt <= 4) return launch_pdl(qrmsnorm_kernel<4, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
+  return launch_pdl(qrmsnorm_kernel<8, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
 }
 
 }  // namespace
