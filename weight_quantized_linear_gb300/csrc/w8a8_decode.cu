@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_mbarrier_init();
-    grid_dependents_launch();  // the next kernel may start streaming its own weights now
   }
   __syncwarp();
   cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
@@ -113,6 +112,9 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
       }
       grid_dependency_wait();
       for (int i = 0; i < pro; ++i) tma_load_2d(smem + i * L::kStage, &tm_x, &full[i], (kb0 + i) * kBK, m0);
+      // the next kernel may launch now: its CTAs open with a burst of weight copies on these SMs'
+      // TMA units, which must not queue ahead of the activation copies above
+      grid_dependents_launch();
       int issued = pro;
       for (; issued < nkb; ++issued) {
         const int s = issued % L::kStages;
