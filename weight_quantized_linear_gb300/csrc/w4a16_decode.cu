@@ -10,8 +10,9 @@
 //     previous kernel; only the activation copies wait.  It lets the next kernel launch as soon as
 //     those activation copies are issued, so the next layer's CTAs stream their weights during
 //     this layer's arithmetic and reduction without delaying its activations.
-//   * Eight consumer warps: two column groups of 64 outputs x four stage lanes (lane l owns every
-//     stage i with i % 4 == l, so every group is reduced by a single warp).  They feed the legacy
+//   * Consumer warps: two column groups of 64 outputs x four stage lanes for 8-token blocks, two
+//     lanes for 16-token blocks (lane l owns every stage i with i % lanes == l, so every group is
+//     reduced by a single warp).  They feed the legacy
 //     mma.sync.m16n8k16 tensor-core path with the weights as the 16-row operand and the tokens as
 //     the 8-column operand ("swap AB").  The int4 codes enter the MMA as the exact fp16 values
 //     1024 + q (or 1024 + 16 q): one PRMT pairs rows k and k+1, one LOP3 per two weights splices
@@ -35,16 +36,24 @@ namespace {
 constexpr int kBK = 128;           // k rows per stage (a multiple of every group size)
 constexpr int kStripWords = 16;    // packed words per row of a CTA strip
 constexpr int kStripCols = 128;    // output columns per CTA
-constexpr int kLanes = 4;          // stage lanes
-constexpr int kConsumerWarps = 2 * kLanes;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+// Stage lanes: four for blocks of 8 tokens, two for blocks of 16.  With two lanes a 16-token CTA
+// has 160 threads, so it and a CTA of the next layer fit one SM's register file together (the
+// next layer's CTAs stream their weights while this one computes).
+template <int MT>
+struct Warps {
+  static constexpr int kLanes = MT <= 1 ? 4 : 2;
+  static constexpr int kConsumerWarps = 2 * kLanes;  // two column groups per lane
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+};
 
 template <int MT, int LG>
 struct Layout {
   static constexpr int G = 1 << LG;
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;      // groups per stage
-  // Slot s of the ring is always served by stage lane s % 4, so a lane can never lap another lane
-  // on a slot (the parity-based barrier waits rely on it): the depth is a multiple of 4.
+  static constexpr int kLanes = Warps<MT>::kLanes;
+  // Slot s of the ring is always served by stage lane s % kLanes, so a lane can never lap another
+  // lane on a slot (the parity-based barrier waits rely on it): the depth is a multiple of kLanes.
   static constexpr int kStages = 8;
   static_assert(kStages % kLanes == 0, "ring depth must be a multiple of the lane count");
   static constexpr int kSlab = 8 * MT * 128;              // token rows x 64 k fp16 (128-byte rows)
@@ -52,17 +61,46 @@ struct Layout {
   static constexpr int kWBytes = kBK * kStripWords * 4;   // 128 rows x 64 B
   static constexpr int kSBytes = kGR * kStripCols * 2;
   static constexpr int kZBytes = kGR * kStripWords * 4;
-  static constexpr int kStage = (kXBytes + kWBytes + kSBytes + kZBytes + 1023) / 1024 * 1024;
+  // A stage is [activation slabs | packed tile], 1024-byte aligned for the 128B swizzle; its
+  // scale and zero-point rows sit in a separate array, so the stages carry no padding.
+  static constexpr int kStage = kXBytes + kWBytes;
+  static_assert(kStage % 1024 == 0, "stages must keep the 128B-swizzled slabs 1024-byte aligned");
+  static constexpr int kSZ = (kSBytes + kZBytes + 127) / 128 * 128;
   static constexpr int kE = 8 * MT * kStripCols;          // elements of one partial tile
   static constexpr int kNQ = kE / 4;                      // float4s of one partial tile
   static constexpr uint32_t kTx = kXBytes + kWBytes + kSBytes + kZBytes;
-  // shared memory map: [stages (1024-aligned)] [receive buffer] [barriers]
-  static constexpr int kOffRecv = kStages * kStage;
+  // shared memory map: [stages (1024-aligned)] [scale/zero rows per stage] [receive buffer] [barriers]
+  static constexpr int kOffSZ = kStages * kStage;
+  static constexpr int kOffRecv = kOffSZ + kStages * kSZ;
   static int bytes(int S) {
     const int lmax = (kNQ + S - 1) / S;
     return kOffRecv + S * lmax * 16 + (2 * kStages + 1) * 8 + 1024;
   }
 };
+
+// Shared-memory footprint of every decode launch with group size 2^LG: the largest over both token
+// blocks and every split, as long as two such CTAs still fit one SM (0 otherwise: each launch then
+// takes its own size).  Back-to-back layers keep one CTA of each of two consecutive layers per SM
+// only when the block scheduler sees alike CTAs; with footprints that differ between 8- and
+// 16-token layers, a change of token count left some SMs with two CTAs of one layer for the rest
+// of the sequence (measured: 48 q_proj layers at M = 1 then 48 at M = 16, 479 -> 402 us).
+template <int LG>
+int common_footprint() {
+  static int bytes = -1;
+  if (bytes < 0) {
+    int f = 0;
+    for (int S = 1; S <= 8; ++S) {
+      f = Layout<1, LG>::bytes(S) > f ? Layout<1, LG>::bytes(S) : f;
+      f = Layout<2, LG>::bytes(S) > f ? Layout<2, LG>::bytes(S) : f;
+    }
+    int dev = 0, per_sm = 0, reserved = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    bytes = 2 * (f + reserved) <= per_sm ? f : 0;
+  }
+  return bytes;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -86,7 +124,7 @@ __device__ __forceinline__ void splice4(uint32_t T, uint32_t out[4]) {
 }
 
 template <int MT, int LG>
-__global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
+__global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
     w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x: 3D {64, M, K/64} box {64, 8MT, 2}, or
                                                                     //    2D {K, M} box {64, 8MT} (x3d == 0)
                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 128}, SW64
@@ -94,6 +132,9 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                         int M, int N, int kblocks, int x3d, __half* __restrict__ y, unsigned* err) {
   using L = Layout<MT, LG>;
+  constexpr int kLanes = L::kLanes;
+  constexpr int kConsumerWarps = Warps<MT>::kConsumerWarps;
+  constexpr int kThreads = Warps<MT>::kThreads;
   constexpr int G = L::G;
   constexpr int kGR = L::kGR;
   constexpr int kStages = L::kStages;
@@ -145,11 +186,12 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
       auto issue_weights = [&](int i) {
         const int s = i % kStages, kb = kb0 + i;
         uint8_t* st = smem + s * L::kStage + L::kXBytes;
+        uint8_t* sz = smem + L::kOffSZ + s * L::kSZ;
         const int grow = (kb * kBK) >> LG;
         mbar_arrive_expect_tx(&full[s], L::kTx);
         tma_load_2d_hint(st, &tm_qw, &full[s], strip * kStripWords, kb * kBK, pol);
-        tma_load_2d_hint(st + L::kWBytes, &tm_s, &full[s], strip * kStripCols, grow, pol);
-        tma_load_2d_hint(st + L::kWBytes + L::kSBytes, &tm_z, &full[s], strip * kStripWords, grow, pol);
+        tma_load_2d_hint(sz, &tm_s, &full[s], strip * kStripCols, grow, pol);
+        tma_load_2d_hint(sz + L::kSBytes, &tm_z, &full[s], strip * kStripWords, grow, pol);
       };
       auto issue_x = [&](int i) {
         const int s = i % kStages, kb = kb0 + i;
@@ -230,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
       }
       const uint32_t xt = smem_u32(smem + s * L::kStage);
       const uint32_t wt = xt + L::kXBytes;
-      const uint32_t sbase = wt + L::kWBytes, zbase = sbase + L::kSBytes;
+      const uint32_t sbase = smem_u32(smem + L::kOffSZ + s * L::kSZ), zbase = sbase + L::kSBytes;
 #pragma unroll
       for (int gi = 0; gi < kGR; ++gi) {
         float acc[4][MT][4];
@@ -303,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // Fold the four lanes' partials in shared memory first.  Once all consumer warps pass this
+    // Fold the lanes' partials in shared memory first.  Once all consumer warps pass this
     // named barrier every stage has been consumed and every issued copy has landed (each one was
     // waited for by its lane), so the pipeline memory is free for staging.
     named_barrier_sync(1, kConsumerWarps * 32);
@@ -322,9 +364,15 @@ __global__ void __launch_bounds__(kThreads, MT <= 1 ? 2 : 1)
     const uint32_t recv_base = smem_u32(recv);
     const uint32_t bar_local = smem_u32(recv_full);
     for (int f = threadIdx.x; f < L::kNQ; f += kConsumerWarps * 32) {
-      const float4 a = stage4[f], b = stage4[L::kNQ + f], c = stage4[2 * L::kNQ + f], d = stage4[3 * L::kNQ + f];
-      const float4 v = make_float4(((a.x + b.x) + c.x) + d.x, ((a.y + b.y) + c.y) + d.y, ((a.z + b.z) + c.z) + d.z,
-                                   ((a.w + b.w) + c.w) + d.w);
+      float4 v = stage4[f];
+#pragma unroll
+      for (int q = 1; q < kLanes; ++q) {  // lane order
+        const float4 p = stage4[q * L::kNQ + f];
+        v.x += p.x;
+        v.y += p.y;
+        v.z += p.z;
+        v.w += p.w;
+      }
       const int owner = f / lmax;
       const uint32_t slot = recv_base + (uint32_t)(((int)rank * lmax + (f - owner * lmax)) * 16);
       st_async_f4(map_cluster_addr(slot, owner), v, map_cluster_addr(bar_local, owner));
@@ -370,12 +418,15 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
                       const CUtensorMap& tz, int M, int N, int kblocks, __half* y, unsigned* dev_err,
                       cudaStream_t stream) {
   using L = Layout<MT, LG>;
+  constexpr int kThreads = Warps<MT>::kThreads;
   auto kern = w4a16_decode_kernel<MT, LG>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  int max_bytes = 0;  // the receive buffer size depends on the cluster size
-  for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S) > max_bytes ? L::bytes(S) : max_bytes;
+  const int common = common_footprint<LG>();
+  int max_bytes = common;  // otherwise the largest over the cluster sizes (the receive buffer varies)
+  if (!common)
+    for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S) > max_bytes ? L::bytes(S) : max_bytes;
   if (dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
     if (e != cudaSuccess) return e;
@@ -389,7 +440,7 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::bytes(S);
+  cfg.dynamicSmemBytes = common ? common : L::bytes(S);
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
