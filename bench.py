@@ -15,6 +15,7 @@ launch streams its weights from HBM.  The step is captured once in a CUDA graph 
 ``--impl reference`` times the CPU oracle itself on the same metric (the source pages ship no
 runnable code; the oracle is the reference arm).  ``--sweep FILE`` additionally measures every
 hot-path row over the five workload families and writes one JSON line per case to FILE.
+``--profile-case OP:DIMS`` only runs a few calls of one operation (for ncu captures).
 """
 from __future__ import annotations
 
@@ -578,6 +579,64 @@ def run_sweep(args):
     return 0
 
 
+# ------------------------------------------------------------------------------------------------
+# small single-operation runs for ncu captures (no timing)
+# ------------------------------------------------------------------------------------------------
+
+def run_profile_case(args):
+    """A few calls of one operation on one shape, for a profiler to capture.
+
+    ``w4a16:M,K,N,G``, ``w8a8:M,K,N``, ``norm:M,K`` or ``prep:K,N`` (awq_pack with G = 128, then
+    per_channel_quant_i8).  Each operation is called ``--calls`` times on synthetic inputs.
+    """
+    import numpy as np
+    import torch
+    from weight_quantized_linear_gb300 import build, inputs
+    import weight_quantized_linear_gb300 as wql
+    build.build()
+    wql.load()
+    dev = torch.device("cuda", 0)
+    op, _, dims = args.profile_case.partition(":")
+    d = [int(v) for v in dims.split(",")] if dims else []
+    calls = args.calls
+    if op == "w4a16":
+        M, K, N, G = d
+        qw, s, qz = wql.awq_pack(torch.from_numpy(inputs.weight(K, N, seed=0, outliers=True)).to(dev), G)
+        x = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for _ in range(calls):
+            wql.w4a16_gemm(x, qw, s, qz, G, out=y)
+    elif op == "w8a8":
+        M, K, N = d
+        rng = np.random.default_rng(0)
+        q = torch.from_numpy(rng.integers(-128, 128, size=(M, K), dtype=np.int8)).to(dev)
+        qW = torch.from_numpy(rng.integers(-127, 128, size=(N, K), dtype=np.int8)).to(dev)
+        xs = torch.full((M,), 0.01, device=dev)
+        ws = torch.full((N,), 0.001, device=dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for _ in range(calls):
+            wql.w8a8_gemm(q, xs, qW, ws, out=y)
+    elif op == "norm":
+        M, K = d
+        X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
+        g = torch.from_numpy(inputs.gamma(K, seed=0)).to(dev)
+        for _ in range(calls):
+            wql.qrmsnorm_quant_i8(X, g, inputs.EPS)
+    elif op == "prep":
+        K, N = d
+        W = torch.from_numpy(inputs.weight(K, N, seed=0)).to(dev)
+        for _ in range(calls):
+            wql.awq_pack(W, 128)
+        for _ in range(calls):
+            wql.per_channel_quant_i8(W)
+    else:
+        raise SystemExit(f"unknown profile case {args.profile_case!r}")
+    torch.cuda.synchronize()
+    wql.device_status(dev)
+    print("ok", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,7 +646,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None, help="measure every hot-path row; JSON lines to this file")
+    ap.add_argument("--profile-case", default=None,
+                    help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N | norm:M,K | prep:K,N")
+    ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
