@@ -155,7 +155,8 @@ wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float
   WQL_REQUIRE_PTR(gamma);
   WQL_REQUIRE_PTR(q);
   WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
-  return cuda_status(wql::launch_qrmsnorm_quant_i8(x, gamma, eps, M, K, q, xs, static_cast<cudaStream_t>(stream)),
+  return cuda_status(wql::launch_qrmsnorm_quant_i8(x, gamma, eps, M, K, q, xs, device_error_word(),
+                                                   static_cast<cudaStream_t>(stream)),
                      "wql_qrmsnorm_quant_i8");
 }
 
@@ -206,7 +207,8 @@ wql_status wql_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, i
     WQL_REQUIRE_PTR(x);
     WQL_REQUIRE_PTR(gamma);
   }
-  return cuda_status(wql::launch_act_absmax(x, gamma, eps, M, K, absmax, static_cast<cudaStream_t>(stream)),
+  return cuda_status(wql::launch_act_absmax(x, gamma, eps, M, K, absmax, device_error_word(),
+                                            static_cast<cudaStream_t>(stream)),
                      "wql_act_absmax");
 }
 

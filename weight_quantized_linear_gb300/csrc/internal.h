@@ -51,10 +51,10 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
 constexpr int kW4A16PrefillMinM = 33;
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
-                                     int8_t* q, float* xs, cudaStream_t s);
+                                     int8_t* q, float* xs, unsigned* dev_err, cudaStream_t s);
 
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
-                              float* absmax, cudaStream_t s);
+                              float* absmax, unsigned* dev_err, cudaStream_t s);
 
 cudaError_t launch_smooth(const float* absmax, const uint16_t* gamma, const float* w, int K, int N,
                           float* s_out, uint16_t* gamma_out, float* w_out, cudaStream_t s);

@@ -3,8 +3,9 @@
 // rms_norm_dynamic_quant, per_token_quant_int8 with scale = absmax / 127 and codes rounded to
 // integers; smoothing statistics are the per-channel absmax of the norm output).
 //
-// One CTA of 256 threads per token row.  The row is read once with 16-byte loads and kept in
-// registers; the sum of squares uses a fixed order (chunk c of 8 elements belongs to thread
+// CTAs of 256 threads walk the token rows; each row is brought into shared memory by a bulk copy
+// (several rows in flight per CTA) and held in registers while it is normalised.  The sum of
+// squares uses a fixed order (chunk c of 8 elements belongs to thread
 // c mod 256, which adds its elements in increasing k; the 256 partial sums are then folded
 // pairwise (t, t+128), (t, t+64), ..., (t, t+1)), so int8 codes are reproducible bit for bit.
 // Every float operation uses an explicitly rounded intrinsic: nothing is contracted into FMA.
@@ -15,27 +16,6 @@ namespace wql {
 namespace {
 
 constexpr int kNormThreads = 256;
-
-// Sum of the 256 lane partials in the fixed order (t, t+128), (t, t+64), ..., (t, t+1).  The three
-// cross-warp levels are evaluated by lane l of warp 0 from the eight partials l + 32 w, in exactly
-// that order; the last five levels are warp shuffles.  Two barriers; every thread gets the total.
-__device__ __forceinline__ float block_sum_fixed(float p, float* red) {
-  const int tid = threadIdx.x;
-  red[tid] = p;
-  __syncthreads();
-  if (tid < 32) {
-    const float* r = red + tid;
-    const float a0 = __fadd_rn(r[0], r[128]), a1 = __fadd_rn(r[64], r[192]);    // (t, t+128) at t, t+64
-    const float a2 = __fadd_rn(r[32], r[160]), a3 = __fadd_rn(r[96], r[224]);   // ... at t+32, t+96
-    const float b0 = __fadd_rn(a0, a1), b1 = __fadd_rn(a2, a3);                  // (t, t+64) at t, t+32
-    float v = __fadd_rn(b0, b1);                                                 // (t, t+32)
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
-    if (tid == 0) red[256] = v;
-  }
-  __syncthreads();
-  return red[256];
-}
 
 // Row maximum; `slot` selects a scratch area distinct from the one the sum used, so one barrier
 // suffices.
@@ -50,84 +30,155 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
-// round_half_even(fl(y / s)) clamped to [-128, 127], without a division in the common case.
+// Bulk copy of `bytes` contiguous bytes from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+constexpr int kNormSlots = 4;  // rows in flight per CTA
+
+// Round to the nearest integer (ties to even) and saturate to [-128, 127], in one conversion.
+__device__ __forceinline__ int cvt_rni_sat_s8(float f) {
+  int r;
+  asm("{\n .reg .s8 t;\n cvt.rni.sat.s8.f32 t, %1;\n cvt.s32.s8 %0, t;\n}" : "=r"(r) : "f"(f));
+  return r;
+}
+
+// clamp(round_half_even(fl(y / s)), -128, 127), without a division in the common case.
 // t = fl(y * inv) with inv = fl(1 / s) lies within 2.3e-5 of fl(y / s) when |y / s| <= 127.5
 // (two roundings of relative size 2^-24 each, plus fl(y / s)'s own half ulp), so whenever t is
-// more than 5e-5 away from a half-integer, both round to the same integer.  Otherwise the exact
-// quotient is computed.
-__device__ __forceinline__ float quant_code(float y, float s, float inv) {
+// more than 5e-5 from a half-integer (|t - rint(t)| < 0.49995), both round to the same integer.
+// quant_fast returns rint(t) saturated and sets `exact` when that is not guaranteed; quant_exact
+// then divides.
+__device__ __forceinline__ int quant_fast(float y, float inv, bool& exact) {
   const float t = __fmul_rn(y, inv);
-  const float fr = fabsf(t - truncf(t));  // distance above the lower integer, in [0, 1)
-  float r;
-  if (fabsf(fr - 0.5f) > 5e-5f) {
-    r = rintf(t);
-  } else {
-    r = rintf(__fdiv_rn(y, s));
-  }
-  return fminf(fmaxf(r, -128.f), 127.f);
+  const float rt = rintf(t);
+  exact |= !(fabsf(__fsub_rn(t, rt)) < 0.49995f);
+  return cvt_rni_sat_s8(rt);
+}
+__device__ __forceinline__ int quant_exact(float y, float s, float inv) {
+  const float t = __fmul_rn(y, inv);
+  const float rt = rintf(t);
+  if (fabsf(__fsub_rn(t, rt)) < 0.49995f) return cvt_rni_sat_s8(rt);
+  return cvt_rni_sat_s8(__fdiv_rn(y, s));
+}
+
+// Low bytes of four ints, packed little-endian.
+__device__ __forceinline__ uint32_t pack_s8x4(int c0, int c1, int c2, int c3) {
+  const uint32_t lo = prmt((uint32_t)c0, (uint32_t)c1, 0x0040u), hi = prmt((uint32_t)c2, (uint32_t)c3, 0x0040u);
+  return prmt(lo, hi, 0x5410u);
+}
+
+// Sum of the 256 lane partials in the fixed order (t, t+128), (t, t+64), ..., (t, t+1), with one
+// barrier: every warp evaluates the three cross-warp levels (lane l from the eight partials
+// l + 32 w, in exactly that order) and the five shuffle levels itself, so all threads get the same
+// total.  The barrier also votes: it returns false in every thread if `ok` is false in any thread.
+__device__ __forceinline__ bool row_sum_vote(float p, bool ok, float* red, float& total) {
+  const int lane = threadIdx.x & 31;
+  red[threadIdx.x] = p;
+  if (__syncthreads_or(!ok)) return false;
+  const float* r = red + lane;
+  const float a0 = __fadd_rn(r[0], r[128]), a1 = __fadd_rn(r[64], r[192]);
+  const float a2 = __fadd_rn(r[32], r[160]), a3 = __fadd_rn(r[96], r[224]);
+  const float b0 = __fadd_rn(a0, a1), b1 = __fadd_rn(a2, a3);
+  float v = __fadd_rn(b0, b1);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+  total = __shfl_sync(0xffffffffu, v, 0);
+  return true;
 }
 
 // MODE 0: quantise (q, xs); MODE 1: per-channel absmax of the norm output (atomic max into absmax).
-// A CTA normalises R consecutive rows (R = 1 as launched); every row's 16-byte loads are issued
-// before the first reduction.
-template <int CPT, int R, int MODE>
-__global__ void __launch_bounds__(kNormThreads)
+// Persistent CTAs: CTA b normalises rows b, b + gridDim.x, ...  Thread 0 keeps kNormSlots rows in
+// flight with bulk copies into a shared-memory ring, so HBM reads continue through every row's
+// reductions; a slot is refilled as soon as all threads have read it (the first barrier of the
+// row's sum).
+template <int CPT, int MODE>
+__global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? 4 : 1)
     qrmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma, float eps, int M, int K,
-                    int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax) {
+                    int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax, unsigned* err) {
   __shared__ float red[272];  // [0, 256) lane partials, 256 row sum, [264, 272) warp maxima
+  __shared__ __align__(8) uint64_t full[kNormSlots];
+  extern __shared__ __align__(16) uint8_t rows[];  // kNormSlots x 2K bytes
   const int tid = threadIdx.x;
-  // programmatic dependent launch: the next kernel (typically the int8 GEMM) may start fetching its
-  // weights now; this kernel's input comes from the preceding kernel
-  if (tid == 0) grid_dependents_launch();
-  grid_dependency_wait();
   const int nchunks = K >> 3;
-  const int m0 = blockIdx.x * R;
-
-  uint4 xv[R][CPT];
+  const uint32_t row_bytes = 2u * (uint32_t)K;
+  const int nrows = M > (int)blockIdx.x ? (M - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  auto issue = [&](int j) {  // row j of this CTA into slot j % kNormSlots
+    const int s = j % kNormSlots;
+    mbar_arrive_expect_tx(&full[s], row_bytes);
+    bulk_load(rows + (size_t)s * row_bytes, x + (size_t)(blockIdx.x + (size_t)j * gridDim.x) * K, row_bytes, &full[s]);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kNormSlots; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  // x comes from the preceding kernel, which may also still read q and xs
+  grid_dependency_wait();
+  if (tid == 0) {
+    for (int j = 0; j < nrows && j < kNormSlots; ++j) issue(j);
+    grid_dependents_launch();  // the next kernel's copies now queue behind these
+  }
+  // gamma is read once per CTA and kept in registers, as fp32, for all of its rows
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  float gf[CPT][8];
 #pragma unroll
-  for (int rr = 0; rr < R; ++rr) {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(m0 + rr) * K);
+  for (int i = 0; i < CPT; ++i) {
+    const int c = tid + kNormThreads * i;
+    if (c < nchunks) {
+      const uint4 gv = __ldg(gr + c);
+      const __half* gh = reinterpret_cast<const __half*>(&gv);
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      const int c = tid + kNormThreads * i;
-      if (m0 + rr < M && c < nchunks) xv[rr][i] = __ldg(xr + c);
+      for (int e = 0; e < 8; ++e) gf[i][e] = __half2float(gh[e]);
     }
   }
 
-#pragma unroll
-  for (int rr = 0; rr < R; ++rr) {
-    const int m = m0 + rr;
-    if (m >= M) break;  // uniform over the CTA
+  int j = 0;
+  for (; j < nrows; ++j) {
+    const int m = blockIdx.x + j * gridDim.x;
+    const int s = j % kNormSlots;
+    // Every thread waits; the row sum's barrier votes, so that all threads leave together if a wait
+    // ever expires (the values read from an unfinished slot are then discarded).
+    const bool ok = mbar_wait_bounded(&full[s], (j / kNormSlots) & 1);
+    const uint4* xr = reinterpret_cast<const uint4*>(rows + (size_t)s * row_bytes);
+    float yv[CPT][8];  // x, then the normalised row
     float p = 0.f;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
-        const __half* h = reinterpret_cast<const __half*>(&xv[rr][i]);
+        const uint4 xv = xr[c];
+        const __half* h = reinterpret_cast<const __half*>(&xv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float v = __half2float(h[e]);
+          yv[i][e] = v;
           p = __fadd_rn(p, __fmul_rn(v, v));
         }
       }
     }
-    const float ss = block_sum_fixed(p, red);
+    float ss;
+    if (!row_sum_vote(p, ok, red, ss)) {
+      if (tid == 0) report_error(err, kErrTimeoutFull);
+      break;
+    }
+    // every thread has read slot s (it passed the sum's barrier): refill it
+    if (tid == 0 && j + kNormSlots < nrows) issue(j + kNormSlots);
     const float mean = __fdiv_rn(ss, (float)K);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 
-    float yv[CPT][8];
     float amax = 0.f;
-    const uint4* gr = reinterpret_cast<const uint4*>(gamma);
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
-        const uint4 gv = __ldg(gr + c);
-        const __half* h = reinterpret_cast<const __half*>(&xv[rr][i]);
-        const __half* gh = reinterpret_cast<const __half*>(&gv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float yy = __fmul_rn(__fmul_rn(__half2float(h[e]), r), __half2float(gh[e]));
+          const float yy = __fmul_rn(__fmul_rn(yv[i][e], r), gf[i][e]);
           yv[i][e] = yy;
           amax = fmaxf(amax, fabsf(yy));
         }
@@ -144,6 +195,7 @@ __global__ void __launch_bounds__(kNormThreads)
             atomicMax(reinterpret_cast<int*>(absmax) + 8 * c + e, __float_as_int(fabsf(yv[i][e])));
         }
       }
+      __syncthreads();  // the lane partials in red[] are read by every warp before the next row writes them
       continue;
     }
 
@@ -156,26 +208,38 @@ __global__ void __launch_bounds__(kNormThreads)
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
-        uint32_t packed[2] = {0u, 0u};
+        int k8[8];
+        bool exact = false;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float v = quant_code(yv[i][e], scale, inv);
-          packed[e >> 2] |= (uint32_t)(uint8_t)(int8_t)(int)v << (8 * (e & 3));
+        for (int e = 0; e < 8; ++e) k8[e] = quant_fast(yv[i][e], inv, exact);
+        if (exact) {  // rare: some element lies within 5e-5 of a rounding tie
+#pragma unroll
+          for (int e = 0; e < 8; ++e) k8[e] = quant_exact(yv[i][e], scale, inv);
         }
-        *reinterpret_cast<uint2*>(qr + 8 * c) = make_uint2(packed[0], packed[1]);
+        *reinterpret_cast<uint2*>(qr + 8 * c) =
+            make_uint2(pack_s8x4(k8[0], k8[1], k8[2], k8[3]), pack_s8x4(k8[4], k8[5], k8[6], k8[7]));
       }
     }
+  }
+  // Leave no copy in flight: after an expired wait, wait (bounded) for the rows still issued.
+  if (j < nrows && tid == 0) {
+    const int issued = nrows < j + kNormSlots ? nrows : j + kNormSlots;
+    for (int i = j; i < issued; ++i)
+      if (!mbar_wait_bounded(&full[i % kNormSlots], (i / kNormSlots) & 1)) {
+        report_error(err, kErrTimeoutDrain);
+        break;
+      }
   }
 }
 
 // Launch with programmatic stream serialisation: the kernel may start while its predecessor drains
 // (it waits with griddepcontrol.wait before touching its inputs).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -185,33 +249,59 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+template <int CPT, int MODE>
+cudaError_t launch_rows(const __half* x, const __half* gamma, float eps, int M, int K, int8_t* q, float* xs,
+                        float* absmax, unsigned* err, cudaStream_t s) {
+  auto kern = qrmsnorm_kernel<CPT, MODE>;
+  const size_t smem = (size_t)kNormSlots * 2 * K;
+  static int set_bytes[64] = {0};   // dynamic shared memory limit set on the kernel, per device
+  static int fit_bytes[64] = {0};   // ring size of the cached occupancy
+  static int fit_ctas[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (set_bytes[dev] < (int)smem) {  // a longer row needs a larger ring: raise the limit
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    set_bytes[dev] = (int)smem;
+  }
+  if (fit_bytes[dev] != (int)smem) {
+    int fit = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, kNormThreads, smem);
+    if (e != cudaSuccess) return e;
+    fit_bytes[dev] = (int)smem;
+    fit_ctas[dev] = fit > 0 ? fit : 1;
+  }
+  const long long cap = (long long)fit_ctas[dev] * num_sms();
+  const dim3 grid((unsigned)(M < cap ? M : cap)), block(kNormThreads);
+  return launch_pdl(kern, grid, block, smem, s, x, gamma, eps, M, K, q, xs, absmax, err);
+}
+
 template <int MODE>
 cudaError_t launch_norm(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q, float* xs,
-                        float* absmax, cudaStream_t s) {
+                        float* absmax, unsigned* err, cudaStream_t s) {
   const __half* xh = reinterpret_cast<const __half*>(x);
   const __half* gh = reinterpret_cast<const __half*>(gamma);
   const int cpt = (K + 2047) / 2048;
-  // one row per CTA (two rows per CTA measured slower at M = 4096)
-  const dim3 grid(M), block(kNormThreads);
-  if (cpt <= 1) return launch_pdl(qrmsnorm_kernel<1, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
-  if (cpt <= 2) return launch_pdl(qrmsnorm_kernel<2, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
-  if (cpt <= 4) return launch_pdl(qrmsnorm_kernel<4, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
-  return launch_pdl(qrmsnorm_kernel<8, 1, MODE>, grid, block, s, xh, gh, eps, M, K, q, xs, absmax);
+  if (cpt <= 1) return launch_rows<1, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
+  if (cpt <= 2) return launch_rows<2, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
+  if (cpt <= 4) return launch_rows<4, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
+  return launch_rows<8, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
 }
 
 }  // namespace
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
-                                     float* xs, cudaStream_t s) {
-  return launch_norm<0>(x, gamma, eps, M, K, q, xs, nullptr, s);
+                                     float* xs, unsigned* dev_err, cudaStream_t s) {
+  return launch_norm<0>(x, gamma, eps, M, K, q, xs, nullptr, dev_err, s);
 }
 
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,
-                              cudaStream_t s) {
+                              unsigned* dev_err, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(absmax, 0, sizeof(float) * (size_t)K, s);
   if (e != cudaSuccess) return e;
   if (M == 0) return cudaSuccess;
-  return launch_norm<1>(x, gamma, eps, M, K, nullptr, nullptr, absmax, s);
+  return launch_norm<1>(x, gamma, eps, M, K, nullptr, nullptr, absmax, dev_err, s);
 }
 
 }  // namespace wql
