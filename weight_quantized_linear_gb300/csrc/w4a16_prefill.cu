@@ -6,14 +6,16 @@
 // [x tile | A | packed | s | z]:
 //   * warp 0, one thread: TMA copies of the activation tile (K-major, 128B swizzle), the packed
 //     weight tile, and its scale / zero-point rows;
-//   * warps 2-9: dequantise the packed tile into the MMA's A operand: each packed word (8 output
-//     channels at one k) becomes one 16-byte chunk of fp16 (q - z) * s (exact q - z via the
-//     1024 + q bit-splice trick, one rounding for the scale) in an MN-major 128B-swizzled layout;
+//   * warps 2-9: dequantise the packed tile into the MMA's A operand, fp16 (q - z) * s (exact q - z
+//     via the 1024 + q bit-splice trick, one rounding for the scale).  Token tiles up to 128: into
+//     tensor memory with tcgen05.st, one channel per TMEM lane, so that shared memory carries only
+//     the activations and the packed weights; the widest tile: into an MN-major 128B-swizzled
+//     shared-memory layout, one 16-byte chunk per packed word (8 channels at one k);
 //   * warp 1: allocates TMEM; one thread issues tcgen05.mma.kind::f16 (M = 128 channels,
 //     N = BN tokens, K = 16) into a double-buffered fp32 accumulator and commits stage releases;
 //   * warps 10-13: tcgen05.ld the accumulator (lane = channel, column = token), round to fp16, store.
 // Swapping A and B puts the dequantised weights (not the activations) in the 128-row operand, so
-// the converter writes 128 x 64 fp16 per stage whatever the token count.
+// the dequantisers write 128 x kBK fp16 per stage whatever the token count.
 //
 // Two launch shapes:
 //   * persistent (gridDim.y == 1): one CTA per SM walks the tiles;
@@ -45,26 +47,35 @@ constexpr int kThreads = (kXProducerWarp + 1) * 32;
 template <int BN, int LG>
 struct PLayout {
   static constexpr int G = 1 << LG;
+  // Token tiles up to 128: the dequantised weights go straight to tensor memory (tcgen05.st) and the
+  // MMA reads its A operand there, so shared memory carries only the activations and packed
+  // weights.  The widest tile needs all 512 TMEM columns for its two accumulators and keeps A in
+  // shared memory.
+  static constexpr bool kTA = BN <= 128;
   static constexpr int kBK = bk_for(BN);
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;
   static constexpr int kXBox = BN * 128;                 // BN token rows x 64 k fp16
   static constexpr int kXBoxes = kBK / 64;
   static constexpr int kXBytes = kXBoxes * kXBox;
   static constexpr int kAAtom = kBK * 128;               // 64 channels x kBK k fp16, MN-major
-  static constexpr int kABytes = 2 * kAAtom;             // kBK k rows x 128 channels fp16
+  static constexpr int kABytes = kTA ? 0 : 2 * kAAtom;   // kBK k rows x 128 channels fp16
   static constexpr int kWBytes = kBK * kStripWords * 4;  // kBK rows x 16 packed words
   static constexpr int kSBytes = kGR * kBM * 2;
   static constexpr int kZBytes = kGR * kStripWords * 4;
-  static constexpr int kOffA = kXBytes;                  // both 1024-aligned
+  static constexpr int kOffA = kXBytes;                  // both 1024-aligned (the packed tile: 512)
   static constexpr int kOffW = kOffA + kABytes;
   static constexpr int kOffS = kOffW + kWBytes;
   static constexpr int kOffZ = kOffS + kSBytes;
   static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 64 ? 3 : 4);
+  // with A in TMEM, stage s also owns A slot s: the producers' wait for the stage to be free (the
+  // MMAs of the stage kStages earlier have completed) frees the slot too
+  static constexpr int kStages = 4;
   static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
   static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
-  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr uint32_t kAColBase = 2 * BN;  // A slots (64 columns = 128 k each) after the accumulators
+  static constexpr uint32_t kTmemCols = kTA ? 512 : (2 * BN < 32 ? 32 : 2 * BN);
+  static_assert(!kTA || (kBK == 128 && kAColBase + 64 * kStages <= kTmemCols), "TMEM budget");
   // split-K receive buffer (aliases the ring once every main loop of the cluster has ended):
   // [source split][channel][BN / S + 4] fp32, largest for S = 8
   static constexpr int kRecvBytesMax = 8 * kBM * (BN / 8 + 4) * 4;
@@ -92,7 +103,8 @@ __device__ __forceinline__ void cluster_phase() {
 template <int BN, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,   // x [M][K] fp16, box {64, BN}, SW128
-                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 64}
+                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8]: box {16, 64}, or (A in TMEM)
+                                                                     // 3D {N/8, K/4, 4} box {16, 32, 4}, SW64
                          const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                          const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                          int M, int N, int K, __half* __restrict__ y, unsigned* err) {
@@ -120,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 2);               // the weight and the activation producer
       mbar_init(&empty[s], 1);              // tcgen05.commit of the MMAs reading the stage
-      mbar_init(&afull[s], kDqWarps * 32);  // every dequantising thread
+      // A in TMEM: one arrival per dequantising warp; A in shared memory: every dequantising thread
+      mbar_init(&afull[s], L::kTA ? kDqWarps : kDqWarps * 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
@@ -169,7 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * L::kStage;
           if (wprod) {
             mbar_arrive_expect_tx(&full[stage], L::kWTx);
-            tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
+            if constexpr (L::kTA)  // rows k = 4a + b land at row 32 b + a of the tile
+              tma_load_3d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * (kBK / 4), 0);
+            else
+              tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
             tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
             tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
           } else {
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A MN-major*/ 1, /*B K-major*/ 0);
+      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A MN-major (smem) or TMEM*/ L::kTA ? 0 : 1, /*B K-major*/ 0);
       int stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
@@ -216,14 +232,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t xs = smem_u32(smem + stage * L::kStage);
+          // the B descriptors of the stage differ only in the start address (bits 0-13, addr >> 4;
+          // shared-memory addresses stay below 2^18, so adding to it never carries)
+          const uint64_t bdesc0 = umma_sdesc_sw128(xs, 16, 1024);
 #pragma unroll
           for (int s = 0; s < kBK / 16; ++s) {
-            // A: MN-major, 2 channel atoms of 64 (kAAtom apart), k groups of 8 rows 1 KB apart; a
-            // k16 step spans two k groups (2048 bytes).  B: 64-k boxes of K-major 128-byte rows,
-            // 8-row groups 1 KB apart; a k16 step is 32 bytes along the row.
-            umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, L::kAAtom, 1024),
-                     umma_sdesc_sw128(xs + (s >> 2) * L::kXBox + (s & 3) * 32, 16, 1024), idesc,
-                     (kb != kb0 || s != 0) ? 1u : 0u);
+            // B: 64-k boxes of K-major 128-byte rows, 8-row groups 1 KB apart; a k16 step is 32
+            // bytes along the row.  A in TMEM: slot `stage`, eight columns per k16 step.  A in
+            // shared memory: MN-major, 2 channel atoms of 64 (kAAtom apart), k groups of 8 rows
+            // 1 KB apart; a k16 step spans two k groups (2048 bytes).
+            const uint64_t bdesc = bdesc0 + (uint64_t)(((s >> 2) * L::kXBox + (s & 3) * 32) >> 4);
+            const uint32_t acc = (kb != kb0 || s != 0) ? 1u : 0u;
+            if constexpr (L::kTA)
+              umma_f16_ta(d_tmem, tmem_base + L::kAColBase + stage * 64 + s * 8, bdesc, idesc, acc);
+            else
+              umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, L::kAAtom, 1024), bdesc, idesc, acc);
           }
           umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == kStages) {
@@ -238,8 +261,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(finalbar);
       if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
     }
+  } else if (warp < kEpiWarp0 && L::kTA) {
+    // ---------------- dequantisers: packed int4 -> fp16 A operand in TMEM ----------------
+    // Warp w writes TMEM lane quarter q = w % 4 (channels 32 q ..) for k in [64 hk, 64 hk + 64) of
+    // each stage.  Thread (g, c) = (lane / 4, lane % 4) takes packed word 4 q + g / 2, nibbles
+    // 4 (g % 2) + e (e = 0..3), i.e. channels 32 q + 4 g + e, at k = 16 m + 4 c + {0..3}; through
+    // tcgen05.st.16x256b, e = 0, 1 go to lanes g, g + 8 and e = 2, 3 to lanes 16 + g, 24 + g, so
+    // TMEM lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8.  Rows k and k + 1 are paired by
+    // one PRMT, so each 32-bit value is the fp16 pair (k, k + 1) of one channel: a TMEM column.
+    const int dw = warp - kDqWarp0;
+    const int q = warp & 3, hk = dw >> 2;
+    const int g = lane >> 2, c = lane & 3;
+    const int wj = 4 * q + (g >> 1);
+    const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+    const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + L::kAColBase + 32 * hk;
+    const uint32_t taddr1 = taddr0 + (16u << 16);
+    constexpr uint32_t kMagic = 0x64006400u, kSixteenth = 0x2C002C00u;
+    int stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_warp(&full[stage], phase)) {  // warp-uniform: tcgen05.st is .sync.aligned
+          report_error(err, kErrTimeoutFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();  // this slot's earlier MMAs (ordered through the stage barriers) come first
+        const uint32_t st = smem_u32(smem + stage * L::kStage);
+        uint32_t r0[16], r1[16];
+        uint32_t zc[4], sp[4];  // per channel e: -(1024 + z) or -(64 + z), and s, in both halves
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          // the quantisation group changes within the warp's 64 k only when G = 32 (at m = 2)
+          if (m == 0 || (L::kGR == 4 && m == 2)) {
+            const int gi = L::kGR == 1 ? 0 : ((64 * hk + 16 * m) >> LG);
+            const uint32_t zw = lds_u32(st + L::kOffZ + gi * (kStripWords * 4) + wj * 4) >> (16 * (g & 1));
+            uint32_t sv0, sv1;  // scales of channels 32 q + 4 g + {0, 1} and {2, 3}
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                         : "=r"(sv0), "=r"(sv1)
+                         : "r"(st + L::kOffS + gi * (kBM * 2) + (32 * q + 4 * g) * 2));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t v = (zw >> (4 * e)) & 15u;
+              // codes spliced as 1024 + q take -(1024 + z); codes spliced as 1024 + 16 q, scaled by
+              // 1/16, take -(64 + z)
+              zc[e] = (e & 1) ? (0xD400D400u | (v << 4) | (v << 20)) : (0xE400E400u | v | (v << 16));
+              const uint32_t sw = e < 2 ? sv0 : sv1;
+              sp[e] = prmt(sw, sw, (e & 1) ? 0x3232u : 0x1010u);
+            }
+          }
+          uint32_t w[4];
+#pragma unroll
+          for (int dd = 0; dd < 4; ++dd) {
+            // k = 64 hk + 16 m + 4 c + dd sits at tile row 32 dd + 16 hk + 4 m + c (64-byte rows,
+            // 16-byte chunk index XOR bits 1-2 of the row)
+            const int row = 32 * dd + 16 * hk + 4 * m + c;
+            w[dd] = lds_u32(st + L::kOffW + row * 64 + ((q ^ ((row >> 1) & 3)) << 4) + (g >> 1) * 4);
+          }
+          const uint32_t t01 = prmt(w[0], w[1], sel), t23 = prmt(w[2], w[3], sel);
+          const uint32_t t01h = t01 >> 8, t23h = t23 >> 8;
+          // channel e of the pair (k, k + 1) from t01 (column 8 m + 2 c) and (k + 2, k + 3) from t23
+          r0[4 * m + 0] = hmul2_u32(hadd2_u32(and_or(t01, 0x000F000Fu, kMagic), zc[0]), sp[0]);
+          r0[4 * m + 1] = hmul2_u32(hadd2_u32(and_or(t23, 0x000F000Fu, kMagic), zc[0]), sp[0]);
+          r0[4 * m + 2] = hmul2_u32(hfma2_u32(and_or(t01, 0x00F000F0u, kMagic), kSixteenth, zc[1]), sp[1]);
+          r0[4 * m + 3] = hmul2_u32(hfma2_u32(and_or(t23, 0x00F000F0u, kMagic), kSixteenth, zc[1]), sp[1]);
+          r1[4 * m + 0] = hmul2_u32(hadd2_u32(and_or(t01h, 0x000F000Fu, kMagic), zc[2]), sp[2]);
+          r1[4 * m + 1] = hmul2_u32(hadd2_u32(and_or(t23h, 0x000F000Fu, kMagic), zc[2]), sp[2]);
+          r1[4 * m + 2] = hmul2_u32(hfma2_u32(and_or(t01h, 0x00F000F0u, kMagic), kSixteenth, zc[3]), sp[3]);
+          r1[4 * m + 3] = hmul2_u32(hfma2_u32(and_or(t23h, 0x00F000F0u, kMagic), kSixteenth, zc[3]), sp[3]);
+        }
+        tmem_st_16x256b_x4(taddr0 + stage * 64, r0);
+        tmem_st_16x256b_x4(taddr1 + stage * 64, r1);
+        tmem_st_wait();
+        tc_fence_before_sync();  // the stores are ordered before the MMA thread's wait on afull
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
   } else if (warp < kEpiWarp0) {
-    // ---------------- dequantisers: packed int4 -> fp16 A operand ----------------
+    // ---------------- dequantisers: packed int4 -> fp16 A operand in shared memory ----------------
     const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
     const int j = d & 15, r0 = d >> 4;          // packed word column, first row (rows r0 + 16 i)
     const uint32_t aoff_col = (j >> 3) * L::kAAtom;
@@ -299,7 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue: TMEM -> fp16 -> global ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int i = quad * 32 + lane;
-    const int col_in_tile = 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);  // chunk order n0 n4 n1 n5 ...
+    // channel of TMEM lane i: A in TMEM, lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8; A in
+    // shared memory, rows follow the chunk order n0 n4 n1 n5 ...
+    const int col_in_tile = L::kTA ? 32 * (i >> 5) + 4 * (i & 7) + ((i >> 3) & 3)
+                                   : 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);
     grid_dependency_wait();  // y may still be read by the preceding kernel
     if (S == 1) {
       int it = 0;
@@ -460,8 +567,11 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
   CUtensorMap tx, tq, ts, tz;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B, err) ||
-      !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords, BK,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
+      !(BN <= 128  // A in TMEM: rows k = 4a + b as a 3D box {words, a, b}, so that b varies slowest
+            ? make_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N / 8, K / 4, 4, (uint64_t)N * 2,
+                           (uint64_t)N / 2, kStripWords, BK / 4, 4, CU_TENSOR_MAP_SWIZZLE_64B, err)
+            : make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords,
+                           BK, CU_TENSOR_MAP_SWIZZLE_NONE, err)) ||
       !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / group, (uint64_t)N * 2, kBM, GR,
                     CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
       !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qzeros, N / 8, K / group, (uint64_t)N / 2, kStripWords, GR,

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < L::kASlots; ++a) mbar_init(&afull[a], kCvWarps * 32);
+    for (int a = 0; a < L::kASlots; ++a) mbar_init(&afull[a], kCvWarps);  // one arrival per converter warp
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], kEpiWarps);
@@ -183,10 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const uint32_t xs_s = smem_u32(smem + stage * L::kStage);
             const uint32_t a_tmem = tmem_base + L::kAColBase + aslot * 64;
+            // the stage's B descriptors differ only in the start address field (bits 0-13, addr >> 4;
+            // shared-memory addresses stay below 2^18, so adding to it never carries)
+            const uint64_t bdesc0 = umma_sdesc_sw128(xs_s, 16, 1024);
 #pragma unroll
             for (int s = 0; s < kBK / 16; ++s) {
               // k16 step s: x box s / 4, 32 bytes per step along its 128-byte rows
-              const uint64_t bdesc = umma_sdesc_sw128(xs_s + (s >> 2) * L::kXBox + (s & 3) * 32, 16, 1024);
+              const uint64_t bdesc = bdesc0 + (uint64_t)(((s >> 2) * L::kXBox + (s & 3) * 32) >> 4);
               umma_f16_ta(d_tmem, a_tmem + s * 8, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
             }
             umma_commit(&empty[stage]);  // the stage and this block's A slot are free again
@@ -239,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_32x32b_x32(lane_addr + aslot * 64, a);
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&afull[aslot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[aslot]);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
