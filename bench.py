@@ -518,8 +518,8 @@ def run_sweep(args):
         nbytes = w4a16_bytes(M, K, N, G)
         reps = 20 if flops * len(stack) < 5e12 else 3
         sec = timed(fn, len(stack), reps)
-        bound = "hbm" if M <= 32 else "tensor"
-        row = "a2_w4a16_decode" if M < 33 else "a3_w4a16_prefill"
+        row = "a3_w4a16_prefill" if wql.w4a16_kernel_for(M, K, N) == "prefill" else "a2_w4a16_decode"
+        bound = "tensor" if flops / (bf16 * 1e12) > nbytes / (hbm * 1e9) else "hbm"  # the larger roofline time
         emit(row, f"{fam}:M{M}K{K}N{N}G{G}", sec, nbytes, flops, bound, {"copies": len(stack)})
         del x, y
     packed.clear()

@@ -96,6 +96,14 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
                           void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * w4a16_kernel_for: the kernel wql_w4a16_gemm runs for an M x K x N call on the current
+ * device: 0 = the weight-streaming decode kernel, 1 = the tcgen05 tensor-core kernel.  Up to
+ * 16 tokens it is always 0 and from 33 on always 1; in between it depends on N and K.
+ * Host-only, never fails (the WQL_FORCE_KERNEL benchmarking switch is not consulted).
+ * ---------------------------------------------------------------------------------------- */
+int wql_w4a16_kernel_for(int M, int K, int N);
+
+/* ----------------------------------------------------------------------------------------
  * qrmsnorm_quant_i8  [W8A8] QRMSNorm.forward + rms_norm_dynamic_quant / per_token_quant_int8.
  * Per row m of x [M, K] fp16, with gamma [K] fp16 (smoothing already folded in):
  *     ss   = sum_k x^2 in a fixed order: element k joins lane (k/8) % 256, lanes add in

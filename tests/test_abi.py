@@ -37,6 +37,12 @@ def test_host_only_entry_points(wql_lib):
     assert lib.wql_status_string(0) == b"ok"
     assert lib.wql_status_string(4) == b"device-side wait timed out"
     assert lib.wql_w8a8_workspace_bytes(16, 4096, 4096) >= 0
+    # kernel choice: decode up to 16 tokens, tcgen05 from 33, in between by shape
+    assert lib.wql_w4a16_kernel_for(1, 4096, 4096) == 0
+    assert lib.wql_w4a16_kernel_for(16, 4096, 22016) == 0
+    assert lib.wql_w4a16_kernel_for(33, 4096, 4096) == 1
+    assert lib.wql_w4a16_kernel_for(32, 11008, 4096) == 1   # long K: split-K pays
+    assert lib.wql_w4a16_kernel_for(32, 4096, 4096) == 0    # 32 output tiles: decode
 
 
 def test_validation_rejects_bad_arguments_without_a_gpu(wql_lib):

@@ -42,7 +42,8 @@ def row_rel_err(y, ref):
                                      # owner column ranges down to 4 tokens, and ragged token tails
                                      (20, 4096, 256, 32), (31, 4160, 2048, 64), (64, 4096, 8192, 128),
                                      (33, 8192, 1024, 128)])
-def test_w4a16_prefill_ragged(wql, M, K, N, G):
+def test_w4a16_prefill_ragged(wql, monkeypatch, M, K, N, G):
+    monkeypatch.setenv("WQL_FORCE_KERNEL", "prefill")  # below 33 tokens the choice depends on the shape
     W = inputs.weight(K, N, seed=2, outliers=True)
     X = inputs.activations(M, K, seed=2, outlier_channels=True)
     qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
@@ -51,6 +52,20 @@ def test_w4a16_prefill_ragged(wql, M, K, N, G):
     ref = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
     assert np.isfinite(y).all()
     assert row_rel_err(y[rows], ref) <= 1e-2
+    wql.device_status()
+
+
+@pytest.mark.parametrize("M,K,N,G,kernel", [(24, 4096, 12288, 64, "prefill"), (32, 11008, 4096, 128, "prefill"),
+                                            (32, 4096, 4096, 128, "decode"), (16, 4096, 12288, 32, "decode")])
+def test_w4a16_default_kernel_choice(wql, M, K, N, G, kernel):
+    # between 17 and 32 tokens w4a16_gemm picks the kernel by shape; the default path must be correct
+    assert wql.w4a16_kernel_for(M, K, N) == kernel
+    W = inputs.weight(K, N, seed=6, outliers=True)
+    X = inputs.activations(M, K, seed=6, outlier_channels=True)
+    qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
+    y = host(wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G))
+    rows = np.array([0, M // 2, M - 1], dtype=np.int64)
+    assert row_rel_err(y[rows], oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)) <= 1e-2
     wql.device_status()
 
 

@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     qrmsnorm_quant_i8,
     smooth,
     w4a16_gemm,
+    w4a16_kernel_for,
     w8a8_gemm,
     w8a8_gemm_noalloc,
     w8a8_workspace_bytes,
@@ -22,5 +23,5 @@ from ._lib import (  # noqa: F401
 
 __all__ = [
     "WQLError", "act_absmax", "awq_pack", "device_status", "load", "per_channel_quant_i8",
-    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w8a8_gemm", "w8a8_gemm_noalloc", "w8a8_workspace_bytes",
+    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w4a16_kernel_for", "w8a8_gemm", "w8a8_gemm_noalloc", "w8a8_workspace_bytes",
 ]

@@ -31,6 +31,7 @@ SIGNATURES = {
     "wql_device_status": (_I, [_P]),
     "wql_awq_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_w8a8_workspace_bytes": (_SZ, [_I, _I, _I]),
     "wql_w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
@@ -154,6 +155,11 @@ def qrmsnorm_quant_i8(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
     _check(load().wql_qrmsnorm_quant_i8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q), _ptr(xs), _stream(x.device)),
            "wql_qrmsnorm_quant_i8")
     return q, xs
+
+
+def w4a16_kernel_for(M: int, K: int, N: int) -> str:
+    """The kernel w4a16_gemm runs for this shape: "decode" or "prefill"."""
+    return "prefill" if load().wql_w4a16_kernel_for(M, K, N) else "decode"
 
 
 def w8a8_workspace_bytes(M: int, K: int, N: int) -> int:

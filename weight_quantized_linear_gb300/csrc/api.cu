@@ -133,7 +133,7 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
   const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode" or "prefill"
   const bool prefill = force && strcmp(force, "decode") == 0   ? false
                        : force && strcmp(force, "prefill") == 0 ? true
-                                                                : M >= wql::kW4A16PrefillMinM;
+                                                                : wql::w4a16_use_prefill(M, K, N);
   cudaError_t e = prefill ? wql::launch_w4a16_prefill(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
                                                       static_cast<cudaStream_t>(stream), &err)
                           : wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
@@ -141,6 +141,8 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
   if (!err.empty()) return fail(WQL_ECUDA, "wql_w4a16_gemm: " + err);
   return cuda_status(e, "wql_w4a16_gemm");
 }
+
+int wql_w4a16_kernel_for(int M, int K, int N) { return wql::w4a16_use_prefill(M, K, N) ? 1 : 0; }
 
 wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
                                  float* xs, void* stream) {

@@ -47,8 +47,22 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
                                  const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
                                  unsigned* dev_err, cudaStream_t s, std::string* err);
 
-// Token count from which w4a16_gemm uses the tcgen05 kernel instead of the streaming decode kernel.
+// Token count from which w4a16_gemm always uses the tcgen05 kernel instead of the streaming decode
+// kernel; from 17 tokens on it does so for the shapes w4a16_use_prefill picks.
 constexpr int kW4A16PrefillMinM = 33;
+
+// Kernel choice for w4a16_gemm.  Up to 16 tokens the decode kernel streams each weight tile once.
+// From 17 to 32 it runs two 16-token blocks, so every tile is dequantised twice; the tcgen05 kernel
+// (one 32-token tile) is then faster when its output tiles of 128 channels fill most SMs in one
+// wave, or when K is long enough for its split-K (measured on GB300, us, decode vs tcgen05 at
+// M = 32: K = 4096 with N = 4096: 7.8 / 9.3, N = 12288: 22.8 / 18.5, N = 22016: 30.0 / 35.3;
+// K = 11008, N = 4096: 17.8 / 16.4).
+inline bool w4a16_use_prefill(int M, int K, int N) {
+  if (M >= kW4A16PrefillMinM) return true;
+  if (M <= 16) return false;
+  const int ntn = (N + 127) / 128, sms = num_sms();
+  return K >= 8192 || (2 * ntn >= sms && ntn <= sms);
+}
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                                      int8_t* q, float* xs, unsigned* dev_err, cudaStream_t s);
