@@ -175,7 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem_base + b * BN;
           const int kb1 = (c + 1) * kChunkKB < nkb ? (c + 1) * kChunkKB : nkb;
           for (int kb = c * kChunkKB; kb < kb1; ++kb) {
-            if (!mbar_wait_bounded(&afull[aslot], aph) || !mbar_wait_bounded(&full[stage], phase)) {
+            // The converters wait for the stage's copies before they arrive on afull, so this wait
+            // also orders the x tile (one wait per stage instead of two: 372 -> 354 us at M = 4096,
+            // N = 11008)
+            if (!mbar_wait_bounded(&afull[aslot], aph)) {
               report_error(err, kErrTimeoutMma);
               ok = false;
               break;
