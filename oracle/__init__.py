@@ -49,6 +49,8 @@ _SIGS = {
     "wql_oracle_per_channel_quant_i8": (None, [_P, _I, _I, _P, _P]),
     "wql_oracle_w8a8_acc": (_I, [_P, _P, _I, _I, _P, _I, _P]),
     "wql_oracle_w8a8_epilogue": (None, [_P, _P, _P, _I, _I, _P]),
+    "wql_oracle_w8a8_epilogue_fused": (None, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "wql_oracle_add_qrmsnorm_quant_i8": (None, [_P, _P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_oracle_w8a8_epilogue_f64": (None, [_P, _P, _P, _I, _I, _P]),
     "wql_oracle_sym_int4_per_tensor": (_F, [_P, _I64, _P]),
 }
@@ -191,6 +193,18 @@ def qrmsnorm_quant_i8(X, gamma, eps: float):
     return q, xs
 
 
+def add_qrmsnorm_quant_i8(X, R, gamma, eps: float):
+    """Residual-fused QRMSNorm: returns (h fp16 [M, K] = fp16(x + r), q int8 [M, K], xs fp32 [M])."""
+    Xb, Rb = _half_bits(X), _half_bits(R)
+    M, K = Xb.shape
+    h = np.empty((M, K), np.uint16)
+    q = np.empty((M, K), np.int8)
+    xs = np.empty((M,), np.float32)
+    _load().wql_oracle_add_qrmsnorm_quant_i8(_ptr(Xb), _ptr(Rb), _ptr(_half_bits(gamma)), eps, M, K, _ptr(h),
+                                             _ptr(q), _ptr(xs))
+    return h.view(np.float16), q, xs
+
+
 def act_absmax(X, gamma, eps: float) -> np.ndarray:
     Xb = _half_bits(X)
     M, K = Xb.shape
@@ -241,6 +255,19 @@ def w8a8_epilogue(acc, xs, ws) -> np.ndarray:
     R, N = acc.shape
     y = np.empty((R, N), np.uint16)
     _load().wql_oracle_w8a8_epilogue(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)), R, N, _ptr(y))
+    return y.view(np.float16)
+
+
+def w8a8_epilogue_fused(acc, xs, ws, bias=None, residual=None) -> np.ndarray:
+    """fp16 [R, N] = fp16(((float(acc) * xs) * ws + bias) + residual); a None term is left out."""
+    acc = _c(acc, np.int32)
+    R, N = acc.shape
+    y = np.empty((R, N), np.uint16)
+    b = None if bias is None else _half_bits(bias).reshape(N)
+    r = None if residual is None else _half_bits(residual).reshape(R, N)
+    _load().wql_oracle_w8a8_epilogue_fused(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)),
+                                           None if b is None else _ptr(b), None if r is None else _ptr(r), R, N,
+                                           _ptr(y))
     return y.view(np.float16)
 
 

@@ -261,6 +261,20 @@ void wql_oracle_qrmsnorm_quant_i8(const uint16_t* X, const uint16_t* gamma, floa
 }
 
 /* [W8A8] calibration statistic used by smoothing: a_j = max_m |RMSNorm_gamma(X)_mj|. */
+/* [W8A8] "inference kernels": rms_norm_dynamic_quant with its residual fusion
+ * (add_rms_norm_quant_kernel).  Reading (the page names the fusion, not its arithmetic):
+ * h = fp16(float(x) + float(r)) -- one fp32 addition of the two fp16 values, rounded to fp16 --
+ * is the new residual stream H, and the row that is normalised and quantised, exactly as
+ * wql_oracle_qrmsnorm_quant_i8 does for an unfused input. */
+void wql_oracle_add_qrmsnorm_quant_i8(const uint16_t* X, const uint16_t* R, const uint16_t* gamma,
+                                     float eps, int M, int K, uint16_t* H, int8_t* q, float* xs) {
+  for (int64_t i = 0; i < (int64_t)M * K; ++i) {
+    float sum = wql_oracle_half_to_float(X[i]) + wql_oracle_half_to_float(R[i]);
+    H[i] = wql_oracle_float_to_half(sum);
+  }
+  wql_oracle_qrmsnorm_quant_i8(H, gamma, eps, M, K, q, xs);
+}
+
 void wql_oracle_act_absmax(const uint16_t* X, const uint16_t* gamma, float eps, int M, int K,
                            float* absmax) {
   float* y = (float*)malloc(sizeof(float) * (size_t)M * K);
@@ -341,6 +355,25 @@ void wql_oracle_w8a8_epilogue(const int32_t* acc, const float* xs, const float* 
       float c = (float)acc[(size_t)i * N + n];
       float t = c * xs[i];
       y[(size_t)i * N + n] = wql_oracle_float_to_half(t * ws[n]);
+    }
+}
+
+/* [W8A8] "inference kernels": matmul_kernel_dynamic_quant's _linear_add variant, with the
+ * optional bias and residual the page names.  Reading (the page names the fusion, not its
+ * arithmetic): the plain epilogue's fp32 value, then + bias[n], then + residual[i, n] (each an
+ * fp16 value widened to fp32), left to right, one rounding to fp16 at the end.  A NULL bias or
+ * residual leaves its term out altogether (adding 0.0 would turn a -0.0 result into +0.0). */
+void wql_oracle_w8a8_epilogue_fused(const int32_t* acc, const float* xs, const float* ws,
+                                    const uint16_t* bias, const uint16_t* residual, int nrows, int N,
+                                    uint16_t* y) {
+  for (int i = 0; i < nrows; ++i)
+    for (int n = 0; n < N; ++n) {
+      float c = (float)acc[(size_t)i * N + n];
+      float t = c * xs[i];
+      float u = t * ws[n];
+      if (bias) u = u + wql_oracle_half_to_float(bias[n]);
+      if (residual) u = u + wql_oracle_half_to_float(residual[(size_t)i * N + n]);
+      y[(size_t)i * N + n] = wql_oracle_float_to_half(u);
     }
 }
 

@@ -246,6 +246,26 @@ def test_qrmsnorm_closed_forms():
     assert np.array_equal(qa, qb) and np.array_equal(xa, xb)
 
 
+def test_add_qrmsnorm_residual_sum_and_special_cases():
+    # [W8A8] residual fusion: h = fp16(x + r) from an fp32 sum, then the unfused QRMSNorm of h
+    M, K = 6, 1024
+    X = inputs.activations(M, K, seed=11, outlier_channels=True)
+    R = inputs.activations(M, K, seed=12)
+    g = inputs.gamma(K, seed=11)
+    h, q, xs = oracle.add_qrmsnorm_quant_i8(X, R, g, inputs.EPS)
+    # the residual sum against numpy's own fp32 addition and round-to-nearest-even fp16 cast
+    assert np.array_equal(h.view(np.uint16), (X.astype(np.float32) + R.astype(np.float32)).astype(np.float16).view(np.uint16))
+    q2, xs2 = oracle.qrmsnorm_quant_i8(h, g, inputs.EPS)
+    assert np.array_equal(q, q2) and np.array_equal(xs, xs2)
+    # r = 0: the fused op is the plain QRMSNorm of x, bit for bit
+    h0, q0, xs0 = oracle.add_qrmsnorm_quant_i8(X, np.zeros_like(X), g, inputs.EPS)
+    qx, xsx = oracle.qrmsnorm_quant_i8(X, g, inputs.EPS)
+    assert np.array_equal(h0.view(np.uint16), X.view(np.uint16)) and np.array_equal(q0, qx) and np.array_equal(xs0, xsx)
+    # r = -x: every row cancels to zero, all codes 0 with scale 1
+    hz, qz, xsz = oracle.add_qrmsnorm_quant_i8(X, -X, g, inputs.EPS)
+    assert np.all(hz == 0) and np.all(qz == 0) and np.all(xsz == 1.0)
+
+
 def test_act_absmax_matches_float64_rmsnorm():
     M, K = 32, 1024
     X = inputs.activations(M, K, seed=3, outlier_channels=True)
@@ -328,6 +348,32 @@ def test_w8a8_epilogue_against_float64():
     y64 = acc.astype(np.float64) * xs[:, None].astype(np.float64) * ws[None, :].astype(np.float64)
     assert np.array_equal(oracle.w8a8_epilogue_f64(acc, xs, ws), y64)
     assert np.all(np.abs(y - y64) <= np.abs(y64) * (2.0 ** -11 + 2.0 ** -22) + 2.0 ** -25)
+
+
+def test_w8a8_fused_epilogue_bias_residual():
+    rng = np.random.default_rng(4)
+    R, N = 7, 96
+    acc = rng.integers(-2 ** 20, 2 ** 20, size=(R, N), dtype=np.int32)
+    xs = rng.uniform(0.001, 0.1, R).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    bias = rng.normal(0, 2, N).astype(np.float16)
+    res = rng.normal(0, 4, (R, N)).astype(np.float16)
+    # without the optional terms it is the plain epilogue, bit for bit
+    assert np.array_equal(oracle.w8a8_epilogue_fused(acc, xs, ws).view(np.uint16),
+                          oracle.w8a8_epilogue(acc, xs, ws).view(np.uint16))
+    # against the exact value: fp32 steps of relative size 2^-24 each, one fp16 rounding at the end
+    y = oracle.w8a8_epilogue_fused(acc, xs, ws, bias, res).astype(np.float64)
+    t64 = acc.astype(np.float64) * xs[:, None].astype(np.float64) * ws[None, :].astype(np.float64)
+    y64 = t64 + bias.astype(np.float64)[None, :] + res.astype(np.float64)
+    slack = (np.abs(t64) + np.abs(bias.astype(np.float64))[None, :] + np.abs(res.astype(np.float64))) * 2.0 ** -22
+    assert np.all(np.abs(y - y64) <= np.abs(y64) * 2.0 ** -11 + slack + 2.0 ** -24)
+    # closed forms with acc = 0: the result is the residual itself, bias + residual, or +0 when they cancel
+    z = np.zeros((R, N), np.int32)
+    assert np.array_equal(oracle.w8a8_epilogue_fused(z, xs, ws, residual=res).view(np.uint16), res.view(np.uint16))
+    assert np.array_equal(oracle.w8a8_epilogue_fused(z, xs, ws, bias=bias).view(np.uint16),
+                          np.broadcast_to(bias, (R, N)).view(np.uint16))
+    cancel = oracle.w8a8_epilogue_fused(z, xs, ws, bias=bias, residual=np.broadcast_to(-bias, (R, N)))
+    assert np.all(cancel.view(np.uint16) == 0)
 
 
 # ------------------------------------------------------------------------------------------------
