@@ -119,6 +119,19 @@ wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float
                                  int K, int8_t* q, float* xs, void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * add_qrmsnorm_quant_i8  [W8A8] "inference kernels": rms_norm_dynamic_quant with its residual
+ * fusion (add_rms_norm_quant_kernel).  The page names the fusion, not its arithmetic; reading:
+ *     h[m, k] = fp16(float(x[m, k]) + float(residual[m, k]))   (one fp32 add, one rounding)
+ * h is written to residual_out [M, K] fp16 (the new residual stream; residual_out may be the
+ * residual buffer itself), and q [M, K] int8, xs [M] fp32 are QRMSNorm + per-token int8 of h,
+ * exactly as wql_qrmsnorm_quant_i8 computes them for an input h.
+ * Requires K % 8 == 0, 8 <= K <= 16384; every pointer 16-byte aligned (xs: 4-byte).
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual,
+                                     const uint16_t* gamma, float eps, int M, int K,
+                                     uint16_t* residual_out, int8_t* q, float* xs, void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * w8a8_gemm  [W8A8] QLinear.forward / matmul_kernel_dynamic_quant.
  *     acc[m, n] = sum_k q[m, k] * qw[n, k]                 (exact int32)
  *     y[m, n]   = fp16((float(acc[m, n]) * xs[m]) * ws[n])  (fp32, left to right)
@@ -134,6 +147,20 @@ size_t wql_w8a8_workspace_bytes(int M, int K, int N);
 wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
                          int M, int K, int N, uint16_t* y, int32_t* acc_out, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * w8a8_gemm_fused  [W8A8] "inference kernels": the _linear_add variant of
+ * matmul_kernel_dynamic_quant with its optional bias and residual.  The page names the
+ * fusion, not its arithmetic; reading:
+ *     y[m, n] = fp16(((float(acc[m, n]) * xs[m]) * ws[n] + float(bias[n])) + float(residual[m, n]))
+ * in fp32, left to right, one rounding to fp16.  bias [N] fp16 and residual [M, N] fp16 are
+ * each optional (NULL leaves the term out); residual may be y itself (in place).  Everything
+ * else, including acc_out and the workspace, is as for wql_w8a8_gemm.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_w8a8_gemm_fused(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
+                               const uint16_t* bias, const uint16_t* residual, int M, int K, int N,
+                               uint16_t* y, int32_t* acc_out, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* ----------------------------------------------------------------------------------------
  * w8a8_gemm_noalloc -- the same operation as wql_w8a8_gemm (same kernels, same results) for

@@ -8,6 +8,7 @@ the first call does, and raises if it is missing.
 from ._lib import (  # noqa: F401
     WQLError,
     act_absmax,
+    add_qrmsnorm_quant_i8,
     awq_pack,
     device_status,
     load,
@@ -17,11 +18,12 @@ from ._lib import (  # noqa: F401
     w4a16_gemm,
     w4a16_kernel_for,
     w8a8_gemm,
+    w8a8_gemm_fused,
     w8a8_gemm_noalloc,
     w8a8_workspace_bytes,
 )
 
 __all__ = [
-    "WQLError", "act_absmax", "awq_pack", "device_status", "load", "per_channel_quant_i8",
-    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w4a16_kernel_for", "w8a8_gemm", "w8a8_gemm_noalloc", "w8a8_workspace_bytes",
+    "WQLError", "act_absmax", "add_qrmsnorm_quant_i8", "awq_pack", "device_status", "load", "per_channel_quant_i8",
+    "qrmsnorm_quant_i8", "smooth", "w4a16_gemm", "w4a16_kernel_for", "w8a8_gemm", "w8a8_gemm_fused", "w8a8_gemm_noalloc", "w8a8_workspace_bytes",
 ]

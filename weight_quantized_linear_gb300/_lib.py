@@ -33,9 +33,11 @@ SIGNATURES = {
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
+    "wql_add_qrmsnorm_quant_i8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
     "wql_w8a8_workspace_bytes": (_SZ, [_I, _I, _I]),
     "wql_w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "wql_w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "wql_w8a8_gemm_fused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "wql_act_absmax": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "wql_smooth": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P]),
     "wql_per_channel_quant_i8": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -157,6 +159,30 @@ def qrmsnorm_quant_i8(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
     return q, xs
 
 
+def add_qrmsnorm_quant_i8(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+                          residual_out: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                          xs: torch.Tensor | None = None):
+    """Residual-fused QRMSNorm: h = fp16(x + residual) -> (h [M, K] fp16, q int8 [M, K], xs fp32 [M]).
+
+    residual_out receives h (it may be `residual` itself, for an in-place update)."""
+    M, K = x.shape
+    _need(x, "x", torch.float16, (M, K))
+    _need(residual, "residual", torch.float16, (M, K))
+    _need(gamma, "gamma", torch.float16, (K,))
+    if residual_out is None:
+        residual_out = torch.empty((M, K), dtype=torch.float16, device=x.device)
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(residual_out, "residual_out", torch.float16, (M, K))
+    _need(q, "q", torch.int8, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _check(load().wql_add_qrmsnorm_quant_i8(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), M, K, _ptr(residual_out),
+                                            _ptr(q), _ptr(xs), _stream(x.device)), "wql_add_qrmsnorm_quant_i8")
+    return residual_out, q, xs
+
+
 def w4a16_kernel_for(M: int, K: int, N: int) -> str:
     """The kernel w4a16_gemm runs for this shape: "decode" or "prefill"."""
     return "prefill" if load().wql_w4a16_kernel_for(M, K, N) else "decode"
@@ -187,6 +213,37 @@ def w8a8_gemm(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch.Ten
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().wql_w8a8_gemm(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), M, K, N, _ptr(out), _ptr(acc_out),
                                 _ptr(workspace), ws_bytes, _stream(q.device)), "wql_w8a8_gemm")
+    return out
+
+
+def w8a8_gemm_fused(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch.Tensor,
+                    bias: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp16 = fp16(((float(q @ qw^T) * xs) * ws + bias) + residual); bias [N] and residual
+    [M, N] fp16 are optional (None leaves the term out); `out` may be `residual` (in place)."""
+    M, K = q.shape
+    N = qw.shape[0]
+    _need(q, "q", torch.int8, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _need(qw, "qw", torch.int8, (N, K))
+    _need(ws, "ws", torch.float32, (N,))
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,))
+    if residual is not None:
+        _need(residual, "residual", torch.float16, (M, N))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=q.device)
+    _need(out, "out", torch.float16, (M, N))
+    if acc_out is not None:
+        _need(acc_out, "acc_out", torch.int32, (M, N))
+    need = w8a8_workspace_bytes(M, K, N)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().wql_w8a8_gemm_fused(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), _ptr(bias), _ptr(residual), M, K, N,
+                                      _ptr(out), _ptr(acc_out), _ptr(workspace), ws_bytes, _stream(q.device)),
+           "wql_w8a8_gemm_fused")
     return out
 
 

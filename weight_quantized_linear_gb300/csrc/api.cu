@@ -162,14 +162,38 @@ wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float
                      "wql_qrmsnorm_quant_i8");
 }
 
+wql_status wql_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps,
+                                     int M, int K, uint16_t* residual_out, int8_t* q, float* xs, void* stream) {
+  WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (K > 16384) return fail(WQL_EUNSUPPORTED, "K > 16384 is not supported by the register-resident row kernel");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(x);
+  WQL_REQUIRE_PTR(residual);
+  WQL_REQUIRE_PTR(gamma);
+  WQL_REQUIRE_PTR(residual_out);
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  return cuda_status(wql::launch_add_qrmsnorm_quant_i8(x, residual, gamma, eps, M, K, residual_out, q, xs,
+                                                       device_error_word(), static_cast<cudaStream_t>(stream)),
+                     "wql_add_qrmsnorm_quant_i8");
+}
+
 size_t wql_w8a8_workspace_bytes(int M, int K, int N) {
   (void)N;
   if (M < wql::kW8A8PrefillMinM || K <= 0) return 0;  // the streaming decode kernel needs no scratch
   return wql::w8a8_prefill_workspace_bytes(M, K);      // fp16 copy of the activation codes
 }
 
-wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K, int N,
-                         uint16_t* y, int32_t* acc_out, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// wql_w8a8_gemm and wql_w8a8_gemm_fused: one validation and dispatch path.
+wql_status w8a8_gemm(const char* fn, const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
+                     const uint16_t* bias, const uint16_t* residual, int M, int K, int N, uint16_t* y,
+                     int32_t* acc_out, void* workspace, size_t workspace_bytes, void* stream) {
   WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
   WQL_REQUIRE(K <= 131072, "K must be <= 131072 so that the int32 accumulator cannot overflow");
   WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
@@ -184,6 +208,8 @@ wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, con
   WQL_REQUIRE_PTR(y);
   WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
   WQL_REQUIRE(acc_out == nullptr || aligned16(acc_out), "acc_out must be NULL or 16-byte aligned");
+  WQL_REQUIRE(bias == nullptr || aligned16(bias), "bias must be NULL or 16-byte aligned");
+  WQL_REQUIRE(residual == nullptr || aligned16(residual), "residual must be NULL or 16-byte aligned");
   const size_t need = wql_w8a8_workspace_bytes(M, K, N);
   WQL_REQUIRE(workspace_bytes >= need, "workspace is smaller than wql_w8a8_workspace_bytes()");
   WQL_REQUIRE(need == 0 || (workspace != nullptr && aligned16(workspace)), "workspace must be 16-byte aligned");
@@ -191,12 +217,27 @@ wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, con
   std::string err;
   const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode" or "prefill"
   const bool prefill = force && strcmp(force, "decode") == 0 ? false : M >= wql::kW8A8PrefillMinM;
-  cudaError_t e = prefill ? wql::launch_w8a8_prefill(q, xs, qw, ws, M, K, N, y, acc_out, workspace, dev_err,
-                                                     static_cast<cudaStream_t>(stream), &err)
-                          : wql::launch_w8a8_decode(q, xs, qw, ws, M, K, N, y, acc_out, dev_err,
+  cudaError_t e = prefill ? wql::launch_w8a8_prefill(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, workspace,
+                                                     dev_err, static_cast<cudaStream_t>(stream), &err)
+                          : wql::launch_w8a8_decode(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, dev_err,
                                                     static_cast<cudaStream_t>(stream), &err);
-  if (!err.empty()) return fail(WQL_ECUDA, "wql_w8a8_gemm: " + err);
-  return cuda_status(e, "wql_w8a8_gemm");
+  if (!err.empty()) return fail(WQL_ECUDA, std::string(fn) + ": " + err);
+  return cuda_status(e, fn);
+}
+
+}  // namespace
+
+wql_status wql_w8a8_gemm(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K, int N,
+                         uint16_t* y, int32_t* acc_out, void* workspace, size_t workspace_bytes, void* stream) {
+  return w8a8_gemm("wql_w8a8_gemm", q, xs, qw, ws, nullptr, nullptr, M, K, N, y, acc_out, workspace,
+                   workspace_bytes, stream);
+}
+
+wql_status wql_w8a8_gemm_fused(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
+                               const uint16_t* bias, const uint16_t* residual, int M, int K, int N, uint16_t* y,
+                               int32_t* acc_out, void* workspace, size_t workspace_bytes, void* stream) {
+  return w8a8_gemm("wql_w8a8_gemm_fused", q, xs, qw, ws, bias, residual, M, K, N, y, acc_out, workspace,
+                   workspace_bytes, stream);
 }
 
 wql_status wql_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,

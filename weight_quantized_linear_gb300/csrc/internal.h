@@ -67,6 +67,10 @@ inline bool w4a16_use_prefill(int M, int K, int N) {
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                                      int8_t* q, float* xs, unsigned* dev_err, cudaStream_t s);
 
+cudaError_t launch_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma,
+                                         float eps, int M, int K, uint16_t* residual_out, int8_t* q, float* xs,
+                                         unsigned* dev_err, cudaStream_t s);
+
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                               float* absmax, unsigned* dev_err, cudaStream_t s);
 
@@ -79,12 +83,14 @@ cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw
 // Token count from which w8a8_gemm uses the tcgen05 kernel (which needs the workspace).
 constexpr int kW8A8PrefillMinM = 17;
 size_t w8a8_prefill_workspace_bytes(int M, int K);
+// bias [N] and residual [M, N] (fp16, either may be null) are the optional epilogue terms
+// y = fp16(((acc * xs) * ws + bias) + residual).
 cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
-                                int N, uint16_t* y, int32_t* acc_out, void* workspace, unsigned* dev_err,
-                                cudaStream_t stream, std::string* err);
+                                int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
+                                void* workspace, unsigned* dev_err, cudaStream_t stream, std::string* err);
 
 cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws,
-                               int M, int K, int N, uint16_t* y, int32_t* acc_out, unsigned* dev_err,
-                               cudaStream_t s, std::string* err);
+                               int M, int K, int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias,
+                               const uint16_t* residual, unsigned* dev_err, cudaStream_t s, std::string* err);
 
 }  // namespace wql

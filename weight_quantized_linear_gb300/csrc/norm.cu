@@ -38,7 +38,9 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                : "memory");
 }
 
-constexpr int kNormSlots = 4;  // rows in flight per CTA
+// Rows in flight per CTA: four, or three when each slot holds two long rows (MODE 2, K > 8192).
+__host__ __device__ constexpr int norm_slots(int cpt, int mode) { return (mode == 2 && cpt > 4) ? 3 : 4; }
+__host__ __device__ constexpr int norm_rows_per_slot(int mode) { return mode == 2 ? 2 : 1; }
 
 // Round to the nearest integer (ties to even) and saturate to [-128, 127], in one conversion.
 __device__ __forceinline__ int cvt_rni_sat_s8(float f) {
@@ -91,26 +93,35 @@ __device__ __forceinline__ bool row_sum_vote(float p, bool ok, float* red, float
   return true;
 }
 
-// MODE 0: quantise (q, xs); MODE 1: per-channel absmax of the norm output (atomic max into absmax).
+// MODE 0: quantise (q, xs); MODE 1: per-channel absmax of the norm output (atomic max into absmax);
+// MODE 2: add the residual first ("LMDeploy W8A8 quantisation guide", inference kernels: the
+// residual fusion of rms_norm_dynamic_quant): h = fp16(fp32(x) + fp32(r)) is stored to h_out (the
+// new residual; it may be the residual buffer itself) and normalised and quantised as in MODE 0.
 // Persistent CTAs: CTA b normalises rows b, b + gridDim.x, ...  Thread 0 keeps kNormSlots rows in
 // flight with bulk copies into a shared-memory ring, so HBM reads continue through every row's
 // reductions; a slot is refilled as soon as all threads have read it (the first barrier of the
 // row's sum).
 template <int CPT, int MODE>
-__global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? 4 : 1)
-    qrmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma, float eps, int M, int K,
-                    int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax, unsigned* err) {
+// (the residual mode holds the new residual across the row sum: three CTAs per SM, no spill)
+__global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) : 1)
+    qrmsnorm_kernel(const __half* __restrict__ x, const __half* residual, const __half* __restrict__ gamma, float eps,
+                    int M, int K, int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax,
+                    __half* h_out, unsigned* err) {
+  constexpr int kNormSlots = norm_slots(CPT, MODE), kRowsPerSlot = norm_rows_per_slot(MODE);
   __shared__ float red[272];  // [0, 256) lane partials, 256 row sum, [264, 272) warp maxima
   __shared__ __align__(8) uint64_t full[kNormSlots];
-  extern __shared__ __align__(16) uint8_t rows[];  // kNormSlots x 2K bytes
+  extern __shared__ __align__(16) uint8_t rows[];  // kNormSlots x kRowsPerSlot x 2K bytes
   const int tid = threadIdx.x;
   const int nchunks = K >> 3;
   const uint32_t row_bytes = 2u * (uint32_t)K;
+  const uint32_t slot_bytes = kRowsPerSlot * row_bytes;
   const int nrows = M > (int)blockIdx.x ? (M - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  auto issue = [&](int j) {  // row j of this CTA into slot j % kNormSlots
+  auto issue = [&](int j) {  // row j of this CTA (and its residual row) into slot j % kNormSlots
     const int s = j % kNormSlots;
-    mbar_arrive_expect_tx(&full[s], row_bytes);
-    bulk_load(rows + (size_t)s * row_bytes, x + (size_t)(blockIdx.x + (size_t)j * gridDim.x) * K, row_bytes, &full[s]);
+    const size_t off = (size_t)(blockIdx.x + (size_t)j * gridDim.x) * K;
+    mbar_arrive_expect_tx(&full[s], slot_bytes);
+    bulk_load(rows + (size_t)s * slot_bytes, x + off, row_bytes, &full[s]);
+    if constexpr (MODE == 2) bulk_load(rows + (size_t)s * slot_bytes + row_bytes, residual + off, row_bytes, &full[s]);
   };
   if (tid == 0) {
     for (int s = 0; s < kNormSlots; ++s) mbar_init(&full[s], 1);
@@ -144,14 +155,25 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? 4 : 1)
     // Every thread waits; the row sum's barrier votes, so that all threads leave together if a wait
     // ever expires (the values read from an unfinished slot are then discarded).
     const bool ok = mbar_wait_bounded(&full[s], (j / kNormSlots) & 1);
-    const uint4* xr = reinterpret_cast<const uint4*>(rows + (size_t)s * row_bytes);
-    float yv[CPT][8];  // x, then the normalised row
+    const uint4* xr = reinterpret_cast<const uint4*>(rows + (size_t)s * slot_bytes);
+    float yv[CPT][8];  // x (MODE 2: x + r as fp16), then the normalised row
+    uint4 hv[MODE == 2 ? CPT : 1];  // MODE 2: the new residual, stored once the row's wait is confirmed
     float p = 0.f;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
-        const uint4 xv = xr[c];
+        uint4 xv = xr[c];
+        if constexpr (MODE == 2) {
+          const uint4 rv = reinterpret_cast<const uint4*>(rows + (size_t)s * slot_bytes + row_bytes)[c];
+          const __half* xh = reinterpret_cast<const __half*>(&xv);
+          const __half* rh = reinterpret_cast<const __half*>(&rv);
+          __align__(16) __half hh[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) hh[e] = __float2half_rn(__fadd_rn(__half2float(xh[e]), __half2float(rh[e])));
+          hv[i] = *reinterpret_cast<const uint4*>(hh);
+          xv = hv[i];
+        }
         const __half* h = reinterpret_cast<const __half*>(&xv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -168,6 +190,13 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? 4 : 1)
     }
     // every thread has read slot s (it passed the sum's barrier): refill it
     if (tid == 0 && j + kNormSlots < nrows) issue(j + kNormSlots);
+    if constexpr (MODE == 2) {
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = tid + kNormThreads * i;
+        if (c < nchunks) *reinterpret_cast<uint4*>(h_out + (size_t)m * K + 8 * c) = hv[i];
+      }
+    }
     const float mean = __fdiv_rn(ss, (float)K);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 
@@ -250,10 +279,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 template <int CPT, int MODE>
-cudaError_t launch_rows(const __half* x, const __half* gamma, float eps, int M, int K, int8_t* q, float* xs,
-                        float* absmax, unsigned* err, cudaStream_t s) {
+cudaError_t launch_rows(const __half* x, const __half* residual, const __half* gamma, float eps, int M, int K,
+                        int8_t* q, float* xs, float* absmax, __half* h_out, unsigned* err, cudaStream_t s) {
   auto kern = qrmsnorm_kernel<CPT, MODE>;
-  const size_t smem = (size_t)kNormSlots * 2 * K;
+  const size_t smem = (size_t)norm_slots(CPT, MODE) * norm_rows_per_slot(MODE) * 2 * K;
   static int set_bytes[64] = {0};   // dynamic shared memory limit set on the kernel, per device
   static int fit_bytes[64] = {0};   // ring size of the cached occupancy
   static int fit_ctas[64] = {0};
@@ -274,26 +303,34 @@ cudaError_t launch_rows(const __half* x, const __half* gamma, float eps, int M, 
   }
   const long long cap = (long long)fit_ctas[dev] * num_sms();
   const dim3 grid((unsigned)(M < cap ? M : cap)), block(kNormThreads);
-  return launch_pdl(kern, grid, block, smem, s, x, gamma, eps, M, K, q, xs, absmax, err);
+  return launch_pdl(kern, grid, block, smem, s, x, residual, gamma, eps, M, K, q, xs, absmax, h_out, err);
 }
 
 template <int MODE>
-cudaError_t launch_norm(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q, float* xs,
-                        float* absmax, unsigned* err, cudaStream_t s) {
+cudaError_t launch_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps, int M, int K,
+                        int8_t* q, float* xs, float* absmax, uint16_t* h_out, unsigned* err, cudaStream_t s) {
   const __half* xh = reinterpret_cast<const __half*>(x);
+  const __half* rh = reinterpret_cast<const __half*>(residual);
   const __half* gh = reinterpret_cast<const __half*>(gamma);
+  __half* hh = reinterpret_cast<__half*>(h_out);
   const int cpt = (K + 2047) / 2048;
-  if (cpt <= 1) return launch_rows<1, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
-  if (cpt <= 2) return launch_rows<2, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
-  if (cpt <= 4) return launch_rows<4, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
-  return launch_rows<8, MODE>(xh, gh, eps, M, K, q, xs, absmax, err, s);
+  if (cpt <= 1) return launch_rows<1, MODE>(xh, rh, gh, eps, M, K, q, xs, absmax, hh, err, s);
+  if (cpt <= 2) return launch_rows<2, MODE>(xh, rh, gh, eps, M, K, q, xs, absmax, hh, err, s);
+  if (cpt <= 4) return launch_rows<4, MODE>(xh, rh, gh, eps, M, K, q, xs, absmax, hh, err, s);
+  return launch_rows<8, MODE>(xh, rh, gh, eps, M, K, q, xs, absmax, hh, err, s);
 }
 
 }  // namespace
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
                                      float* xs, unsigned* dev_err, cudaStream_t s) {
-  return launch_norm<0>(x, gamma, eps, M, K, q, xs, nullptr, dev_err, s);
+  return launch_norm<0>(x, nullptr, gamma, eps, M, K, q, xs, nullptr, nullptr, dev_err, s);
+}
+
+cudaError_t launch_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma,
+                                         float eps, int M, int K, uint16_t* residual_out, int8_t* q, float* xs,
+                                         unsigned* dev_err, cudaStream_t s) {
+  return launch_norm<2>(x, residual, gamma, eps, M, K, q, xs, nullptr, residual_out, dev_err, s);
 }
 
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,
@@ -301,7 +338,7 @@ cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float ep
   cudaError_t e = cudaMemsetAsync(absmax, 0, sizeof(float) * (size_t)K, s);
   if (e != cudaSuccess) return e;
   if (M == 0) return cudaSuccess;
-  return launch_norm<1>(x, gamma, eps, M, K, nullptr, nullptr, absmax, dev_err, s);
+  return launch_norm<1>(x, nullptr, gamma, eps, M, K, nullptr, nullptr, absmax, nullptr, dev_err, s);
 }
 
 }  // namespace wql

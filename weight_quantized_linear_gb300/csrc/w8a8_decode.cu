@@ -14,6 +14,7 @@
 // 128 output channels x 64 k stream once from HBM through a TMA pipeline; split-K across the
 // CTAs of a cluster, reduced through distributed shared memory in int32.
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace wql {
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
     w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] int8, box {64, 8MT}, SW64
                        const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] int8, box {64, 128}, SW64
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int kblocks,
-                       __half* __restrict__ y, int32_t* __restrict__ acc_out, unsigned* err) {
+                       __half* __restrict__ y, int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = Layout8<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
         const float wv[4] = {wn.x, wn.y, wn.z, wn.w};
         __align__(8) __half hv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hv[e] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(iv[e]), xm), wv[e]));
+        for (int e = 0; e < 4; ++e)
+          hv[e] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(__int2float_rn(iv[e]), xm), wv[e]), ea, m, n + e, N));
         *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = *reinterpret_cast<const uint2*>(hv);
         if (acc_out) *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) = v;
       }
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
 
 template <int MT>
 cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* xs, const float* ws, int M, int N,
-                    int kblocks, __half* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream) {
+                    int kblocks, __half* y, int32_t* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream) {
   using L = Layout8<MT>;
   // 8- and 16-token launches take the same shared-memory footprint, so that back-to-back layers
   // look alike to the block scheduler whatever their token counts: it then keeps one CTA of each
@@ -285,15 +287,16 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, w8a8_decode_kernel<MT>, tx, tw, xs, ws, M, N, kblocks, y, acc_out, dev_err);
+  return cudaLaunchKernelEx(&cfg, w8a8_decode_kernel<MT>, tx, tw, xs, ws, M, N, kblocks, y, acc_out, ea, dev_err);
 }
 
 }  // namespace
 
 cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
-                               int N, uint16_t* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream,
-                               std::string* err) {
+                               int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
+                               unsigned* dev_err, cudaStream_t stream, std::string* err) {
   const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+  const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
   CUtensorMap tx, tw;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, K, M, (uint64_t)K, kBK, 8 * MT,
                     CU_TENSOR_MAP_SWIZZLE_64B, err) ||
@@ -305,11 +308,11 @@ cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* q
   __half* yh = reinterpret_cast<__half*>(y);
   switch (MT) {
     case 1:
-      return launch8<1>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+      return launch8<1>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
     case 2:
-      return launch8<2>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+      return launch8<2>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
     default:
-      return launch8<4>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, dev_err, stream);
+      return launch8<4>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
   }
 }
 

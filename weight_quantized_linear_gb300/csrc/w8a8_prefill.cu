@@ -19,6 +19,7 @@
 //     The tile's last chunk yields acc (written to acc_out if requested) and
 //     y = fp16((float(acc) * xs[m]) * ws[n]).
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w8a8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // fp16 codes [M][K], box {64, BN}, SW128
                         const __grid_constant__ CUtensorMap tm_w,  // qw int8 [N][K], box {64, 128}
                         const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
-                        __half* __restrict__ y, int32_t* __restrict__ acc_out, unsigned* err) {
+                        __half* __restrict__ y, int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = QLayout<BN>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -296,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int m = mbase + k;
               if (m < M) {
                 const int a = (int)sacc[k];
-                y[(size_t)m * N + n] = __float2half_rn(__fmul_rn(__fmul_rn(__int2float_rn(a), xs[m]), wn));
+                y[(size_t)m * N + n] =
+                    __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(__int2float_rn(a), xs[m]), wn), ea, m, n, N));
                 if (acc_out) acc_out[(size_t)m * N + n] = a;
               }
             }
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const float* xs, const float* ws, int M, int N,
-                     int K, __half* y, int32_t* acc_out, unsigned* dev_err, cudaStream_t stream) {
+                     int K, __half* y, int32_t* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream) {
   using L = QLayout<BN>;
   auto kern = w8a8_prefill_kernel<BN>;
   static bool attr_set[64] = {false};
@@ -330,7 +332,7 @@ cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const float* 
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, y, acc_out, dev_err);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, y, acc_out, ea, dev_err);
   return cudaGetLastError();
 }
 
@@ -339,8 +341,9 @@ cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const float* 
 size_t w8a8_prefill_workspace_bytes(int M, int K) { return (size_t)M * (size_t)K * 2; }
 
 cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
-                                int N, uint16_t* y, int32_t* acc_out, void* workspace, unsigned* dev_err,
-                                cudaStream_t stream, std::string* err) {
+                                int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
+                                void* workspace, unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
   // 1. activation codes -> exact fp16 in the workspace
   __half* xh = reinterpret_cast<__half*>(workspace);
   const long long n16 = (long long)M * K / 16;
@@ -359,8 +362,8 @@ cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* 
     return cudaErrorInvalidValue;
   }
   __half* yh = reinterpret_cast<__half*>(y);
-  if (BN == 64) return launch_q<64>(tx, tw, xs, ws, M, N, K, yh, acc_out, dev_err, stream);
-  return launch_q<128>(tx, tw, xs, ws, M, N, K, yh, acc_out, dev_err, stream);
+  if (BN == 64) return launch_q<64>(tx, tw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream);
+  return launch_q<128>(tx, tw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream);
 }
 
 }  // namespace wql
