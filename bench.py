@@ -57,6 +57,11 @@ def qrmsnorm_bytes(M, K):
     return 2 * M * K + 2 * K + M * K + 4 * M
 
 
+def add_qrmsnorm_bytes(M, K):
+    # x and the residual in, the new residual h out, then the QRMSNorm of h
+    return 2 * M * K + 2 * M * K + 2 * M * K + 2 * K + M * K + 4 * M
+
+
 def gemm_flops(M, K, N):
     return 2 * M * K * N
 
@@ -579,7 +584,24 @@ def run_sweep(args):
             secb = timed(block, copies, reps)
             emit("a4+a6_w8a8_block", f"M{M}K{K}N{N}", secb, qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N), flops,
                  "hbm" if M <= 16 else "tensor")
-            del stack, y, wsp, X, q, xs, qW, ws, a, s_, g2
+
+            # the same block with its residual and bias fusions: h = x + r feeds the norm, and the GEMM
+            # adds a bias [N] and a residual [M, N] before its single rounding to fp16
+            R = torch.from_numpy(inputs.activations(M, K, seed=1)).to(dev)
+            H = torch.empty_like(R)
+            bias = torch.from_numpy(inputs.activations(1, N, seed=2)[0]).to(dev)
+            RY = torch.from_numpy(inputs.activations(M, N, seed=3)).to(dev)
+
+            def fused(stack=stack, X=X, R=R, H=H, g2=g2, q=q, xs=xs, ws=ws, bias=bias, RY=RY, y=y, wsp=wsp):
+                for w in stack:
+                    wql.add_qrmsnorm_quant_i8(X, R, g2, inputs.EPS, residual_out=H, q=q, xs=xs)
+                    wql.w8a8_gemm_fused(q, xs, w, ws, bias, RY, out=y, workspace=wsp)
+
+            secf = timed(fused, copies, reps)
+            emit("f1_w8a8_fused_block", f"M{M}K{K}N{N}", secf,
+                 add_qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N) + 2 * N + 2 * M * N, flops,
+                 "hbm" if M <= 16 else "tensor", {"unfused_us": round(secb * 1e6, 3)})
+            del stack, y, wsp, X, q, xs, qW, ws, a, s_, g2, R, H, bias, RY
 
     # a5 per-channel weight quantisation (offline prep)
     W = weight(4096, 11008, False)
