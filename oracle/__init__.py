@@ -53,6 +53,13 @@ _SIGS = {
     "wql_oracle_add_qrmsnorm_quant_i8": (None, [_P, _P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_oracle_w8a8_epilogue_f64": (None, [_P, _P, _P, _I, _I, _P]),
     "wql_oracle_sym_int4_per_tensor": (_F, [_P, _I64, _P]),
+    "wql_oracle_e4m3_to_float_n": (None, [_P, _P, _I64]),
+    "wql_oracle_float_to_e4m3_n": (None, [_P, _P, _I64]),
+    "wql_oracle_qrmsnorm_quant_fp8": (None, [_P, _P, _F, _I, _I, _P, _P]),
+    "wql_oracle_add_qrmsnorm_quant_fp8": (None, [_P, _P, _P, _F, _I, _I, _P, _P, _P]),
+    "wql_oracle_per_channel_quant_fp8": (None, [_P, _I, _I, _P, _P]),
+    "wql_oracle_fp8_acc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
+    "wql_oracle_fp8_epilogue_f64": (None, [_P, _P, _P, _P, _P, _I, _I, _P]),
 }
 
 
@@ -276,6 +283,88 @@ def w8a8_epilogue_f64(acc, xs, ws) -> np.ndarray:
     R, N = acc.shape
     y = np.empty((R, N), np.float64)
     _load().wql_oracle_w8a8_epilogue_f64(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)), R, N, _ptr(y))
+    return y
+
+
+# ---- SmoothQuant W8A8, fp8 (e4m3) variant --------------------------------------------------
+
+def _e4m3_bits(a) -> np.ndarray:
+    """float8_e4m3fn codes as uint8 (torch float8 tensors are passed as their uint8 view)."""
+    a = np.asarray(a)
+    assert a.dtype == np.uint8, "e4m3 data must be its uint8 bit pattern"
+    return np.ascontiguousarray(a)
+
+
+def e4m3_to_float(b) -> np.ndarray:
+    b = _e4m3_bits(b)
+    out = np.empty(b.shape, np.float32)
+    _load().wql_oracle_e4m3_to_float_n(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+def float_to_e4m3(x) -> np.ndarray:
+    """Nearest e4m3 code (ties to even, saturating at +-448) of fp32 values, as uint8."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().wql_oracle_float_to_e4m3_n(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def qrmsnorm_quant_fp8(X, gamma, eps: float):
+    """Returns (q e4m3 codes uint8 [M, K], xs fp32 [M]) with xs = absmax / 448."""
+    Xb = _half_bits(X)
+    M, K = Xb.shape
+    q = np.empty((M, K), np.uint8)
+    xs = np.empty((M,), np.float32)
+    _load().wql_oracle_qrmsnorm_quant_fp8(_ptr(Xb), _ptr(_half_bits(gamma)), eps, M, K, _ptr(q), _ptr(xs))
+    return q, xs
+
+
+def add_qrmsnorm_quant_fp8(X, R, gamma, eps: float):
+    """Residual-fused fp8 QRMSNorm: returns (h fp16 [M, K], q e4m3 uint8 [M, K], xs fp32 [M])."""
+    Xb, Rb = _half_bits(X), _half_bits(R)
+    M, K = Xb.shape
+    h = np.empty((M, K), np.uint16)
+    q = np.empty((M, K), np.uint8)
+    xs = np.empty((M,), np.float32)
+    _load().wql_oracle_add_qrmsnorm_quant_fp8(_ptr(Xb), _ptr(Rb), _ptr(_half_bits(gamma)), eps, M, K, _ptr(h),
+                                              _ptr(q), _ptr(xs))
+    return h.view(np.float16), q, xs
+
+
+def per_channel_quant_fp8(W):
+    """W [K, N] fp32 -> (qW e4m3 uint8 [N, K], ws fp32 [N]) with ws = absmax / 448."""
+    W = _c(W, np.float32)
+    K, N = W.shape
+    qW = np.empty((N, K), np.uint8)
+    ws = np.empty((N,), np.float32)
+    _load().wql_oracle_per_channel_quant_fp8(_ptr(W), K, N, _ptr(qW), _ptr(ws))
+    return qW, ws
+
+
+def fp8_acc(q, qW, rows=None):
+    """Exact fp64 sums [len(rows), N] of e4m3 q [M, K] times qW [N, K]^T, and the sums of |products|."""
+    q = _e4m3_bits(q)
+    qW = _e4m3_bits(qW)
+    M, K = q.shape
+    N = qW.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    acc = np.empty((rows.size, N), np.float64)
+    absacc = np.empty((rows.size, N), np.float64)
+    if _load().wql_oracle_fp8_acc(_ptr(q), _ptr(qW), K, N, _ptr(rows), rows.size, _ptr(acc), _ptr(absacc)):
+        raise ValueError("fp8 GEMM reference: K > 65536 or a NaN code")
+    return acc, absacc
+
+
+def fp8_epilogue_f64(acc, xs, ws, bias=None, residual=None) -> np.ndarray:
+    """fp64 [R, N] = ((acc * xs) * ws + bias) + residual, unrounded; a None term is left out."""
+    acc = _c(acc, np.float64)
+    R, N = acc.shape
+    y = np.empty((R, N), np.float64)
+    b = None if bias is None else _half_bits(bias).reshape(N)
+    r = None if residual is None else _half_bits(residual).reshape(R, N)
+    _load().wql_oracle_fp8_epilogue_f64(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)),
+                                        None if b is None else _ptr(b), None if r is None else _ptr(r), R, N, _ptr(y))
     return y
 
 

@@ -18,7 +18,9 @@
  *          alpha = 0.5), "QRMSNorm / QLinear" (per-token dynamic quant, per-channel weight
  *          quant with fp32 scales) and "inference kernels" (per_token_quant_int8: scale =
  *          absmax / Q_MAX with Q_MAX = 127 for int8, values rounded to integers;
- *          matmul_kernel_dynamic_quant: int32 accumulator, c = c * rms_scale * linear_scale).
+ *          matmul_kernel_dynamic_quant: int32 accumulator, c = c * rms_scale * linear_scale),
+ *          and its fp8 variant (quant_dtype fp8 = float8_e4m3fn, Q_MAX from torch.finfo, values
+ *          cast instead of rounded to integers, fp32 accumulator).
  *
  * Readings taken where the pages are silent (each one is listed in the design notes):
  *   - zero point is an integer z in [0,15] stored 8 per uint32 like the codes; w ~ (q - z) * s;
@@ -30,7 +32,8 @@
  *     stored as fp16 before quantisation); the sum of squares follows the fixed order of
  *     wql_oracle_sumsq below so that int8 codes can be compared bit for bit;
  *   - an all-zero row gets scale 1.0 (all codes 0); weights are clamped to [-127, 127];
- *   - smoothing statistics are the per-channel absmax of RMSNorm_gamma(X) on the same batch.
+ *   - smoothing statistics are the per-channel absmax of RMSNorm_gamma(X) on the same batch;
+ *   - the fp8 cast rounds to the nearest e4m3 value (ties to even) and saturates at +-448.
  */
 #include <math.h>
 #include <stdint.h>
@@ -383,6 +386,169 @@ void wql_oracle_w8a8_epilogue_f64(const int32_t* acc, const float* xs, const flo
   for (int i = 0; i < nrows; ++i)
     for (int n = 0; n < N; ++n)
       y[(size_t)i * N + n] = (double)acc[(size_t)i * N + n] * (double)xs[i] * (double)ws[n];
+}
+
+/* ---------------------------------------------------------------------------------------
+ * [W8A8] FP8 variant: quant_dtype "fp8", the short name of float8_e4m3fn.  The format, from
+ * its definition: 1 sign bit, 4 exponent bits with bias 7, 3 fraction bits; exponent field 0
+ * holds the subnormals, in units of 2^-9; there is no infinity and only S.1111.111 is NaN, so
+ * the largest finite magnitude is 1.75 * 2^8 = 448 -- the Q_MAX that torch.finfo gives.
+ * ------------------------------------------------------------------------------------- */
+float wql_oracle_e4m3_to_float(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, f = b & 7;
+  double v;
+  if (e == 15 && f == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f, -9);
+  } else {
+    v = ldexp((double)(8 + f), e - 10); /* (1 + f/8) * 2^(e-7) */
+  }
+  return (float)(sign ? -v : v);
+}
+
+/* Reading of the page's "FP8 is cast directly instead of being rounded to an integer": the
+ * value goes to the nearest e4m3 number, ties to even (the default rounding of a float cast),
+ * and a magnitude of 448 or more saturates to 448 (the codes come from x / (absmax / 448), which
+ * can exceed 448 only by the rounding of that quotient).  NaN stays NaN. */
+uint8_t wql_oracle_float_to_e4m3(float x) {
+  const uint8_t sign = signbit(x) ? 0x80u : 0u;
+  if (isnan(x)) return (uint8_t)(sign | 0x7fu);
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7eu);
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal (or zero): units of 2^-9, ties to even; 8 units is the smallest normal, 0x08 */
+    const double units = nearbyint(ldexp(a, 9));
+    return (uint8_t)(sign | (uint8_t)units);
+  }
+  int e2;
+  frexp(a, &e2); /* a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;
+  double sig = nearbyint(ldexp(a, 3 - E)); /* in [8, 16], ties to even */
+  if (sig >= 16.0) {
+    sig = 8.0;
+    E += 1;
+  }
+  /* a < 448 keeps E <= 8 and sig <= 14 at E = 8, so the code is finite */
+  return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)(sig - 8.0));
+}
+
+void wql_oracle_e4m3_to_float_n(const uint8_t* b, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = wql_oracle_e4m3_to_float(b[i]);
+}
+void wql_oracle_float_to_e4m3_n(const float* x, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = wql_oracle_float_to_e4m3(x[i]);
+}
+
+/* [W8A8] QRMSNorm with per-token dynamic fp8 quantisation: the same normalised row y as the int8
+ * variant; xs_m = max_k |y_mk| / 448 (1.0 for an all-zero row); q_mk = e4m3(y_mk / xs_m). */
+void wql_oracle_qrmsnorm_quant_fp8(const uint16_t* X, const uint16_t* gamma, float eps, int M,
+                                   int K, uint8_t* q, float* xs) {
+#pragma omp parallel for schedule(static)
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* x = X + (size_t)m * K;
+    float r = rms_factor(x, K, eps);
+    float* y = (float*)malloc(sizeof(float) * (size_t)K);
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float t = wql_oracle_half_to_float(x[k]) * r;
+      y[k] = t * wql_oracle_half_to_float(gamma[k]);
+      float a = fabsf(y[k]);
+      if (a > amax) amax = a;
+    }
+    float scale = amax / 448.0f;
+    if (amax == 0.0f) scale = 1.0f;
+    xs[m] = scale;
+    for (int k = 0; k < K; ++k) q[(size_t)m * K + k] = wql_oracle_float_to_e4m3(y[k] / scale);
+    free(y);
+  }
+}
+
+/* The residual fusion of the fp8 variant: h = fp16(float(x) + float(r)) as for int8, then the
+ * fp8 QRMSNorm of h. */
+void wql_oracle_add_qrmsnorm_quant_fp8(const uint16_t* X, const uint16_t* R, const uint16_t* gamma,
+                                       float eps, int M, int K, uint16_t* H, uint8_t* q, float* xs) {
+  for (int64_t i = 0; i < (int64_t)M * K; ++i) {
+    float sum = wql_oracle_half_to_float(X[i]) + wql_oracle_half_to_float(R[i]);
+    H[i] = wql_oracle_float_to_half(sum);
+  }
+  wql_oracle_qrmsnorm_quant_fp8(H, gamma, eps, M, K, q, xs);
+}
+
+/* [W8A8] per_channel_quant into fp8: ws_n = max_k |W[k, n]| / 448 (1.0 for an all-zero column),
+ * qW[n, k] = e4m3(W[k, n] / ws_n), stored [N, K]. */
+void wql_oracle_per_channel_quant_fp8(const float* W, int K, int N, uint8_t* qW, float* ws) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float a = fabsf(W[(size_t)k * N + n]);
+      if (a > amax) amax = a;
+    }
+    float scale = amax / 448.0f;
+    if (amax == 0.0f) scale = 1.0f;
+    ws[n] = scale;
+    for (int k = 0; k < K; ++k) qW[(size_t)n * K + k] = wql_oracle_float_to_e4m3(W[(size_t)k * N + n] / scale);
+  }
+}
+
+/* [W8A8] fp8 GEMM: the page's kernel takes an fp32 accumulator when its inputs are floating point.
+ * The reference is the exact sum acc[i, n] = sum_k e4m3(q[rows[i], k]) * e4m3(qW[n, k]): every
+ * e4m3 value is an integer multiple of 2^-9 below 2^9 in magnitude, so each product is a multiple
+ * of 2^-18 below 2^18, and a sum of at most 2^16 of them is a multiple of 2^-18 below 2^34: 52
+ * significant bits, which fp64 holds exactly in any order.  absacc[i, n] = sum_k |product| bounds
+ * the error of any fp32 accumulation.  Returns 1 (and computes nothing) for K > 65536, or when a
+ * NaN code is present. */
+int wql_oracle_fp8_acc(const uint8_t* q, const uint8_t* qW, int K, int N, const int64_t* rows,
+                       int nrows, double* acc, double* absacc) {
+  if (K > 65536) return 1;
+  float* wdec = (float*)malloc(sizeof(float) * (size_t)N * K);
+  int bad = 0;
+  for (size_t i = 0; i < (size_t)N * K; ++i) {
+    wdec[i] = wql_oracle_e4m3_to_float(qW[i]);
+    if (isnan(wdec[i])) bad = 1;
+  }
+  for (int i = 0; i < nrows && !bad; ++i)
+    for (int k = 0; k < K; ++k)
+      if ((q[(size_t)rows[i] * K + k] & 0x7fu) == 0x7fu) bad = 1;
+  if (bad) {
+    free(wdec);
+    return 1;
+  }
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < nrows; ++i) {
+    const uint8_t* a = q + (size_t)rows[i] * K;
+    double* xa = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; ++k) xa[k] = (double)wql_oracle_e4m3_to_float(a[k]);
+    for (int n = 0; n < N; ++n) {
+      const float* b = wdec + (size_t)n * K;
+      double s = 0.0, t = 0.0;
+      for (int k = 0; k < K; ++k) {
+        const double p = xa[k] * (double)b[k];
+        s += p;
+        t += fabs(p);
+      }
+      acc[(size_t)i * N + n] = s;
+      absacc[(size_t)i * N + n] = t;
+    }
+    free(xa);
+  }
+  free(wdec);
+  return 0;
+}
+
+/* The fp8 GEMM's epilogue in fp64, without rounding: ((acc * xs_i) * ws_n + bias_n) + residual_in,
+ * the terms of the int8 epilogue (a NULL bias or residual is left out). */
+void wql_oracle_fp8_epilogue_f64(const double* acc, const float* xs, const float* ws,
+                                 const uint16_t* bias, const uint16_t* residual, int nrows, int N,
+                                 double* y) {
+  for (int i = 0; i < nrows; ++i)
+    for (int n = 0; n < N; ++n) {
+      double u = acc[(size_t)i * N + n] * (double)xs[i] * (double)ws[n];
+      if (bias) u += (double)wql_oracle_half_to_float(bias[n]);
+      if (residual) u += (double)wql_oracle_half_to_float(residual[(size_t)i * N + n]);
+      y[(size_t)i * N + n] = u;
+    }
 }
 
 /* Off-path: symmetric per-tensor int4 as printed in [AWQ] section 2 (scale = max|w| / 7.5,

@@ -398,3 +398,192 @@ def test_printed_symmetric_int4_example():
     assert abs(scale - gv["scale"]) <= gv["scale_abs_tol"]
     assert q.min() >= gv["code_min"] and q.max() <= gv["code_max"]
     assert q[0] == gv["code_max"] and q[3] == gv["code_min"]
+
+
+# ------------------------------------------------------------------------------------------------
+# fp8 (float8_e4m3fn) variant of the W8A8 path
+# ------------------------------------------------------------------------------------------------
+
+def _torch_e4m3_values():
+    """The 256 e4m3 codes decoded by torch's own float8_e4m3fn type (a library independent of the
+    oracle), as float64."""
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _nearest_e4m3_brute(x):
+    """Nearest finite e4m3 code of each float64 x by exhaustive search over the 254 finite codes
+    (decoded by torch): smallest |v - x|, ties to the even code (the one whose lowest fraction bit
+    is 0), magnitudes of 448 and more saturated.  Exact for 2^-12 <= |x| < 2^10, where every
+    difference fits in a double."""
+    vals = _torch_e4m3_values()
+    pos = np.arange(0, 0x7f)  # finite non-negative codes 0x00..0x7e
+    a = np.abs(x)
+    d = np.abs(vals[pos][None, :] - a[:, None])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    even = cand & (pos[None, :] % 2 == 0)
+    pick = np.where(even.any(axis=1), np.argmax(even, axis=1), np.argmax(cand, axis=1))
+    code = pos[pick].astype(np.uint8)
+    code[a >= 448.0] = 0x7e
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+def test_e4m3_decode_all_codes_match_torch_and_qmax_is_448():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_float(codes).astype(np.float64)
+    ref = _torch_e4m3_values()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2  # only S.1111.111
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))  # -0.0 is code 0x80
+    # Q_MAX as torch.finfo reports it, and the smallest subnormal / normal of the format
+    assert float(torch.finfo(torch.float8_e4m3fn).max) == 448.0 == np.nanmax(ours)
+    assert ours[1] == 2.0 ** -9 and ours[8] == 2.0 ** -6
+
+
+def test_float_to_e4m3_matches_brute_force_nearest_with_ties_and_saturation():
+    rng = np.random.default_rng(41)
+    vals = _torch_e4m3_values()
+    fin = np.sort(np.unique(vals[:0x7f]))
+    mids = (fin[:-1] + fin[1:]) / 2  # every exact tie between neighbouring non-negative values
+    rand = np.concatenate([rng.standard_normal(20000) * s for s in (3e-3, 0.1, 1.0, 30.0, 200.0)])
+    x = np.concatenate([rand, mids, -mids, fin, -fin, [448.0, 449.0, 463.9, 464.0, 480.0, 1000.0, -600.0]])
+    x = x.astype(np.float32)
+    keep = (np.abs(x.astype(np.float64)) >= 2.0 ** -12) & (np.abs(x) < 2.0 ** 10)
+    ours = oracle.float_to_e4m3(x[keep])
+    assert np.array_equal(ours, _nearest_e4m3_brute(x[keep].astype(np.float64)))
+    # tiny magnitudes go to a signed zero; large ones and infinities saturate; NaN stays NaN
+    tiny = np.array([0.0, -0.0, 2.0 ** -11, -(2.0 ** -11), 2.0 ** -30], np.float32)
+    assert list(oracle.float_to_e4m3(tiny)) == [0x00, 0x80, 0x00, 0x80, 0x00]
+    big = np.array([1e9, -1e9, np.inf, -np.inf], np.float32)
+    assert list(oracle.float_to_e4m3(big)) == [0x7e, 0xfe, 0x7e, 0xfe]
+    assert (oracle.float_to_e4m3(np.array([np.nan], np.float32))[0] & 0x7f) == 0x7f
+
+
+def test_float_to_e4m3_matches_torch_cast_in_range():
+    torch = pytest.importorskip("torch")
+    # every finite fp16 value below 448 in magnitude, as fp32
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float32)
+    h = h[np.isfinite(h) & (np.abs(h) < 448.0)]
+    ours = oracle.float_to_e4m3(h)
+    ref = torch.from_numpy(h).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def _e4m3_error_ok(codes, target, scale):
+    """|decode(code) * scale - target| within half a unit of e4m3 at the code's magnitude: 2^-4 of
+    the value for normals, 2^-10 * scale below the smallest normal (units of 2^-9 * scale)."""
+    v = oracle.e4m3_to_float(codes).astype(np.float64) * np.asarray(scale, np.float64)
+    err = np.abs(v - target.astype(np.float64))
+    bound = np.maximum(np.abs(target) * 2.0 ** -4, 2.0 ** -10 * np.asarray(scale, np.float64)) * (1 + 1e-6)
+    return bool(np.all(err <= bound))
+
+
+def test_qrmsnorm_fp8_against_definition_and_brute_force():
+    M, K = 9, 640
+    X = inputs.activations(M, K, seed=42, outlier_channels=True)
+    X[3] = 0  # an all-zero row
+    g = inputs.gamma(K, seed=42)
+    q, xs = oracle.qrmsnorm_quant_fp8(X, g, inputs.EPS)
+    y = oracle.rmsnorm(X, g, inputs.EPS)
+    amax = np.abs(y).max(axis=1)
+    want_xs = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(xs.view(np.uint32), want_xs.view(np.uint32))
+    t = (y / xs[:, None]).astype(np.float32).astype(np.float64)
+    nz = np.abs(t) >= 2.0 ** -12
+    assert np.array_equal(q[nz], _nearest_e4m3_brute(t[nz]))
+    assert np.all((q[~nz] & 0x7f) == 0)
+    dec = oracle.e4m3_to_float(q)
+    for m in range(M):
+        if m == 3:
+            assert xs[m] == 1.0 and np.all((q[m] & 0x7f) == 0)
+        else:
+            assert np.abs(dec[m]).max() == 448.0  # the row's absmax lands exactly on Q_MAX
+    assert _e4m3_error_ok(q, y, xs[:, None])
+
+
+def test_add_qrmsnorm_fp8_residual_sum():
+    M, K = 5, 256
+    X = inputs.activations(M, K, seed=43)
+    R = inputs.activations(M, K, seed=44, outlier_channels=True)
+    g = inputs.gamma(K, seed=43)
+    h, q, xs = oracle.add_qrmsnorm_quant_fp8(X, R, g, inputs.EPS)
+    # fp16(x + r): the exact sum of two fp16 values rounded once (numpy's binary16 rounding)
+    want_h = (X.astype(np.float64) + R.astype(np.float64)).astype(np.float32).astype(np.float16)
+    assert np.array_equal(h.view(np.uint16), want_h.view(np.uint16))
+    q2, xs2 = oracle.qrmsnorm_quant_fp8(want_h, g, inputs.EPS)
+    assert np.array_equal(q, q2) and np.array_equal(xs, xs2)
+    # r = -x: every row cancels to zero
+    h0, q0, xs0 = oracle.add_qrmsnorm_quant_fp8(X, -X, g, inputs.EPS)
+    assert np.all(h0 == 0) and np.all((q0 & 0x7f) == 0) and np.all(xs0 == 1.0)
+
+
+def test_per_channel_quant_fp8_bounds_and_layout():
+    K, N = 192, 48
+    rng = np.random.default_rng(45)
+    W = (rng.standard_normal((K, N)) * rng.uniform(0.01, 3.0, N)).astype(np.float32)
+    W[:, 7] = 0
+    W[5, 9] = 1e-7  # tiny values land among the subnormals
+    qW, ws = oracle.per_channel_quant_fp8(W)
+    assert qW.shape == (N, K) and ws.shape == (N,)
+    amax = np.abs(W).max(axis=0)
+    want = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(ws.view(np.uint32), want.view(np.uint32))
+    dec = oracle.e4m3_to_float(qW)
+    assert np.all(np.abs(dec[np.arange(N) != 7]).max(axis=1) == 448.0)
+    assert np.all((qW[7] & 0x7f) == 0) and ws[7] == 1.0
+    assert _e4m3_error_ok(qW, W.T, ws[:, None])
+    t = (W.T / ws[:, None]).astype(np.float32).astype(np.float64)
+    nz = np.abs(t) >= 2.0 ** -12
+    assert np.array_equal(qW[nz], _nearest_e4m3_brute(t[nz]))
+
+
+def test_fp8_acc_exact_against_rationals_and_numpy():
+    rng = np.random.default_rng(46)
+    finite = np.array([c for c in range(256) if (c & 0x7f) != 0x7f], np.uint8)
+    vals = _torch_e4m3_values()
+    # tiny: exact rational sums
+    q = rng.choice(finite, size=(3, 24)).astype(np.uint8)
+    qW = rng.choice(finite, size=(5, 24)).astype(np.uint8)
+    acc, absacc = oracle.fp8_acc(q, qW)
+    for i in range(3):
+        for n in range(5):
+            s = sum(Fraction(float(vals[a])) * Fraction(float(vals[b])) for a, b in zip(q[i], qW[n]))
+            assert Fraction(acc[i, n]) == s
+            assert absacc[i, n] == float(sum(abs(Fraction(float(vals[a])) * Fraction(float(vals[b])))
+                                             for a, b in zip(q[i], qW[n])))
+    # larger, with extremes (+-448 everywhere): numpy's float64 matmul is exact here too
+    K = 4096
+    q = rng.choice(finite, size=(4, K)).astype(np.uint8)
+    qW = rng.choice(finite, size=(6, K)).astype(np.uint8)
+    q[0] = 0x7e
+    qW[0] = 0x7e
+    qW[1] = 0xfe
+    rows = np.array([3, 0, 2], np.int64)
+    acc, absacc = oracle.fp8_acc(q, qW, rows=rows)
+    ref = vals[q[rows]] @ vals[qW].T
+    assert np.array_equal(acc, ref)
+    assert acc[1, 0] == 448.0 * 448.0 * K and acc[1, 1] == -448.0 * 448.0 * K
+    assert np.all(absacc >= np.abs(acc))
+    with pytest.raises(ValueError):
+        bad = q.copy()
+        bad[0, 0] = 0x7f
+        oracle.fp8_acc(bad, qW)
+
+
+def test_fp8_epilogue_terms():
+    rng = np.random.default_rng(47)
+    acc = rng.standard_normal((3, 8)) * 1e4
+    xs = rng.uniform(1e-3, 1e-2, 3).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-3, 8).astype(np.float32)
+    bias = rng.standard_normal(8).astype(np.float16)
+    res = rng.standard_normal((3, 8)).astype(np.float16)
+    base = oracle.fp8_epilogue_f64(acc, xs, ws)
+    assert np.allclose(base, acc * xs[:, None].astype(np.float64) * ws[None, :].astype(np.float64), rtol=1e-15)
+    both = oracle.fp8_epilogue_f64(acc, xs, ws, bias, res)
+    assert np.allclose(both - base, bias.astype(np.float64)[None, :] + res.astype(np.float64), rtol=0, atol=1e-9)
+    only_b = oracle.fp8_epilogue_f64(acc, xs, ws, bias=bias)
+    assert np.allclose(only_b - base, np.broadcast_to(bias.astype(np.float64), (3, 8)), rtol=0, atol=1e-9)
