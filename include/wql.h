@@ -205,6 +205,52 @@ wql_status wql_smooth(const float* absmax, const uint16_t* gamma, const float* w
 wql_status wql_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws,
                                     void* stream);
 
+/* ========================================================================================
+ * FP8 variant of W8A8 ([W8A8]: quant_dtype "fp8", the short name of float8_e4m3fn).
+ * Codes are float8 e4m3 bytes (1 sign, 4 exponent bits with bias 7, 3 fraction bits, no
+ * infinity, largest value 448), passed as uint8_t.  Q_MAX = 448 (torch.finfo of the type)
+ * replaces 127, and the page casts instead of rounding to an integer.  Reading of the cast:
+ * nearest e4m3 value, ties to even, magnitudes beyond 448 saturated to 448.
+ * ======================================================================================== */
+
+/* ----------------------------------------------------------------------------------------
+ * qrmsnorm_quant_fp8: wql_qrmsnorm_quant_i8 with fp8 codes.  y is the same fp32 RMSNorm;
+ *     xs[m]   = max_k |y[m, k]| / 448   (1.0 for an all-zero row)
+ *     q[m, k] = e4m3(y[m, k] / xs[m])   (the quotient correctly rounded in fp32 first)
+ * add_qrmsnorm_quant_fp8: the residual fusion, exactly as wql_add_qrmsnorm_quant_i8 (h =
+ * fp16(x + residual) goes to residual_out, which may be residual itself) with fp8 codes.
+ * Requires K % 8 == 0, 8 <= K <= 16384; every pointer 16-byte aligned (xs: 4-byte).
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                                  uint8_t* q, float* xs, void* stream);
+wql_status wql_add_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* residual,
+                                      const uint16_t* gamma, float eps, int M, int K,
+                                      uint16_t* residual_out, uint8_t* q, float* xs, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * per_channel_quant_fp8: ws_n = max_k |w[k, n]| / 448 (1.0 for a zero column);
+ *     qw[n, k] = e4m3(w[k, n] / ws_n)
+ *   w [K, N] fp32 -> qw [N, K] e4m3 (transposed), ws [N] fp32.  Requires K % 16 == 0, N % 32 == 0.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, float* ws,
+                                     void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * w8a8_gemm_fp8  [W8A8] matmul_kernel_dynamic_quant with fp8 inputs (fp32 accumulator) and
+ * the optional terms of its _linear_add variant:
+ *     acc[m, n] = sum_k e4m3(q[m, k]) * e4m3(qw[n, k])       (fp32 accumulation)
+ *     y[m, n]   = fp16(((acc[m, n] * xs[m]) * ws[n] + float(bias[n])) + float(residual[m, n]))
+ * q [M, K], qw [N, K] e4m3; xs [M], ws [N] fp32; bias [N] and residual [M, N] fp16, each
+ * optional (NULL leaves the term out; residual may be y itself).  y [M, N] fp16 is written in
+ * full, and acc_out [M, N] fp32 too when non-NULL.  The order of the fp32 additions is the
+ * kernel's own (tensor-core sums, then a fixed-order split-K reduction), so acc differs from
+ * the exact sum by at most K * 2^-23 * sum_k |product| -- an fp32 rounding per addition.
+ * No workspace.  Requires K % 16 == 0, N % 32 == 0, M >= 0.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_w8a8_gemm_fp8(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws,
+                             const uint16_t* bias, const uint16_t* residual, int M, int K, int N,
+                             uint16_t* y, float* acc_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,6 +41,10 @@ SIGNATURES = {
     "wql_act_absmax": (_I, [_P, _P, _F, _I, _I, _P, _P]),
     "wql_smooth": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P]),
     "wql_per_channel_quant_i8": (_I, [_P, _I, _I, _P, _P, _P]),
+    "wql_qrmsnorm_quant_fp8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
+    "wql_add_qrmsnorm_quant_fp8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
+    "wql_per_channel_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
+    "wql_w8a8_gemm_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -307,3 +311,90 @@ def device_status(device: torch.device | None = None) -> None:
     """Synchronise the current stream and raise if a kernel abandoned a bounded wait."""
     dev = device or torch.device("cuda", torch.cuda.current_device())
     _check(load().wql_device_status(_stream(dev)), "wql_device_status")
+
+
+# ---- fp8 (float8_e4m3fn) variant of W8A8 ------------------------------------------------------
+
+E4M3 = torch.float8_e4m3fn
+
+
+def qrmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, q: torch.Tensor | None = None,
+                       xs: torch.Tensor | None = None):
+    """QRMSNorm + per-token fp8: x [M, K] fp16 -> (q float8_e4m3fn [M, K], xs fp32 [M]), xs = absmax / 448."""
+    M, K = x.shape
+    _need(x, "x", torch.float16, (M, K))
+    _need(gamma, "gamma", torch.float16, (K,))
+    if q is None:
+        q = torch.empty((M, K), dtype=E4M3, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(q, "q", E4M3, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _check(load().wql_qrmsnorm_quant_fp8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q), _ptr(xs), _stream(x.device)),
+           "wql_qrmsnorm_quant_fp8")
+    return q, xs
+
+
+def add_qrmsnorm_quant_fp8(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+                           residual_out: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                           xs: torch.Tensor | None = None):
+    """Residual-fused fp8 QRMSNorm: h = fp16(x + residual) -> (h, q float8_e4m3fn [M, K], xs fp32 [M]).
+
+    residual_out receives h (it may be `residual` itself, for an in-place update)."""
+    M, K = x.shape
+    _need(x, "x", torch.float16, (M, K))
+    _need(residual, "residual", torch.float16, (M, K))
+    _need(gamma, "gamma", torch.float16, (K,))
+    if residual_out is None:
+        residual_out = torch.empty((M, K), dtype=torch.float16, device=x.device)
+    if q is None:
+        q = torch.empty((M, K), dtype=E4M3, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(residual_out, "residual_out", torch.float16, (M, K))
+    _need(q, "q", E4M3, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _check(load().wql_add_qrmsnorm_quant_fp8(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), M, K,
+                                             _ptr(residual_out), _ptr(q), _ptr(xs), _stream(x.device)),
+           "wql_add_qrmsnorm_quant_fp8")
+    return residual_out, q, xs
+
+
+def per_channel_quant_fp8(w: torch.Tensor, qw: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+    """w [K, N] fp32 -> (qw float8_e4m3fn [N, K], ws fp32 [N]) with ws = absmax / 448."""
+    K, N = w.shape
+    _need(w, "w", torch.float32, (K, N))
+    if qw is None:
+        qw = torch.empty((N, K), dtype=E4M3, device=w.device)
+    if ws is None:
+        ws = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _need(qw, "qw", E4M3, (N, K))
+    _need(ws, "ws", torch.float32, (N,))
+    _check(load().wql_per_channel_quant_fp8(_ptr(w), K, N, _ptr(qw), _ptr(ws), _stream(w.device)),
+           "wql_per_channel_quant_fp8")
+    return qw, ws
+
+
+def w8a8_gemm_fp8(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch.Tensor,
+                  bias: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp16 = fp16(((acc * xs) * ws + bias) + residual), acc the fp32 sum of e4m3 products of
+    q [M, K] and qw [N, K]; bias [N] and residual [M, N] fp16 optional; optional fp32 acc_out [M, N]."""
+    M, K = q.shape
+    N = qw.shape[0]
+    _need(q, "q", E4M3, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _need(qw, "qw", E4M3, (N, K))
+    _need(ws, "ws", torch.float32, (N,))
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,))
+    if residual is not None:
+        _need(residual, "residual", torch.float16, (M, N))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=q.device)
+    _need(out, "out", torch.float16, (M, N))
+    if acc_out is not None:
+        _need(acc_out, "acc_out", torch.float32, (M, N))
+    _check(load().wql_w8a8_gemm_fp8(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), _ptr(bias), _ptr(residual), M, K, N,
+                                    _ptr(out), _ptr(acc_out), _stream(q.device)), "wql_w8a8_gemm_fp8")
+    return out

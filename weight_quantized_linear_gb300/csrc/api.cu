@@ -182,6 +182,52 @@ wql_status wql_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual
                      "wql_add_qrmsnorm_quant_i8");
 }
 
+namespace {
+
+// Shared argument checks of the QRMSNorm entry points (residual and residual_out only when fused).
+wql_status norm_args(const uint16_t* x, const uint16_t* gamma, int M, int K, const void* q, const float* xs,
+                     bool fused, const uint16_t* residual, const uint16_t* residual_out) {
+  WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (K > 16384) return fail(WQL_EUNSUPPORTED, "K > 16384 is not supported by the register-resident row kernel");
+  if (M == 0) return WQL_OK;
+  WQL_REQUIRE_PTR(x);
+  WQL_REQUIRE_PTR(gamma);
+  WQL_REQUIRE_PTR(q);
+  if (fused) {
+    WQL_REQUIRE_PTR(residual);
+    WQL_REQUIRE_PTR(residual_out);
+  }
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  return WQL_OK;
+}
+
+}  // namespace
+
+wql_status wql_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, uint8_t* q,
+                                  float* xs, void* stream) {
+  const wql_status st = norm_args(x, gamma, M, K, q, xs, false, nullptr, nullptr);
+  if (st != WQL_OK || M == 0) {
+    if (st == WQL_OK) g_last_error.clear();
+    return st;
+  }
+  return cuda_status(wql::launch_qrmsnorm_quant_fp8(x, nullptr, gamma, eps, M, K, nullptr, q, xs, device_error_word(),
+                                                    static_cast<cudaStream_t>(stream)),
+                     "wql_qrmsnorm_quant_fp8");
+}
+
+wql_status wql_add_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps,
+                                      int M, int K, uint16_t* residual_out, uint8_t* q, float* xs, void* stream) {
+  const wql_status st = norm_args(x, gamma, M, K, q, xs, true, residual, residual_out);
+  if (st != WQL_OK || M == 0) {
+    if (st == WQL_OK) g_last_error.clear();
+    return st;
+  }
+  return cuda_status(wql::launch_qrmsnorm_quant_fp8(x, residual, gamma, eps, M, K, residual_out, q, xs,
+                                                    device_error_word(), static_cast<cudaStream_t>(stream)),
+                     "wql_add_qrmsnorm_quant_fp8");
+}
+
 size_t wql_w8a8_workspace_bytes(int M, int K, int N) {
   (void)N;
   if (M < wql::kW8A8PrefillMinM || K <= 0) return 0;  // the streaming decode kernel needs no scratch
@@ -240,6 +286,36 @@ wql_status wql_w8a8_gemm_fused(const int8_t* q, const float* xs, const int8_t* q
                    workspace_bytes, stream);
 }
 
+wql_status wql_w8a8_gemm_fp8(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws,
+                             const uint16_t* bias, const uint16_t* residual, int M, int K, int N, uint16_t* y,
+                             float* acc_out, void* stream) {
+  WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE_PTR(qw);
+  WQL_REQUIRE_PTR(ws);
+  WQL_REQUIRE_PTR(y);
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  WQL_REQUIRE(acc_out == nullptr || aligned16(acc_out), "acc_out must be NULL or 16-byte aligned");
+  WQL_REQUIRE(bias == nullptr || aligned16(bias), "bias must be NULL or 16-byte aligned");
+  WQL_REQUIRE(residual == nullptr || aligned16(residual), "residual must be NULL or 16-byte aligned");
+  unsigned* dev_err = device_error_word();
+  std::string err;
+  const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode"
+  const bool prefill = force && strcmp(force, "decode") == 0 ? false : M >= wql::kFp8PrefillMinM;
+  cudaError_t e = prefill ? wql::launch_fp8_prefill(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, dev_err,
+                                                    static_cast<cudaStream_t>(stream), &err)
+                          : wql::launch_fp8_decode(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, dev_err,
+                                                   static_cast<cudaStream_t>(stream), &err);
+  if (!err.empty()) return fail(WQL_ECUDA, "wql_w8a8_gemm_fp8: " + err);
+  return cuda_status(e, "wql_w8a8_gemm_fp8");
+}
+
 wql_status wql_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,
                           void* stream) {
   WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
@@ -277,6 +353,16 @@ wql_status wql_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, fl
   WQL_REQUIRE_PTR(ws);
   return cuda_status(wql::launch_per_channel_quant_i8(w, K, N, qw, ws, static_cast<cudaStream_t>(stream)),
                      "wql_per_channel_quant_i8");
+}
+
+wql_status wql_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, float* ws, void* stream) {
+  WQL_REQUIRE(K >= 16 && K % 16 == 0, "K must be a positive multiple of 16");
+  WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE_PTR(w);
+  WQL_REQUIRE_PTR(qw);
+  WQL_REQUIRE_PTR(ws);
+  return cuda_status(wql::launch_per_channel_quant_fp8(w, K, N, qw, ws, static_cast<cudaStream_t>(stream)),
+                     "wql_per_channel_quant_fp8");
 }
 
 }  // extern "C"

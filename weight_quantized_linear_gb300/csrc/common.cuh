@@ -278,6 +278,52 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return d;
 }
 
+// ---------------------------------------------------------------------------------------------
+// float8 e4m3 ("fn": finite only, largest value 448)
+// ---------------------------------------------------------------------------------------------
+
+// Four fp32 -> four e4m3 bytes (a0 in byte 0), nearest value with ties to even, magnitudes beyond
+// 448 saturated to 448.
+__device__ __forceinline__ uint32_t e4m3x4_rn_sat(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};\n}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
+}
+
+// e4m3 codes of fl(y_i / s) for four values, without a division in the common case.
+// t = fl(y * inv) with inv = fl(1 / s) lies within 3 fp32 ulps of fl(y / s) (two roundings of
+// relative size 2^-24 and fl(y / s)'s own half ulp).  Rounding to e4m3 is monotonic, so when the
+// values 8 ulps below and above t (one step of the bit pattern is one ulp) give the same codes,
+// every value between them does, fl(y / s) included.  Otherwise -- near an e4m3 rounding tie, or
+// at zero, where a step below wraps to NaN -- the codes come from the correctly rounded quotient.
+__device__ __forceinline__ uint32_t e4m3x4_div(const float (&y)[4], float s, float inv) {
+  float lo[4], hi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b = __float_as_int(__fmul_rn(y[i], inv));
+    lo[i] = __int_as_float(b - 8);
+    hi[i] = __int_as_float(b + 8);
+  }
+  const uint32_t a = e4m3x4_rn_sat(lo[0], lo[1], lo[2], lo[3]);
+  if (a == e4m3x4_rn_sat(hi[0], hi[1], hi[2], hi[3])) return a;
+  return e4m3x4_rn_sat(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s), __fdiv_rn(y[2], s), __fdiv_rn(y[3], s));
+}
+
+// Four e4m3 bytes -> two f16x2 (bytes 0,1 and bytes 2,3), exact: every e4m3 value is an fp16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n"
+      " mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
 __device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -1,0 +1,262 @@
+// fp8_prefill.cu -- the fp8 (e4m3) variant of the SmoothQuant W8A8 GEMM for prefill-shaped calls,
+// on the tcgen05 tensor cores ("LMDeploy W8A8 quantisation guide": quant_dtype fp8 is
+// float8_e4m3fn; matmul_kernel_dynamic_quant takes an fp32 accumulator for floating-point inputs,
+// then c = c * rms_scale * linear_scale, rounded to fp16; its _linear_add variant adds a bias and a
+// residual).
+//
+// Both operands are e4m3 codes, which kind::f8f6f4 reads straight from shared memory, so nothing is
+// converted: TMA brings 128-byte-swizzled tiles of the weights qw [N, K] (128 output channels, the
+// MMA's M: "swap AB") and of the activation codes q [M, K] (BN tokens, the MMA's N), 128 k per stage,
+// and one thread issues four K = 32 MMAs per stage.  Warp roles: warp 0 the TMA producer, warp 1 the
+// MMA issuer (and TMEM owner), warps 2-5 the epilogue.  Two TMEM accumulators of BN columns alternate
+// between tiles, so a tile's epilogue overlaps the next tile's MMAs.  Persistent CTAs walk the tiles,
+// channel tiles fastest (CTAs running at the same time share the token tile).
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace wql {
+namespace {
+
+constexpr int kBK = 128;  // k per stage (bytes of an e4m3 row): four K = 32 MMAs
+constexpr int kBM = 128;  // output channels per tile (MMA M)
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+
+template <int BN>
+struct FLayout {
+  static constexpr int kWBytes = kBM * kBK;  // 128 channel rows x 128 B, 128-byte swizzle
+  static constexpr int kXBytes = BN * kBK;   // BN token rows x 128 B
+  static constexpr int kStage = kWBytes + kXBytes;
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
+  static constexpr int kBarBytes = (2 * kStages + 5) * 8 + 16;
+  static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
+  static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle atoms");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // q e4m3 [M][K], box {128, BN}, SW128
+                       const __grid_constant__ CUtensorMap tm_w,  // qw e4m3 [N][K], box {128, 128}, SW128
+                       const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
+                       __half* __restrict__ y, float* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+  using L = FLayout<BN>;
+  constexpr int kStages = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
+  uint64_t* empty = full + kStages;     // the stage's MMAs have completed
+  uint64_t* accfull = empty + kStages;  // [2] accumulator holds a finished tile
+  uint64_t* accempty = accfull + 2;     // [2] epilogue has read the accumulator
+  uint64_t* finalbar = accempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntn = (N + kBM - 1) / kBM;
+  const int ntiles = ntn * ((M + BN - 1) / BN);
+  const int nkb = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kEpiWarps);
+    }
+    mbar_init(finalbar, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      grid_dependency_wait();
+      int stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int nt = tile % ntn, mt = tile / ntn;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+            report_error(err, kErrTimeoutEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * L::kStage;
+          mbar_arrive_expect_tx(&full[stage], L::kStage);
+          tma_load_2d(st, &tm_w, &full[stage], kb * kBK, nt * kBM);
+          tma_load_2d(st + L::kWBytes, &tm_x, &full[stage], kb * kBK, mt * BN);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // leave no copy in flight: wait (bounded) for the last stages issued
+      for (int i = 0; i < kStages && i < issued; ++i) {
+        stage = stage == 0 ? kStages - 1 : stage - 1;
+        if (stage == kStages - 1) phase ^= 1;
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          report_error(err, kErrTimeoutDrain);
+          break;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_e4m3(kBM, BN);
+      int stage = 0, phase = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tcount) {
+        const int b = tcount & 1;
+        if (!mbar_wait_bounded(&accempty[b], ((tcount >> 1) & 1) ^ 1)) {
+          report_error(err, kErrTimeoutMma);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase)) {
+            report_error(err, kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          // the stage's descriptors differ only in the start address field (bits 0-13, addr >> 4;
+          // shared-memory addresses stay below 2^18, so adding to it never carries): 32 bytes per
+          // K = 32 step along the 128-byte rows
+          const uint32_t st = smem_u32(smem + stage * L::kStage);
+          const uint64_t adesc0 = umma_sdesc_sw128(st, 16, 1024);
+          const uint64_t bdesc0 = umma_sdesc_sw128(st + L::kWBytes, 16, 1024);
+#pragma unroll
+          for (int s = 0; s < kBK / 32; ++s)
+            umma_f8f6f4(d_tmem, adesc0 + 2 * s, bdesc0 + 2 * s, idesc, (kb > 0 || s > 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&accfull[b]);
+      }
+      umma_commit(finalbar);
+      if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
+    }
+  } else {
+    // ---------------- epilogue: TMEM lane = output channel, column = token ----------------
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
+      const int nt = tile % ntn, mt = tile / ntn;
+      const int b = tcount & 1;
+      const int n = nt * kBM + quad * 32 + lane;
+      const float wn = n < N ? ws[n] : 0.f;
+      if (!mbar_wait_warp(&accfull[b], (tcount >> 1) & 1)) {
+        report_error(err, kErrTimeoutMma);
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_base + b * BN + cc, r);
+        tmem_ld_wait();
+        const int mbase = mt * BN + cc;
+        if (n < N) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int m = mbase + k;
+            if (m < M) {
+              const float c = __uint_as_float(r[k]);
+              y[(size_t)m * N + n] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(c, xs[m]), wn), ea, m, n, N));
+              if (acc_out) acc_out[(size_t)m * N + n] = c;
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+template <int BN>
+cudaError_t launch_f(const void* q, const void* qw, const float* xs, const float* ws, int M, int N, int K, __half* y,
+                     float* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  using L = FLayout<BN>;
+  auto kern = fp8_prefill_kernel<BN>;
+  CUtensorMap tx, tw;
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, K, M, (uint64_t)K, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B,
+                    err) ||
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                    err)) {
+    return cudaErrorInvalidValue;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, y, acc_out, ea, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Token tile for an fp8 GEMM of M tokens: 64 up to 64 tokens; otherwise 128 or 256, whichever needs
+// fewer tile-columns of work on the busiest SM (waves of tiles times tokens per tile).
+int fp8_prefill_tile_n(int M, int N) {
+  if (M <= 64) return 64;
+  const long long ntn = (N + kBM - 1) / kBM, sms = num_sms();
+  const long long w128 = (ntn * ((M + 127) / 128) + sms - 1) / sms, w256 = (ntn * ((M + 255) / 256) + sms - 1) / sms;
+  return w256 * 256 <= w128 * 128 ? 256 : 128;
+}
+
+cudaError_t launch_fp8_prefill(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,
+                               int N, uint16_t* y, float* acc_out, const uint16_t* bias, const uint16_t* residual,
+                               unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
+  __half* yh = reinterpret_cast<__half*>(y);
+  switch (fp8_prefill_tile_n(M, N)) {
+    case 64:
+      return launch_f<64>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
+    case 128:
+      return launch_f<128>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
+    default:
+      return launch_f<256>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
+  }
+}
+
+}  // namespace wql

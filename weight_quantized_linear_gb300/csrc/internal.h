@@ -93,4 +93,21 @@ cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* q
                                int M, int K, int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias,
                                const uint16_t* residual, unsigned* dev_err, cudaStream_t s, std::string* err);
 
+// fp8 (e4m3) variant.  residual (and residual_out) may be null: then the plain QRMSNorm.
+cudaError_t launch_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps,
+                                      int M, int K, uint16_t* residual_out, uint8_t* q, float* xs, unsigned* dev_err,
+                                      cudaStream_t s);
+
+cudaError_t launch_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, float* ws, cudaStream_t s);
+
+// Token count from which the fp8 GEMM uses the tcgen05 kernel; below it, the streaming decode kernel.
+constexpr int kFp8PrefillMinM = 17;
+int fp8_prefill_tile_n(int M, int N);
+cudaError_t launch_fp8_prefill(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,
+                               int N, uint16_t* y, float* acc_out, const uint16_t* bias, const uint16_t* residual,
+                               unsigned* dev_err, cudaStream_t stream, std::string* err);
+cudaError_t launch_fp8_decode(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,
+                              int N, uint16_t* y, float* acc_out, const uint16_t* bias, const uint16_t* residual,
+                              unsigned* dev_err, cudaStream_t stream, std::string* err);
+
 }  // namespace wql

@@ -1,7 +1,8 @@
-// norm.cu -- QRMSNorm fused with per-token dynamic int8 quantisation, and the calibration
+// norm.cu -- QRMSNorm fused with per-token dynamic int8 or fp8 quantisation, and the calibration
 // statistic used by weight smoothing ("LMDeploy W8A8 quantisation guide": QRMSNorm.forward,
-// rms_norm_dynamic_quant, per_token_quant_int8 with scale = absmax / 127 and codes rounded to
-// integers; smoothing statistics are the per-channel absmax of the norm output).
+// rms_norm_dynamic_quant, per_token_quant_int8 with scale = absmax / Q_MAX; int8 codes are rounded
+// to integers (Q_MAX = 127), fp8 codes are the e4m3 cast (Q_MAX = 448); smoothing statistics are
+// the per-channel absmax of the norm output).
 //
 // CTAs of 256 threads walk the token rows; each row is brought into shared memory by a bulk copy
 // (several rows in flight per CTA) and held in registers while it is normalised.  The sum of
@@ -38,9 +39,14 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                : "memory");
 }
 
-// Rows in flight per CTA: four, or three when each slot holds two long rows (MODE 2, K > 8192).
-__host__ __device__ constexpr int norm_slots(int cpt, int mode) { return (mode == 2 && cpt > 4) ? 3 : 4; }
-__host__ __device__ constexpr int norm_rows_per_slot(int mode) { return mode == 2 ? 2 : 1; }
+// Modes of the row kernel: 0 int8 codes, 1 per-channel absmax (atomic max into absmax), 2 residual
+// add then int8 codes, 3 fp8 codes, 4 residual add then fp8 codes.
+__host__ __device__ constexpr bool mode_residual(int mode) { return mode == 2 || mode == 4; }
+__host__ __device__ constexpr bool mode_fp8(int mode) { return mode == 3 || mode == 4; }
+
+// Rows in flight per CTA: four, or three when each slot holds two long rows (residual, K > 8192).
+__host__ __device__ constexpr int norm_slots(int cpt, int mode) { return (mode_residual(mode) && cpt > 4) ? 3 : 4; }
+__host__ __device__ constexpr int norm_rows_per_slot(int mode) { return mode_residual(mode) ? 2 : 1; }
 
 // Round to the nearest integer (ties to even) and saturate to [-128, 127], in one conversion.
 __device__ __forceinline__ int cvt_rni_sat_s8(float f) {
@@ -93,21 +99,22 @@ __device__ __forceinline__ bool row_sum_vote(float p, bool ok, float* red, float
   return true;
 }
 
-// MODE 0: quantise (q, xs); MODE 1: per-channel absmax of the norm output (atomic max into absmax);
-// MODE 2: add the residual first ("LMDeploy W8A8 quantisation guide", inference kernels: the
+// Quantising modes write (q, xs); MODE 1 writes the per-channel absmax of the norm output.  The
+// residual modes add the residual first ("LMDeploy W8A8 quantisation guide", inference kernels: the
 // residual fusion of rms_norm_dynamic_quant): h = fp16(fp32(x) + fp32(r)) is stored to h_out (the
-// new residual; it may be the residual buffer itself) and normalised and quantised as in MODE 0.
+// new residual; it may be the residual buffer itself) and normalised and quantised like x.
 // Persistent CTAs: CTA b normalises rows b, b + gridDim.x, ...  Thread 0 keeps kNormSlots rows in
 // flight with bulk copies into a shared-memory ring, so HBM reads continue through every row's
 // reductions; a slot is refilled as soon as all threads have read it (the first barrier of the
 // row's sum).
 template <int CPT, int MODE>
 // (the residual mode holds the new residual across the row sum: three CTAs per SM, no spill)
-__global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) : 1)
+__global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) ? 3 : 4) : 1)
     qrmsnorm_kernel(const __half* __restrict__ x, const __half* residual, const __half* __restrict__ gamma, float eps,
-                    int M, int K, int8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax,
+                    int M, int K, uint8_t* __restrict__ q, float* __restrict__ xs, float* __restrict__ absmax,
                     __half* h_out, unsigned* err) {
   constexpr int kNormSlots = norm_slots(CPT, MODE), kRowsPerSlot = norm_rows_per_slot(MODE);
+  constexpr bool kResid = mode_residual(MODE);
   __shared__ float red[272];  // [0, 256) lane partials, 256 row sum, [264, 272) warp maxima
   __shared__ __align__(8) uint64_t full[kNormSlots];
   extern __shared__ __align__(16) uint8_t rows[];  // kNormSlots x kRowsPerSlot x 2K bytes
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) :
     const size_t off = (size_t)(blockIdx.x + (size_t)j * gridDim.x) * K;
     mbar_arrive_expect_tx(&full[s], slot_bytes);
     bulk_load(rows + (size_t)s * slot_bytes, x + off, row_bytes, &full[s]);
-    if constexpr (MODE == 2) bulk_load(rows + (size_t)s * slot_bytes + row_bytes, residual + off, row_bytes, &full[s]);
+    if constexpr (kResid) bulk_load(rows + (size_t)s * slot_bytes + row_bytes, residual + off, row_bytes, &full[s]);
   };
   if (tid == 0) {
     for (int s = 0; s < kNormSlots; ++s) mbar_init(&full[s], 1);
@@ -156,15 +163,15 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) :
     // ever expires (the values read from an unfinished slot are then discarded).
     const bool ok = mbar_wait_bounded(&full[s], (j / kNormSlots) & 1);
     const uint4* xr = reinterpret_cast<const uint4*>(rows + (size_t)s * slot_bytes);
-    float yv[CPT][8];  // x (MODE 2: x + r as fp16), then the normalised row
-    uint4 hv[MODE == 2 ? CPT : 1];  // MODE 2: the new residual, stored once the row's wait is confirmed
+    float yv[CPT][8];  // x (or x + r as fp16), then the normalised row
+    uint4 hv[kResid ? CPT : 1];  // the new residual, stored once the row's wait is confirmed
     float p = 0.f;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
       if (c < nchunks) {
         uint4 xv = xr[c];
-        if constexpr (MODE == 2) {
+        if constexpr (kResid) {
           const uint4 rv = reinterpret_cast<const uint4*>(rows + (size_t)s * slot_bytes + row_bytes)[c];
           const __half* xh = reinterpret_cast<const __half*>(&xv);
           const __half* rh = reinterpret_cast<const __half*>(&rv);
@@ -190,7 +197,7 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) :
     }
     // every thread has read slot s (it passed the sum's barrier): refill it
     if (tid == 0 && j + kNormSlots < nrows) issue(j + kNormSlots);
-    if constexpr (MODE == 2) {
+    if constexpr (kResid) {
 #pragma unroll
       for (int i = 0; i < CPT; ++i) {
         const int c = tid + kNormThreads * i;
@@ -229,14 +236,18 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (MODE == 2 ? 3 : 4) :
     }
 
     const float rowmax = block_max(amax, red);
-    const float scale = rowmax == 0.f ? 1.0f : __fdiv_rn(rowmax, 127.0f);
+    const float scale = rowmax == 0.f ? 1.0f : __fdiv_rn(rowmax, mode_fp8(MODE) ? 448.0f : 127.0f);
     const float inv = __fdiv_rn(1.0f, scale);
     if (tid == 0) xs[m] = scale;
-    int8_t* qr = q + (size_t)m * K;
+    uint8_t* qr = q + (size_t)m * K;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = tid + kNormThreads * i;
-      if (c < nchunks) {
+      if (mode_fp8(MODE) && c < nchunks) {
+        const float y0[4] = {yv[i][0], yv[i][1], yv[i][2], yv[i][3]};
+        const float y1[4] = {yv[i][4], yv[i][5], yv[i][6], yv[i][7]};
+        *reinterpret_cast<uint2*>(qr + 8 * c) = make_uint2(e4m3x4_div(y0, scale, inv), e4m3x4_div(y1, scale, inv));
+      } else if (c < nchunks) {
         int k8[8];
         bool exact = false;
 #pragma unroll
@@ -280,7 +291,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 template <int CPT, int MODE>
 cudaError_t launch_rows(const __half* x, const __half* residual, const __half* gamma, float eps, int M, int K,
-                        int8_t* q, float* xs, float* absmax, __half* h_out, unsigned* err, cudaStream_t s) {
+                        uint8_t* q, float* xs, float* absmax, __half* h_out, unsigned* err, cudaStream_t s) {
   auto kern = qrmsnorm_kernel<CPT, MODE>;
   const size_t smem = (size_t)norm_slots(CPT, MODE) * norm_rows_per_slot(MODE) * 2 * K;
   static int set_bytes[64] = {0};   // dynamic shared memory limit set on the kernel, per device
@@ -308,7 +319,7 @@ cudaError_t launch_rows(const __half* x, const __half* residual, const __half* g
 
 template <int MODE>
 cudaError_t launch_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps, int M, int K,
-                        int8_t* q, float* xs, float* absmax, uint16_t* h_out, unsigned* err, cudaStream_t s) {
+                        uint8_t* q, float* xs, float* absmax, uint16_t* h_out, unsigned* err, cudaStream_t s) {
   const __half* xh = reinterpret_cast<const __half*>(x);
   const __half* rh = reinterpret_cast<const __half*>(residual);
   const __half* gh = reinterpret_cast<const __half*>(gamma);
@@ -324,13 +335,21 @@ cudaError_t launch_norm(const uint16_t* x, const uint16_t* residual, const uint1
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
                                      float* xs, unsigned* dev_err, cudaStream_t s) {
-  return launch_norm<0>(x, nullptr, gamma, eps, M, K, q, xs, nullptr, nullptr, dev_err, s);
+  return launch_norm<0>(x, nullptr, gamma, eps, M, K, reinterpret_cast<uint8_t*>(q), xs, nullptr, nullptr, dev_err, s);
 }
 
 cudaError_t launch_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma,
                                          float eps, int M, int K, uint16_t* residual_out, int8_t* q, float* xs,
                                          unsigned* dev_err, cudaStream_t s) {
-  return launch_norm<2>(x, residual, gamma, eps, M, K, q, xs, nullptr, residual_out, dev_err, s);
+  return launch_norm<2>(x, residual, gamma, eps, M, K, reinterpret_cast<uint8_t*>(q), xs, nullptr, residual_out,
+                        dev_err, s);
+}
+
+cudaError_t launch_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma, float eps,
+                                      int M, int K, uint16_t* residual_out, uint8_t* q, float* xs, unsigned* dev_err,
+                                      cudaStream_t s) {
+  if (residual) return launch_norm<4>(x, residual, gamma, eps, M, K, q, xs, nullptr, residual_out, dev_err, s);
+  return launch_norm<3>(x, nullptr, gamma, eps, M, K, q, xs, nullptr, nullptr, dev_err, s);
 }
 
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,

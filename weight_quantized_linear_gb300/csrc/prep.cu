@@ -200,25 +200,28 @@ __global__ void __launch_bounds__(64)
   for (int e = 0; e < 4; ++e) atomicMax(wbits + 4 * c4 + e, __float_as_uint(m[e]));
 }
 
-// ws_n = max / 127 (1.0 for an all-zero column), in place over the max bit patterns.
-__global__ void __launch_bounds__(256) colmax_scale_kernel(float* __restrict__ ws, int N) {
+// ws_n = absmax_n / Q_MAX (127 for int8 codes, 448 for e4m3; 1.0 for an all-zero column), in place
+// over the max bit patterns.
+__global__ void __launch_bounds__(256) colmax_scale_kernel(float* __restrict__ ws, int N, float qmax) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
   const float a = ws[n];
-  ws[n] = a == 0.f ? 1.0f : __fdiv_rn(a, 127.0f);
+  ws[n] = a == 0.f ? 1.0f : __fdiv_rn(a, qmax);
 }
 
-// qw[n, k] = clamp(rint(w[k, n] / ws_n), -127, 127), transposed through a 64 x 64 shared tile:
+// qw[n, k] = clamp(rint(w[k, n] / ws_n), -127, 127) (FP8: the e4m3 code of w[k, n] / ws_n),
+// transposed through a 64 x 64 shared tile:
 // thread (ty, tx) reads rows 4 ty .. 4 ty + 3 of columns 4 tx .. 4 tx + 3 (four 16-byte loads) and
 // stores, per column, its four consecutive codes as one 32-bit word; then each thread writes 16 k
 // of one output row.  K is a multiple of 16 and N of 32, so no piece straddles an edge.
 constexpr int kQT = 64;
 constexpr int kQTStride = kQT + 4;  // bytes per tile row: 4-byte stores of a warp spread over banks
 
+template <bool FP8>
 __global__ void __launch_bounds__(256)
     quant_transpose_kernel(const float* __restrict__ w, const float* __restrict__ ws, int K, int N,
-                           int8_t* __restrict__ qw) {
-  __shared__ __align__(16) int8_t tile[kQT * kQTStride];  // tile[n][k]
+                           uint8_t* __restrict__ qw) {
+  __shared__ __align__(16) uint8_t tile[kQT * kQTStride];  // tile[n][k]
   // rows from the last tile down: the column-max pass reads high k last, so those rows are the
   // likeliest to be still in L2
   const int n0 = blockIdx.x * kQT, k0 = (gridDim.y - 1 - blockIdx.y) * kQT;
@@ -239,12 +242,20 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t word = 0u;
+    if constexpr (FP8) {
+      const float e[4] = {c == 0 ? v[0].x : c == 1 ? v[0].y : c == 2 ? v[0].z : v[0].w,
+                          c == 0 ? v[1].x : c == 1 ? v[1].y : c == 2 ? v[1].z : v[1].w,
+                          c == 0 ? v[2].x : c == 1 ? v[2].y : c == 2 ? v[2].z : v[2].w,
+                          c == 0 ? v[3].x : c == 1 ? v[3].y : c == 2 ? v[3].z : v[3].w};
+      word = e4m3x4_div(e, sc[c], inv[c]);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float e = c == 0 ? v[i].x : c == 1 ? v[i].y : c == 2 ? v[i].z : v[i].w;
-      // |w / ws| <= 127 + rounding by construction of ws; 256 bounds every unclamped value
-      const float r = fminf(fmaxf(rint_div(e, sc[c], inv[c], 256.f, 1e-4f), -127.f), 127.f);
-      word |= ((uint32_t)(int)r & 0xFFu) << (8 * i);
+      for (int i = 0; i < 4; ++i) {
+        const float e = c == 0 ? v[i].x : c == 1 ? v[i].y : c == 2 ? v[i].z : v[i].w;
+        // |w / ws| <= 127 + rounding by construction of ws; 256 bounds every unclamped value
+        const float r = fminf(fmaxf(rint_div(e, sc[c], inv[c], 256.f, 1e-4f), -127.f), 127.f);
+        word |= ((uint32_t)(int)r & 0xFFu) << (8 * i);
+      }
     }
     *reinterpret_cast<uint32_t*>(tile + (4 * tx + c) * kQTStride + 4 * ty) = word;
   }
@@ -275,7 +286,9 @@ cudaError_t launch_smooth(const float* absmax, const uint16_t* gamma, const floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws, cudaStream_t s) {
+namespace {
+template <bool FP8>
+cudaError_t launch_per_channel(const float* w, int K, int N, uint8_t* qw, float* ws, cudaStream_t s) {
   // 1. column maxima: about sixteen CTAs of 64 threads per SM, each over a slice of the rows
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(float) * (size_t)N, s);
   if (e != cudaSuccess) return e;
@@ -285,12 +298,21 @@ cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw
   const int rows_per_cta = (K + ks - 1) / ks;
   colmax_kernel<<<dim3(col_ctas, (K + rows_per_cta - 1) / rows_per_cta), 64, 0, s>>>(
       w, K, N, rows_per_cta, reinterpret_cast<unsigned*>(ws));
-  colmax_scale_kernel<<<(N + 255) / 256, 256, 0, s>>>(ws, N);
+  colmax_scale_kernel<<<(N + 255) / 256, 256, 0, s>>>(ws, N, FP8 ? 448.0f : 127.0f);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. codes, transposed to [N, K]
-  quant_transpose_kernel<<<dim3((N + kQT - 1) / kQT, (K + kQT - 1) / kQT), 256, 0, s>>>(w, ws, K, N, qw);
+  quant_transpose_kernel<FP8><<<dim3((N + kQT - 1) / kQT, (K + kQT - 1) / kQT), 256, 0, s>>>(w, ws, K, N, qw);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_per_channel_quant_i8(const float* w, int K, int N, int8_t* qw, float* ws, cudaStream_t s) {
+  return launch_per_channel<false>(w, K, N, reinterpret_cast<uint8_t*>(qw), ws, s);
+}
+
+cudaError_t launch_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, float* ws, cudaStream_t s) {
+  return launch_per_channel<true>(w, K, N, qw, ws, s);
 }
 
 }  // namespace wql

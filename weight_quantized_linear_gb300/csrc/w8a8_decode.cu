@@ -13,6 +13,10 @@
 // Weights are the 16-row MMA operand ("swap AB"), tokens the 8-column operand.  Weight tiles of
 // 128 output channels x 64 k stream once from HBM through a TMA pipeline; split-K across the
 // CTAs of a cluster, reduced through distributed shared memory in int32.
+//
+// The fp8 variant (the page's quant_dtype fp8, float8_e4m3fn codes, fp32 accumulator) runs the same
+// pipeline: every e4m3 value is an fp16 value, so one cvt per pair of codes feeds the same fp16
+// MMA; its fp32 sums are not folded, and the split-K partials are added in fp32 in rank order.
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
@@ -49,19 +53,25 @@ __device__ __forceinline__ uint32_t tile64_off(int r, int c, int t) {
   return r * 64 + (((c ^ (r >> 1)) & 3) << 4) + t * 4;
 }
 
-// Four int8 -> two f16x2 (bytes 0,1 and bytes 2,3), exact.
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = v ^ 0x80808080u;
-  lo = hadd2_u32(prmt(u, 0x64646464u, 0x4140u), 0xE480E480u);
-  hi = hadd2_u32(prmt(u, 0x64646464u, 0x4342u), 0xE480E480u);
+// Four 8-bit codes -> two f16x2 (bytes 0,1 and bytes 2,3), exact.  int8: each biased byte is placed
+// in the mantissa of 1024 + b + 128 and one f16x2 add removes 1152; e4m3: the hardware conversion.
+template <bool FP8>
+__device__ __forceinline__ void q8x4_to_h2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  if constexpr (FP8) {
+    e4m3x4_to_f16x2x2(v, lo, hi);
+  } else {
+    const uint32_t u = v ^ 0x80808080u;
+    lo = hadd2_u32(prmt(u, 0x64646464u, 0x4140u), 0xE480E480u);
+    hi = hadd2_u32(prmt(u, 0x64646464u, 0x4342u), 0xE480E480u);
+  }
 }
 
-template <int MT>
+template <int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
-    w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] int8, box {64, 8MT}, SW64
-                       const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] int8, box {64, 128}, SW64
+    w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] 8-bit codes, box {64, 8MT}, SW64
+                       const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] 8-bit codes, box {64, 128}, SW64
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int kblocks,
-                       __half* __restrict__ y, int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+                       __half* __restrict__ y, void* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = Layout8<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -89,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
 
   const int g = lane >> 2, t = lane & 3;
   const int tp = warp & 3, kp = warp >> 2;  // tile pair (32 channels) and k16 phase
-  int tot[2][MT][4];
+  int tot[2][MT][4];  // int8: exact int32 sums; fp8: the bits of the fp32 sums
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -153,8 +163,12 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            tot[a][mt][i] += __float2int_rn(acc[a][mt][i]);
-            acc[a][mt][i] = 0.f;
+            if constexpr (FP8) {
+              tot[a][mt][i] = __float_as_int(acc[a][mt][i]);
+            } else {
+              tot[a][mt][i] += __float2int_rn(acc[a][mt][i]);
+              acc[a][mt][i] = 0.f;
+            }
           }
     };
 
@@ -172,20 +186,21 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
         const int c = kp + 2 * h;  // 16-byte chunk = k16 step within the stage
         uint32_t bx[MT][2];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) i8x4_to_h2x2(lds_u32(xt + tile64_off(8 * mt + g, c, t)), bx[mt][0], bx[mt][1]);
+        for (int mt = 0; mt < MT; ++mt)
+          q8x4_to_h2x2<FP8>(lds_u32(xt + tile64_off(8 * mt + g, c, t)), bx[mt][0], bx[mt][1]);
 #pragma unroll
         for (int a = 0; a < 2; ++a) {
           const int r = 32 * tp + 16 * a + g;
           uint32_t A[4];
-          i8x4_to_h2x2(lds_u32(wt + tile64_off(r, c, t)), A[0], A[2]);
-          i8x4_to_h2x2(lds_u32(wt + tile64_off(r + 8, c, t)), A[1], A[3]);
+          q8x4_to_h2x2<FP8>(lds_u32(wt + tile64_off(r, c, t)), A[0], A[2]);
+          q8x4_to_h2x2<FP8>(lds_u32(wt + tile64_off(r + 8, c, t)), A[1], A[3]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) mma_f16_16816(acc[a][mt], A, bx[mt][0], bx[mt][1]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if ((it + 1) % kFoldStages == 0) fold();
+      if (!FP8 && (it + 1) % kFoldStages == 0) fold();
     }
     fold();
   }
@@ -211,13 +226,22 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
   const uint32_t rank = cluster_ctarank();
   const int nq = kE / 4;
   const int lmax = (nq + nsplit - 1) / nsplit;
+  // int4 of int32 sums, or of fp32 bit patterns
+  auto add4 = [](int4 a, int4 b) {
+    if constexpr (FP8)
+      return make_int4(__float_as_int(__fadd_rn(__int_as_float(a.x), __int_as_float(b.x))),
+                       __float_as_int(__fadd_rn(__int_as_float(a.y), __int_as_float(b.y))),
+                       __float_as_int(__fadd_rn(__int_as_float(a.z), __int_as_float(b.z))),
+                       __float_as_int(__fadd_rn(__int_as_float(a.w), __int_as_float(b.w))));
+    else
+      return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+  };
   {  // fold the two k-phase partials and push each slice to its owner
     const int4* r4 = reinterpret_cast<const int4*>(red);
     for (int f = threadIdx.x; f < nq; f += kThreads) {
-      const int4 a = r4[f], b = r4[nq + f];
       const int owner = slice_owner(f, nq, nsplit);
       const int f0 = (int)((long long)nq * owner / nsplit);
-      st_cluster_i4(map_cluster(recv + rank * lmax + (f - f0), owner), make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+      st_cluster_i4(map_cluster(recv + rank * lmax + (f - f0), owner), add4(r4[f], r4[nq + f]));
     }
   }
   __syncwarp();
@@ -226,13 +250,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
     const int f0 = (int)((long long)nq * rank / nsplit), f1 = (int)((long long)nq * (rank + 1) / nsplit);
     for (int f = f0 + threadIdx.x; f < f1; f += kThreads) {
       int4 v = recv[f - f0];
-      for (int q = 1; q < nsplit; ++q) {
-        const int4 p = recv[q * lmax + (f - f0)];
-        v.x += p.x;
-        v.y += p.y;
-        v.z += p.z;
-        v.w += p.w;
-      }
+      for (int q = 1; q < nsplit; ++q) v = add4(v, recv[q * lmax + (f - f0)]);
       const int row = (4 * f) / kRows, col = (4 * f) % kRows;
       const int m = m0 + row, n = strip * kRows + col;
       if (m < M && n < N) {
@@ -242,18 +260,20 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
         const float wv[4] = {wn.x, wn.y, wn.z, wn.w};
         __align__(8) __half hv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          hv[e] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(__int2float_rn(iv[e]), xm), wv[e]), ea, m, n + e, N));
+        for (int e = 0; e < 4; ++e) {
+          const float c = FP8 ? __int_as_float(iv[e]) : __int2float_rn(iv[e]);
+          hv[e] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(c, xm), wv[e]), ea, m, n + e, N));
+        }
         *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = *reinterpret_cast<const uint2*>(hv);
-        if (acc_out) *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) = v;
+        if (acc_out) reinterpret_cast<int4*>(acc_out)[((size_t)m * N + n) / 4] = v;
       }
     }
   }
 }
 
-template <int MT>
+template <int MT, bool FP8>
 cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* xs, const float* ws, int M, int N,
-                    int kblocks, __half* y, int32_t* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream) {
+                    int kblocks, __half* y, void* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream) {
   using L = Layout8<MT>;
   // 8- and 16-token launches take the same shared-memory footprint, so that back-to-back layers
   // look alike to the block scheduler whatever their token counts: it then keeps one CTA of each
@@ -265,13 +285,13 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_decode_kernel<MT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int strips = (N + kRows - 1) / kRows;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);
-  const int S = pick_k_split(reinterpret_cast<const void*>(w8a8_decode_kernel<MT>), kThreads, bytes, strips * mblocks,
+  const int S = pick_k_split(reinterpret_cast<const void*>(w8a8_decode_kernel<MT, FP8>), kThreads, bytes, strips * mblocks,
                              kblocks, /*pow2=*/false, /*balanced=*/true);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(strips, S, mblocks);
@@ -287,14 +307,13 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, w8a8_decode_kernel<MT>, tx, tw, xs, ws, M, N, kblocks, y, acc_out, ea, dev_err);
+  return cudaLaunchKernelEx(&cfg, w8a8_decode_kernel<MT, FP8>, tx, tw, xs, ws, M, N, kblocks, y, acc_out, ea, dev_err);
 }
 
-}  // namespace
-
-cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
-                               int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
-                               unsigned* dev_err, cudaStream_t stream, std::string* err) {
+template <bool FP8>
+cudaError_t launch_decode(const void* q, const float* xs, const void* qw, const float* ws, int M, int K, int N,
+                          uint16_t* y, void* acc_out, const uint16_t* bias, const uint16_t* residual, unsigned* dev_err,
+                          cudaStream_t stream, std::string* err) {
   const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
   const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
   CUtensorMap tx, tw;
@@ -308,12 +327,26 @@ cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* q
   __half* yh = reinterpret_cast<__half*>(y);
   switch (MT) {
     case 1:
-      return launch8<1>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
+      return launch8<1, FP8>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
     case 2:
-      return launch8<2>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
+      return launch8<2, FP8>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
     default:
-      return launch8<4>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
+      return launch8<4, FP8>(tx, tw, xs, ws, M, N, kblocks, yh, acc_out, ea, dev_err, stream);
   }
+}
+
+}  // namespace
+
+cudaError_t launch_w8a8_decode(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
+                               int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
+                               unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  return launch_decode<false>(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, dev_err, stream, err);
+}
+
+cudaError_t launch_fp8_decode(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,
+                              int N, uint16_t* y, float* acc_out, const uint16_t* bias, const uint16_t* residual,
+                              unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  return launch_decode<true>(q, xs, qw, ws, M, K, N, y, acc_out, bias, residual, dev_err, stream, err);
 }
 
 }  // namespace wql
