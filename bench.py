@@ -490,12 +490,19 @@ def run_sweep(args):
         del g
         return t / (reps * copies)
 
-    def emit(row, case, sec, nbytes, flops, bound, extra=None):
+    rows = [r for r in (args.rows or "").split(",") if r]
+
+    def want(*prefixes):
+        """Whether any of these row families was asked for (all of them without --rows)."""
+        return not rows or any(p.startswith(r) or r.startswith(p) for p in prefixes for r in rows)
+
+    def emit(row, case, sec, nbytes, flops, bound, extra=None, peak_tensor=None):
         gbs = nbytes / sec / 1e9
         tfs = flops / sec / 1e12
+        pt = bf16 if peak_tensor is None else peak_tensor
         rec = {"row": row, "case": case, "us": round(sec * 1e6, 3), "GB_s": round(gbs, 1), "TFLOP_s": round(tfs, 2),
-               "bound": bound, "frac": round(gbs / hbm if bound == "hbm" else tfs / bf16, 4),
-               "peak": hbm if bound == "hbm" else bf16, "peak_source": peak_src}
+               "bound": bound, "frac": round(gbs / hbm if bound == "hbm" else tfs / pt, 4),
+               "peak": hbm if bound == "hbm" else pt, "peak_source": peak_src}
         if extra:
             rec.update(extra)
         out.write(json.dumps(rec) + "\n")
@@ -503,7 +510,7 @@ def run_sweep(args):
         print(json.dumps(rec), flush=True)
 
     # a1 awq_pack (offline prep): fp32 W in, packed out
-    for (K, N, G) in [(4096, 11008, 128), (4096, 22016, 32)]:
+    for (K, N, G) in [(4096, 11008, 128), (4096, 22016, 32)] if want("a1") else ():
         W = weight(K, N, True)
         qw, s, qz = wql.awq_pack(W, G)
         sec = timed(lambda: wql.awq_pack(W, G), 1, 10)
@@ -513,7 +520,7 @@ def run_sweep(args):
     w4 = ([("tiny", c) for c in inputs.tiny_cases()] + [("decode", c) for c in inputs.decode_cases()] +
           [("sweep", c) for c in inputs.sweep_cases()] + [("prefill", c) for c in inputs.prefill_cases()])
     packed = {}
-    for fam, c in w4:
+    for fam, c in w4 if want("a2", "a3") else ():
         M, K, N, G = c["M"], c["K"], c["N"], c["G"]
         key = (K, N, G, c["w_outliers"])
         if key not in packed:
@@ -540,73 +547,111 @@ def run_sweep(args):
         del x, y
     packed.clear()
 
-    # a4 qrmsnorm_quant_i8 and a6 w8a8_gemm (SmoothQuant block, config 5)
+    # a4 qrmsnorm_quant_i8 and a6 w8a8_gemm (SmoothQuant block, Llama-7B shapes); f1 its residual and
+    # bias fusions; f2 the fp8 (e4m3) variant of the same block
     K = 4096
-    for N in (4096, 11008):
+    for N in (4096, 11008) if want("a4", "a6", "f1", "f2") else ():
         W = weight(K, N, False)
         for M in (1, 16, 512, 4096):
             X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
             g = torch.from_numpy(inputs.gamma(K, seed=0)).to(dev)
             a = wql.act_absmax(X, g, inputs.EPS)
             s_, g2, W2 = wql.smooth(a, g, W)
-            qW, ws = wql.per_channel_quant_i8(W2)
-            del W2
-            q, xs = wql.qrmsnorm_quant_i8(X, g2, inputs.EPS)
-            if N == 4096:
-                # 24 calls per graph, so that graph launch overhead does not count as kernel time
-                def norms(X=X, g2=g2, q=q, xs=xs):
-                    for _ in range(24):
-                        wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
-
-                sec = timed(norms, 24, 20)
-                emit("a4_qrmsnorm_quant_i8", f"M{M}K{K}", sec, qrmsnorm_bytes(M, K), 0, "hbm")
             per = N * K
             copies = int(max(2, min(64, -(-3 * l2 // per))))
-            stack = [qW] + [qW.clone() for _ in range(copies - 1)]
-            y = torch.empty((M, N), dtype=torch.float16, device=dev)
-            wsp = torch.empty((max(1, wql.w8a8_workspace_bytes(M, K, N)),), dtype=torch.uint8, device=dev)
-
-            def fn8(stack=stack, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
-                for w in stack:
-                    wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
-
             flops = gemm_flops(M, K, N)
             reps = 20 if flops * copies < 5e12 else 3
-            sec = timed(fn8, copies, reps)
-            emit("a6_w8a8_gemm", f"M{M}K{K}N{N}", sec, w8a8_bytes(M, K, N), flops, "hbm" if M <= 16 else "tensor",
-                 {"copies": copies, "tensor_peak_note": "int8 run as exact fp16 on kind::f16; peak = measured bf16"})
-
-            def block(stack=stack, X=X, g2=g2, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
-                for w in stack:
-                    wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
-                    wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
-
-            secb = timed(block, copies, reps)
-            emit("a4+a6_w8a8_block", f"M{M}K{K}N{N}", secb, qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N), flops,
-                 "hbm" if M <= 16 else "tensor")
-
-            # the same block with its residual and bias fusions: h = x + r feeds the norm, and the GEMM
-            # adds a bias [N] and a residual [M, N] before its single rounding to fp16
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
             R = torch.from_numpy(inputs.activations(M, K, seed=1)).to(dev)
             H = torch.empty_like(R)
             bias = torch.from_numpy(inputs.activations(1, N, seed=2)[0]).to(dev)
             RY = torch.from_numpy(inputs.activations(M, N, seed=3)).to(dev)
+            if want("a4", "a6", "f1"):
+                qW, ws = wql.per_channel_quant_i8(W2)
+                q, xs = wql.qrmsnorm_quant_i8(X, g2, inputs.EPS)
+                if N == 4096 and want("a4"):
+                    # 24 calls per graph, so that graph launch overhead does not count as kernel time
+                    def norms(X=X, g2=g2, q=q, xs=xs):
+                        for _ in range(24):
+                            wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
 
-            def fused(stack=stack, X=X, R=R, H=H, g2=g2, q=q, xs=xs, ws=ws, bias=bias, RY=RY, y=y, wsp=wsp):
-                for w in stack:
-                    wql.add_qrmsnorm_quant_i8(X, R, g2, inputs.EPS, residual_out=H, q=q, xs=xs)
-                    wql.w8a8_gemm_fused(q, xs, w, ws, bias, RY, out=y, workspace=wsp)
+                    sec = timed(norms, 24, 20)
+                    emit("a4_qrmsnorm_quant_i8", f"M{M}K{K}", sec, qrmsnorm_bytes(M, K), 0, "hbm")
+                stack = [qW] + [qW.clone() for _ in range(copies - 1)]
+                wsp = torch.empty((max(1, wql.w8a8_workspace_bytes(M, K, N)),), dtype=torch.uint8, device=dev)
 
-            secf = timed(fused, copies, reps)
-            emit("f1_w8a8_fused_block", f"M{M}K{K}N{N}", secf,
-                 add_qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N) + 2 * N + 2 * M * N, flops,
-                 "hbm" if M <= 16 else "tensor", {"unfused_us": round(secb * 1e6, 3)})
-            del stack, y, wsp, X, q, xs, qW, ws, a, s_, g2, R, H, bias, RY
+                def fn8(stack=stack, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
+                    for w in stack:
+                        wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
+
+                sec = timed(fn8, copies, reps)
+                emit("a6_w8a8_gemm", f"M{M}K{K}N{N}", sec, w8a8_bytes(M, K, N), flops, "hbm" if M <= 16 else "tensor",
+                     {"copies": copies, "tensor_peak_note": "int8 run as exact fp16 on kind::f16; peak = measured bf16"})
+
+                def block(stack=stack, X=X, g2=g2, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
+                    for w in stack:
+                        wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
+                        wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
+
+                secb = timed(block, copies, reps)
+                emit("a4+a6_w8a8_block", f"M{M}K{K}N{N}", secb, qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N), flops,
+                     "hbm" if M <= 16 else "tensor")
+
+                # the same block with its residual and bias fusions: h = x + r feeds the norm, and the
+                # GEMM adds a bias [N] and a residual [M, N] before its single rounding to fp16
+                def fused(stack=stack, X=X, R=R, H=H, g2=g2, q=q, xs=xs, ws=ws, bias=bias, RY=RY, y=y, wsp=wsp):
+                    for w in stack:
+                        wql.add_qrmsnorm_quant_i8(X, R, g2, inputs.EPS, residual_out=H, q=q, xs=xs)
+                        wql.w8a8_gemm_fused(q, xs, w, ws, bias, RY, out=y, workspace=wsp)
+
+                secf = timed(fused, copies, reps)
+                emit("f1_w8a8_fused_block", f"M{M}K{K}N{N}", secf,
+                     add_qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N) + 2 * N + 2 * M * N, flops,
+                     "hbm" if M <= 16 else "tensor", {"unfused_us": round(secb * 1e6, 3)})
+                del stack, wsp, q, xs, qW, ws
+            if want("f2"):
+                # fp8: e4m3 codes, the same byte counts as int8; the tensor roofline is the fp8 peak
+                qW8, ws8 = wql.per_channel_quant_fp8(W2)
+                q8, xs8 = wql.qrmsnorm_quant_fp8(X, g2, inputs.EPS)
+                fp8_note = {"tensor_peak_note": "kind::f8f6f4; peak = measured bf16 x 2 (nominal fp8 / bf16 ratio)"}
+                if N == 4096:
+                    def norms8(X=X, g2=g2, q=q8, xs=xs8):
+                        for _ in range(24):
+                            wql.qrmsnorm_quant_fp8(X, g2, inputs.EPS, q=q, xs=xs)
+
+                    sec = timed(norms8, 24, 20)
+                    emit("f2_qrmsnorm_quant_fp8", f"M{M}K{K}", sec, qrmsnorm_bytes(M, K), 0, "hbm")
+                stack8 = [qW8] + [qW8.clone() for _ in range(copies - 1)]
+
+                def fnf(stack=stack8, q=q8, xs=xs8, ws=ws8, y=y):
+                    for w in stack:
+                        wql.w8a8_gemm_fp8(q, xs, w, ws, out=y)
+
+                sec = timed(fnf, copies, reps)
+                emit("f2_w8a8_gemm_fp8", f"M{M}K{K}N{N}", sec, w8a8_bytes(M, K, N), flops,
+                     "hbm" if M <= 16 else "tensor", dict(copies=copies, **fp8_note), peak_tensor=2 * bf16)
+
+                def fblock(stack=stack8, X=X, R=R, H=H, g2=g2, q=q8, xs=xs8, ws=ws8, bias=bias, RY=RY, y=y):
+                    for w in stack:
+                        wql.add_qrmsnorm_quant_fp8(X, R, g2, inputs.EPS, residual_out=H, q=q, xs=xs)
+                        wql.w8a8_gemm_fp8(q, xs, w, ws, bias, RY, out=y)
+
+                sec = timed(fblock, copies, reps)
+                emit("f2_fp8_fused_block", f"M{M}K{K}N{N}", sec,
+                     add_qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N) + 2 * N + 2 * M * N, flops,
+                     "hbm" if M <= 16 else "tensor", fp8_note, peak_tensor=2 * bf16)
+                del stack8, q8, xs8, qW8, ws8
+            del y, X, a, s_, g2, W2, R, H, bias, RY
 
     # a5 per-channel weight quantisation (offline prep)
-    W = weight(4096, 11008, False)
-    sec = timed(lambda: wql.per_channel_quant_i8(W), 1, 10)
-    emit("a5_per_channel_quant_i8", "K4096N11008", sec, 4096 * 11008 * 5 + 11008 * 4, 0, "hbm")
+    if want("a5"):
+        W = weight(4096, 11008, False)
+        sec = timed(lambda: wql.per_channel_quant_i8(W), 1, 10)
+        emit("a5_per_channel_quant_i8", "K4096N11008", sec, 4096 * 11008 * 5 + 11008 * 4, 0, "hbm")
+    if want("f2"):
+        W = weight(4096, 11008, False)
+        sec = timed(lambda: wql.per_channel_quant_fp8(W), 1, 10)
+        emit("f2_per_channel_quant_fp8", "K4096N11008", sec, 4096 * 11008 * 5 + 11008 * 4, 0, "hbm")
     wql.device_status(dev)
     out.close()
     return 0
@@ -619,8 +664,8 @@ def run_sweep(args):
 def run_profile_case(args):
     """A few calls of one operation on one shape, for a profiler to capture.
 
-    ``w4a16:M,K,N,G``, ``w8a8:M,K,N``, ``norm:M,K`` or ``prep:K,N`` (awq_pack with G = 128, then
-    per_channel_quant_i8).  Each operation is called ``--calls`` times on synthetic inputs.
+    ``w4a16:M,K,N,G``, ``w8a8:M,K,N``, ``fp8:M,K,N``, ``norm:M,K``, ``normfp8:M,K`` or ``prep:K,N``
+    (awq_pack with G = 128, then per_channel_quant_i8).  Each operation is called ``--calls`` times on synthetic inputs.
     """
     import numpy as np
     import torch
@@ -649,6 +694,22 @@ def run_profile_case(args):
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
         for _ in range(calls):
             wql.w8a8_gemm(q, xs, qW, ws, out=y)
+    elif op == "fp8":
+        M, K, N = d
+        rng = np.random.default_rng(0)
+        q8 = (torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)) * 60).to(wql.E4M3).to(dev)
+        qW8 = (torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)) * 60).to(wql.E4M3).to(dev)
+        xs = torch.full((M,), 0.01, device=dev)
+        ws = torch.full((N,), 0.001, device=dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for _ in range(calls):
+            wql.w8a8_gemm_fp8(q8, xs, qW8, ws, out=y)
+    elif op == "normfp8":
+        M, K = d
+        X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
+        g = torch.from_numpy(inputs.gamma(K, seed=0)).to(dev)
+        for _ in range(calls):
+            wql.qrmsnorm_quant_fp8(X, g, inputs.EPS)
     elif op == "norm":
         M, K = d
         X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
@@ -680,8 +741,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None, help="measure every hot-path row; JSON lines to this file")
     ap.add_argument("--profile-case", default=None,
-                    help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N | norm:M,K | prep:K,N")
+                    help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N | fp8:M,K,N | norm:M,K | "
+                         "normfp8:M,K | prep:K,N")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--rows", default=None,
+                    help="with --sweep: comma-separated row families to measure (e.g. a6,f2); default all")
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)

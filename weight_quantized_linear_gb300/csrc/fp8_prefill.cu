@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fp8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // q e4m3 [M][K], box {128, BN}, SW128
                        const __grid_constant__ CUtensorMap tm_w,  // qw e4m3 [N][K], box {128, 128}, SW128
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
-                       __half* __restrict__ y, float* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+                       __half* y, float* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = FLayout<BN>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tcount & 1;
       const int n = nt * kBM + quad * 32 + lane;
       const float wn = n < N ? ws[n] : 0.f;
+      const float bn = (ea.bias && n < N) ? __half2float(ea.bias[n]) : 0.f;
       if (!mbar_wait_warp(&accfull[b], (tcount >> 1) & 1)) {
         report_error(err, kErrTimeoutMma);
         break;
@@ -181,17 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < BN; cc += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(lane_base + b * BN + cc, r);
-        tmem_ld_wait();
+        // the chunk's 32 token scales (one load per lane, then broadcast) and residual values are all
+        // loaded before the first store
         const int mbase = mt * BN + cc;
-        if (n < N) {
+        const float xl = mbase + lane < M ? xs[mbase + lane] : 0.f;
+        float rv[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int m = mbase + k;
-            if (m < M) {
-              const float c = __uint_as_float(r[k]);
-              y[(size_t)m * N + n] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(c, xs[m]), wn), ea, m, n, N));
-              if (acc_out) acc_out[(size_t)m * N + n] = c;
-            }
+        for (int k = 0; k < 32; ++k)
+          rv[k] = (ea.residual && n < N && mbase + k < M) ? __half2float(ea.residual[(size_t)(mbase + k) * N + n]) : 0.f;
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int m = mbase + k;
+          const float xm = __shfl_sync(0xffffffffu, xl, k);
+          if (n < N && m < M) {
+            const float c = __uint_as_float(r[k]);
+            y[(size_t)m * N + n] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(c, xm), wn), ea, bn, rv[k]));
+            if (acc_out) acc_out[(size_t)m * N + n] = c;
           }
         }
       }
@@ -235,13 +242,12 @@ cudaError_t launch_f(const void* q, const void* qw, const float* xs, const float
 
 }  // namespace
 
-// Token tile for an fp8 GEMM of M tokens: 64 up to 64 tokens; otherwise 128 or 256, whichever needs
-// fewer tile-columns of work on the busiest SM (waves of tiles times tokens per tile).
+// Token tile for an fp8 GEMM of M tokens: 64 up to 64 tokens, else 128.  A 256-token tile (fewer,
+// longer tiles, four stages) measured slower at every shape tried on GB300 (K = 4096, N = 4096 and
+// 11008, M = 128 .. 8192: e.g. M = 4096, N = 11008: 198 vs 182 us; M = 512, N = 4096: 28.4 vs 19.8 us).
 int fp8_prefill_tile_n(int M, int N) {
-  if (M <= 64) return 64;
-  const long long ntn = (N + kBM - 1) / kBM, sms = num_sms();
-  const long long w128 = (ntn * ((M + 127) / 128) + sms - 1) / sms, w256 = (ntn * ((M + 255) / 256) + sms - 1) / sms;
-  return w256 * 256 <= w128 * 128 ? 256 : 128;
+  (void)N;
+  return M <= 64 ? 64 : 128;
 }
 
 cudaError_t launch_fp8_prefill(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
     w8a8_decode_kernel(const __grid_constant__ CUtensorMap tm_x,  // q [M][K] 8-bit codes, box {64, 8MT}, SW64
                        const __grid_constant__ CUtensorMap tm_w,  // qw [N][K] 8-bit codes, box {64, 128}, SW64
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int kblocks,
-                       __half* __restrict__ y, void* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+                       __half* y, void* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = Layout8<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -258,11 +258,14 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
         const float4 wn = *reinterpret_cast<const float4*>(ws + n);
         const int iv[4] = {v.x, v.y, v.z, v.w};
         const float wv[4] = {wn.x, wn.y, wn.z, wn.w};
+        float bv[4] = {0.f, 0.f, 0.f, 0.f}, rv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ea.bias) load_half4(ea.bias + n, bv);
+        if (ea.residual) load_half4(ea.residual + (size_t)m * N + n, rv);
         __align__(8) __half hv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float c = FP8 ? __int_as_float(iv[e]) : __int2float_rn(iv[e]);
-          hv[e] = __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(c, xm), wv[e]), ea, m, n + e, N));
+          hv[e] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(c, xm), wv[e]), ea, bv[e], rv[e]));
         }
         *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = *reinterpret_cast<const uint2*>(hv);
         if (acc_out) reinterpret_cast<int4*>(acc_out)[((size_t)m * N + n) / 4] = v;

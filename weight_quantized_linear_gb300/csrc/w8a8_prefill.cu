@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w8a8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // fp16 codes [M][K], box {64, BN}, SW128
                         const __grid_constant__ CUtensorMap tm_w,  // qw int8 [N][K], box {64, 128}
                         const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
-                        __half* __restrict__ y, int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+                        __half* y, int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
   using L = QLayout<BN>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = tile % ntn, mt = tile / ntn;
       const int n = nt * kBM + n_in_tile;
       const float wn = n < N ? ws[n] : 0.f;
+      const float bn = (ea.bias && n < N) ? __half2float(ea.bias[n]) : 0.f;
       for (int c = 0; c < nchunks; ++c, ++cseq) {
         const int b = cseq & 1;
         if (!mbar_wait_warp(&accfull[b], (cseq >> 1) & 1)) {
@@ -290,15 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!last) {
             tmem_st_32x32b_x32(lane_base + sum_col + cc, sacc);
             tmem_st_wait();
-          } else if (n < N) {
+          } else {
+            // the chunk's 32 token scales (one load per lane, then broadcast) and residual values
+            // are all loaded before the first store
             const int mbase = mt * BN + cc;
+            const float xl = mbase + lane < M ? xs[mbase + lane] : 0.f;
+            float rv[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              rv[k] = (ea.residual && n < N && mbase + k < M) ? __half2float(ea.residual[(size_t)(mbase + k) * N + n])
+                                                               : 0.f;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int m = mbase + k;
-              if (m < M) {
+              const float xm = __shfl_sync(0xffffffffu, xl, k);
+              if (n < N && m < M) {
                 const int a = (int)sacc[k];
-                y[(size_t)m * N + n] =
-                    __float2half_rn(epilogue_add(__fmul_rn(__fmul_rn(__int2float_rn(a), xs[m]), wn), ea, m, n, N));
+                y[(size_t)m * N + n] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(__int2float_rn(a), xm), wn), ea, bn, rv[k]));
                 if (acc_out) acc_out[(size_t)m * N + n] = a;
               }
             }
