@@ -695,15 +695,18 @@ def run_profile_case(args):
         for _ in range(calls):
             wql.w8a8_gemm(q, xs, qW, ws, out=y)
     elif op == "fp8":
-        M, K, N = d
+        M, K, N = d[:3]
+        fused = len(d) > 3 and d[3] == 1  # fp8:M,K,N,1 adds a bias and a residual in the epilogue
         rng = np.random.default_rng(0)
         q8 = (torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)) * 60).to(wql.E4M3).to(dev)
         qW8 = (torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)) * 60).to(wql.E4M3).to(dev)
         xs = torch.full((M,), 0.01, device=dev)
         ws = torch.full((N,), 0.001, device=dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        bias = torch.zeros((N,), dtype=torch.float16, device=dev) if fused else None
+        res = torch.ones((M, N), dtype=torch.float16, device=dev) if fused else None
         for _ in range(calls):
-            wql.w8a8_gemm_fp8(q8, xs, qW8, ws, out=y)
+            wql.w8a8_gemm_fp8(q8, xs, qW8, ws, bias, res, out=y)
     elif op == "normfp8":
         M, K = d
         X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)

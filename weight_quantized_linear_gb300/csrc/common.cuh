@@ -16,6 +16,7 @@ enum : unsigned {
   kErrTimeoutEmpty = 2u,   // producer gave up waiting for a free stage
   kErrTimeoutMma = 4u,     // MMA / accumulator hand-off wait expired
   kErrTimeoutDrain = 8u,   // exit-time drain of in-flight copies expired
+  kErrSmemAlign = 16u,     // dynamic shared memory not 1024-byte aligned where a kernel has no slack for it
 };
 
 // A bounded wait polls for at most this long (nanoseconds of %globaltimer).  Normal waits take
@@ -120,6 +121,21 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+// 2D tiled store of a shared-memory box to global memory at (x = inner, y = outer coordinate); the
+// part of the box outside the tensor is not written.  Completion is tracked per issuing thread
+// through bulk groups: bulk_commit_group() after the stores, then one of the waits below.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Every bulk store committed by this thread has finished reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every bulk store committed by this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Generic-proxy writes to shared memory become visible to the async proxy (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -11,6 +11,18 @@
 // MMA issuer (and TMEM owner), warps 2-5 the epilogue.  Two TMEM accumulators of BN columns alternate
 // between tiles, so a tile's epilogue overlaps the next tile's MMAs.  Persistent CTAs walk the tiles,
 // channel tiles fastest (CTAs running at the same time share the token tile).
+//
+// The epilogue stages its output through shared memory: each epilogue warp owns 32 channels and
+// works on 32 tokens at a time, in a 32 x 32 fp16 box.  When a residual is fused, TMA loads the next
+// box of it into the warp's other buffer while the current one is computed (the values are then
+// replaced by the outputs in place); a TMA store writes each finished box to y.  So the epilogue
+// issues no scalar global loads or stores on its critical path (the residual read through scalar
+// loads doubled the kernel's time: ncu, M = N = K = 4096, 82.5 -> 161 us).
+//
+// One CTA's MMA thread keeps the tensor pipe busy only about 40 % of the time (ncu, M = N = K = 4096:
+// its barrier round trips and commits leave gaps that deeper stages or 256-k stages do not close).
+// When there are more tiles than SMs, two CTAs of three stages share each SM and fill each other's
+// gaps: M = 8192, N = 4096: 143 -> 107 us; M = 4096, N = 11008: 184 -> 144 us.
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
@@ -24,40 +36,55 @@ constexpr int kBM = 128;  // output channels per tile (MMA M)
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 
-template <int BN>
+template <int BN, int CTAS>
 struct FLayout {
   static constexpr int kWBytes = kBM * kBK;  // 128 channel rows x 128 B, 128-byte swizzle
   static constexpr int kXBytes = BN * kBK;   // BN token rows x 128 B
   static constexpr int kStage = kWBytes + kXBytes;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kStages = CTAS == 2 ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
-  static constexpr int kBarBytes = (2 * kStages + 5) * 8 + 16;
-  static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
+  static constexpr int kBox = 32 * 32 * 2;                     // one 32 tokens x 32 channels fp16 box
+  static constexpr int kOffOut = kStages * kStage;             // [epilogue warp][2 buffers] boxes
+  static constexpr int kOffBar = kOffOut + kEpiWarps * 2 * kBox;
+  static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kEpiWarps) * 8 + 16;
+  // Two CTAs per SM leave no room for aligning the dynamic shared memory by hand: the kernel then
+  // relies on its base being 1024-byte aligned (it is placed right after the reserved 1 KB), checks
+  // it, and reports kErrSmemAlign instead of running if it is not.
+  static constexpr int kSlack = CTAS == 2 ? 0 : 1024;
+  static constexpr int kBytes = kOffBar + kBarBytes + kSlack;
   static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle atoms");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kBytes <= (CTAS == 2 ? 113 : 227) * 1024, "shared memory budget");
+  static_assert(CTAS == 1 || 2 * kTmemCols <= 512, "TMEM budget of two CTAs per SM");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS)
     fp8_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,  // q e4m3 [M][K], box {128, BN}, SW128
                        const __grid_constant__ CUtensorMap tm_w,  // qw e4m3 [N][K], box {128, 128}, SW128
+                       const __grid_constant__ CUtensorMap tm_y,  // y fp16 [M][N], box {32, 32}
+                       const __grid_constant__ CUtensorMap tm_r,  // residual fp16 [M][N], box {32, 32}
                        const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
-                       __half* y, float* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
-  using L = FLayout<BN>;
+                       float* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+  using L = FLayout<BN, CTAS>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
+  if (smem - smem_raw > L::kSlack) {  // uniform over the CTA: before any barrier or TMEM use
+    if (threadIdx.x == 0) report_error(err, kErrSmemAlign);
+    return;
+  }
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* empty = full + kStages;     // the stage's MMAs have completed
   uint64_t* accfull = empty + kStages;  // [2] accumulator holds a finished tile
   uint64_t* accempty = accfull + 2;     // [2] epilogue has read the accumulator
   uint64_t* finalbar = accempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
+  uint64_t* rfull = finalbar + 1;       // [epilogue warp][2] residual box landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + 2 * kEpiWarps);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntn = (N + kBM - 1) / kBM;
@@ -74,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accempty[b], kEpiWarps);
     }
     mbar_init(finalbar, 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rfull[i], 1);
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
@@ -164,47 +192,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue: TMEM lane = output channel, column = token ----------------
+    const int ew = warp - kEpiWarp0;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    __half* box = reinterpret_cast<__half*>(smem + L::kOffOut + ew * 2 * L::kBox);  // [2][32 tokens][32 ch]
+    uint64_t* rbar = rfull + 2 * ew;
+    const bool has_res = ea.residual != nullptr;
+    uint32_t rph = 0;   // parity of the next wait on rbar[0] (bit 0) and rbar[1] (bit 1)
+    uint32_t pend = 0;  // residual loads issued and not yet waited for, per buffer
+    int seq = 0;        // boxes handled by this warp so far (buffer = seq & 1)
+    // lane 0: load the residual box of tokens m0.. for this warp's channels into buffer `buf`, once
+    // the store that last read that buffer is done with it
+    auto load_res = [&](int buf, int n0, int m0) {
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive_expect_tx(&rbar[buf], L::kBox);
+        tma_load_2d(box + buf * 32 * 32, &tm_r, &rbar[buf], n0, m0);
+      }
+      pend |= 1u << buf;
+    };
     int tcount = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcount) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tcount) {
       const int nt = tile % ntn, mt = tile / ntn;
       const int b = tcount & 1;
-      const int n = nt * kBM + quad * 32 + lane;
+      const int n0 = nt * kBM + quad * 32, n = n0 + lane;
       const float wn = n < N ? ws[n] : 0.f;
       const float bn = (ea.bias && n < N) ? __half2float(ea.bias[n]) : 0.f;
+      if (has_res) load_res(seq & 1, n0, mt * BN);  // lands while the tile's MMAs run
       if (!mbar_wait_warp(&accfull[b], (tcount >> 1) & 1)) {
         report_error(err, kErrTimeoutMma);
         break;
       }
       tc_fence_after_sync();
 #pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 32) {
+      for (int cc = 0; cc < BN; cc += 32, ++seq) {
+        const int buf = seq & 1;
+        __half* bx = box + buf * 32 * 32;
+        if (has_res && cc + 32 < BN) load_res(buf ^ 1, n0, mt * BN + cc + 32);
         uint32_t r[32];
         tmem_ld_32x32b_x32(lane_base + b * BN + cc, r);
-        // the chunk's 32 token scales (one load per lane, then broadcast) and residual values are all
-        // loaded before the first store
         const int mbase = mt * BN + cc;
         const float xl = mbase + lane < M ? xs[mbase + lane] : 0.f;
-        float rv[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          rv[k] = (ea.residual && n < N && mbase + k < M) ? __half2float(ea.residual[(size_t)(mbase + k) * N + n]) : 0.f;
         tmem_ld_wait();
+        if (has_res) {
+          if (!mbar_wait_warp(&rbar[buf], (rph >> buf) & 1)) {
+            report_error(err, kErrTimeoutFull);
+            ok = false;
+            break;
+          }
+          rph ^= 1u << buf;
+          pend &= ~(1u << buf);
+        } else {
+          if (lane == 0) bulk_wait_read_all();  // the store that last read this buffer
+          __syncwarp();
+        }
+        // row k of the box = token mbase + k; lane = channel: 32 lanes touch 64 contiguous bytes
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int m = mbase + k;
           const float xm = __shfl_sync(0xffffffffu, xl, k);
-          if (n < N && m < M) {
-            const float c = __uint_as_float(r[k]);
-            y[(size_t)m * N + n] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(c, xm), wn), ea, bn, rv[k]));
-            if (acc_out) acc_out[(size_t)m * N + n] = c;
-          }
+          const float c = __uint_as_float(r[k]);
+          const float rr = has_res ? __half2float(bx[k * 32 + lane]) : 0.f;
+          bx[k * 32 + lane] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(c, xm), wn), ea, bn, rr));
+          if (acc_out && n < N && mbase + k < M) acc_out[(size_t)(mbase + k) * N + n] = c;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_y, bx, n0, mbase);  // clipped to [M, N]
+          bulk_commit_group();
         }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
+    }
+    if (lane == 0) {
+      bulk_wait_all();
+      // after an expired wait, leave no residual copy in flight
+      for (int i = 0; i < 2; ++i)
+        if (((pend >> i) & 1) && !mbar_wait_bounded(&rbar[i], (rph >> i) & 1)) report_error(err, kErrTimeoutDrain);
     }
   }
 
@@ -214,18 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
-template <int BN>
-cudaError_t launch_f(const void* q, const void* qw, const float* xs, const float* ws, int M, int N, int K, __half* y,
-                     float* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream, std::string* err) {
-  using L = FLayout<BN>;
-  auto kern = fp8_prefill_kernel<BN>;
-  CUtensorMap tx, tw;
-  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, K, M, (uint64_t)K, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B,
-                    err) ||
-      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
-                    err)) {
-    return cudaErrorInvalidValue;
-  }
+template <int BN, int CTAS>
+cudaError_t launch_f(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const CUtensorMap& tr,
+                     const float* xs, const float* ws, int M, int N, int K, float* acc_out, EpilogueAdd ea,
+                     unsigned* dev_err, cudaStream_t stream) {
+  using L = FLayout<BN, CTAS>;
+  auto kern = fp8_prefill_kernel<BN, CTAS>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -235,9 +296,32 @@ cudaError_t launch_f(const void* q, const void* qw, const float* xs, const float
     attr_set[dev] = true;
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, y, acc_out, ea, dev_err);
+  const int grid = ntiles < CTAS * num_sms() ? ntiles : CTAS * num_sms();
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err);
   return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_bn(const void* q, const void* qw, const float* xs, const float* ws, int M, int N, int K, __half* y,
+                      float* acc_out, EpilogueAdd ea, unsigned* dev_err, cudaStream_t stream, std::string* err) {
+  CUtensorMap tx, tw, ty, tr;
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, K, M, (uint64_t)K, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B,
+                    err) ||
+      !make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qw, K, N, (uint64_t)K, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                    err) ||
+      !make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, y, N, M, (uint64_t)N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    err) ||
+      (ea.residual && !make_tmap_2d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ea.residual, N, M, (uint64_t)N * 2, 32, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, err))) {
+    return cudaErrorInvalidValue;
+  }
+  if (!ea.residual) tr = ty;  // not read
+  // two CTAs per SM only when every SM gets at least one tile: with fewer tiles than SMs the block
+  // scheduler may pair CTAs on some SMs while others stay idle (M = 512, N = 4096: 19.6 -> 20.5 us)
+  const long long ntiles = (long long)((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  if constexpr (BN == 128)
+    if (ntiles > num_sms()) return launch_f<BN, 2>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
+  return launch_f<BN, 1>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
 }
 
 }  // namespace
@@ -255,14 +339,8 @@ cudaError_t launch_fp8_prefill(const uint8_t* q, const float* xs, const uint8_t*
                                unsigned* dev_err, cudaStream_t stream, std::string* err) {
   const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
   __half* yh = reinterpret_cast<__half*>(y);
-  switch (fp8_prefill_tile_n(M, N)) {
-    case 64:
-      return launch_f<64>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
-    case 128:
-      return launch_f<128>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
-    default:
-      return launch_f<256>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
-  }
+  if (fp8_prefill_tile_n(M, N) == 64) return launch_bn<64>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
+  return launch_bn<128>(q, qw, xs, ws, M, N, K, yh, acc_out, ea, dev_err, stream, err);
 }
 
 }  // namespace wql
