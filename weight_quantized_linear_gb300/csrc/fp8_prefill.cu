@@ -13,11 +13,11 @@
 // channel tiles fastest (CTAs running at the same time share the token tile).
 //
 // The epilogue stages its output through shared memory: each epilogue warp owns 32 channels and
-// works on 32 tokens at a time, in a 32 x 32 fp16 box.  When a residual is fused, TMA loads the next
-// box of it into the warp's other buffer while the current one is computed (the values are then
-// replaced by the outputs in place); a TMA store writes each finished box to y.  So the epilogue
-// issues no scalar global loads or stores on its critical path (the residual read through scalar
-// loads doubled the kernel's time: ncu, M = N = K = 4096, 82.5 -> 161 us).
+// works on 32 tokens at a time, in a 32 x 32 fp16 box.  When a residual is fused, TMA loads the
+// tile's residual boxes ahead (all four with one CTA per SM, two with two) while the tile's MMAs
+// run, and the outputs replace them in place; a TMA store writes each finished box to y.  So the
+// epilogue issues no scalar global loads or stores on its critical path (the residual read through
+// scalar loads doubled the kernel's time: ncu, M = N = K = 4096, 82.5 -> 161 us).
 //
 // One CTA's MMA thread keeps the tensor pipe busy only about 40 % of the time (ncu, M = N = K = 4096:
 // its barrier round trips and commits leave gaps that deeper stages or 256-k stages do not close).
@@ -44,9 +44,10 @@ struct FLayout {
   static constexpr int kStages = CTAS == 2 ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
   static constexpr int kBox = 32 * 32 * 2;                     // one 32 tokens x 32 channels fp16 box
-  static constexpr int kOffOut = kStages * kStage;             // [epilogue warp][2 buffers] boxes
-  static constexpr int kOffBar = kOffOut + kEpiWarps * 2 * kBox;
-  static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kEpiWarps) * 8 + 16;
+  static constexpr int kBufs = CTAS == 2 ? 2 : 4;              // output boxes per epilogue warp
+  static constexpr int kOffOut = kStages * kStage;             // [epilogue warp][kBufs] boxes
+  static constexpr int kOffBar = kOffOut + kEpiWarps * kBufs * kBox;
+  static constexpr int kBarBytes = (2 * kStages + 5 + kBufs * kEpiWarps) * 8 + 16;
   // Two CTAs per SM leave no room for aligning the dynamic shared memory by hand: the kernel then
   // relies on its base being 1024-byte aligned (it is placed right after the reserved 1 KB), checks
   // it, and reports kErrSmemAlign instead of running if it is not.
@@ -83,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, CTAS)
   uint64_t* accfull = empty + kStages;  // [2] accumulator holds a finished tile
   uint64_t* accempty = accfull + 2;     // [2] epilogue has read the accumulator
   uint64_t* finalbar = accempty + 2;
-  uint64_t* rfull = finalbar + 1;       // [epilogue warp][2] residual box landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + 2 * kEpiWarps);
+  uint64_t* rfull = finalbar + 1;       // [epilogue warp][kBufs] residual box landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + L::kBufs * kEpiWarps);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntn = (N + kBM - 1) / kBM;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, CTAS)
       mbar_init(&accempty[b], kEpiWarps);
     }
     mbar_init(finalbar, 1);
-    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rfull[i], 1);
+    for (int i = 0; i < L::kBufs * kEpiWarps; ++i) mbar_init(&rfull[i], 1);
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
@@ -195,22 +196,9 @@ __global__ void __launch_bounds__(kThreads, CTAS)
     const int ew = warp - kEpiWarp0;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    __half* box = reinterpret_cast<__half*>(smem + L::kOffOut + ew * 2 * L::kBox);  // [2][32 tokens][32 ch]
-    uint64_t* rbar = rfull + 2 * ew;
-    const bool has_res = ea.residual != nullptr;
-    uint32_t rph = 0;   // parity of the next wait on rbar[0] (bit 0) and rbar[1] (bit 1)
-    uint32_t pend = 0;  // residual loads issued and not yet waited for, per buffer
-    int seq = 0;        // boxes handled by this warp so far (buffer = seq & 1)
-    // lane 0: load the residual box of tokens m0.. for this warp's channels into buffer `buf`, once
-    // the store that last read that buffer is done with it
-    auto load_res = [&](int buf, int n0, int m0) {
-      if (lane == 0) {
-        bulk_wait_read_all();
-        mbar_arrive_expect_tx(&rbar[buf], L::kBox);
-        tma_load_2d(box + buf * 32 * 32, &tm_r, &rbar[buf], n0, m0);
-      }
-      pend |= 1u << buf;
-    };
+    BoxStage<L::kBufs> out;
+    out.init(reinterpret_cast<__half*>(smem + L::kOffOut + ew * L::kBufs * L::kBox), rfull + ew * L::kBufs, &tm_y,
+             &tm_r, ea.residual != nullptr);
     int tcount = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tcount) {
@@ -219,60 +207,41 @@ __global__ void __launch_bounds__(kThreads, CTAS)
       const int n0 = nt * kBM + quad * 32, n = n0 + lane;
       const float wn = n < N ? ws[n] : 0.f;
       const float bn = (ea.bias && n < N) ? __half2float(ea.bias[n]) : 0.f;
-      if (has_res) load_res(seq & 1, n0, mt * BN);  // lands while the tile's MMAs run
+      out.begin(n0, mt * BN, BN / 32, lane);  // residual boxes land while the tile's MMAs run
       if (!mbar_wait_warp(&accfull[b], (tcount >> 1) & 1)) {
         report_error(err, kErrTimeoutMma);
         break;
       }
       tc_fence_after_sync();
 #pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 32, ++seq) {
-        const int buf = seq & 1;
-        __half* bx = box + buf * 32 * 32;
-        if (has_res && cc + 32 < BN) load_res(buf ^ 1, n0, mt * BN + cc + 32);
+      for (int j = 0; j < BN / 32; ++j) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_base + b * BN + cc, r);
-        const int mbase = mt * BN + cc;
+        tmem_ld_32x32b_x32(lane_base + b * BN + 32 * j, r);
+        const int mbase = mt * BN + 32 * j;
         const float xl = mbase + lane < M ? xs[mbase + lane] : 0.f;
         tmem_ld_wait();
-        if (has_res) {
-          if (!mbar_wait_warp(&rbar[buf], (rph >> buf) & 1)) {
-            report_error(err, kErrTimeoutFull);
-            ok = false;
-            break;
-          }
-          rph ^= 1u << buf;
-          pend &= ~(1u << buf);
-        } else {
-          if (lane == 0) bulk_wait_read_all();  // the store that last read this buffer
-          __syncwarp();
+        __half* bx = out.acquire(j, lane);
+        if (!bx) {
+          report_error(err, kErrTimeoutFull);
+          ok = false;
+          break;
         }
         // row k of the box = token mbase + k; lane = channel: 32 lanes touch 64 contiguous bytes
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const float xm = __shfl_sync(0xffffffffu, xl, k);
           const float c = __uint_as_float(r[k]);
-          const float rr = has_res ? __half2float(bx[k * 32 + lane]) : 0.f;
+          const float rr = out.has_res ? __half2float(bx[k * 32 + lane]) : 0.f;
           bx[k * 32 + lane] = __float2half_rn(add_terms(__fmul_rn(__fmul_rn(c, xm), wn), ea, bn, rr));
           if (acc_out && n < N && mbase + k < M) acc_out[(size_t)(mbase + k) * N + n] = c;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tm_y, bx, n0, mbase);  // clipped to [M, N]
-          bulk_commit_group();
-        }
+        out.store(j, bx, lane);
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
     }
-    if (lane == 0) {
-      bulk_wait_all();
-      // after an expired wait, leave no residual copy in flight
-      for (int i = 0; i < 2; ++i)
-        if (((pend >> i) & 1) && !mbar_wait_bounded(&rbar[i], (rph >> i) & 1)) report_error(err, kErrTimeoutDrain);
-    }
+    if (!out.finish(lane)) report_error(err, kErrTimeoutDrain);
   }
 
   tc_fence_before_sync();
