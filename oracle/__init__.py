@@ -60,6 +60,8 @@ _SIGS = {
     "wql_oracle_per_channel_quant_fp8": (None, [_P, _I, _I, _P, _P]),
     "wql_oracle_fp8_acc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "wql_oracle_fp8_epilogue_f64": (None, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "wql_oracle_kv_quant_i8": (None, [_P, _I64, _I, _P, _P]),
+    "wql_oracle_kv_dequant_i8": (None, [_P, _P, _I64, _I, _P]),
 }
 
 
@@ -366,6 +368,28 @@ def fp8_epilogue_f64(acc, xs, ws, bias=None, residual=None) -> np.ndarray:
     _load().wql_oracle_fp8_epilogue_f64(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)),
                                         None if b is None else _ptr(b), None if r is None else _ptr(r), R, N, _ptr(y))
     return y
+
+
+# ---- KV-cache int8, groups of 128 ------------------------------------------------------------
+
+def kv_quant_i8(kv):
+    """kv [rows, D] fp16 (D % 128 == 0) -> (q int8 [rows, D], scales fp32 [rows, D / 128])."""
+    kb = _half_bits(kv)
+    rows, D = kb.shape
+    assert D % 128 == 0
+    q = np.empty((rows, D), np.int8)
+    s = np.empty((rows, D // 128), np.float32)
+    _load().wql_oracle_kv_quant_i8(_ptr(kb), rows, D, _ptr(q), _ptr(s))
+    return q, s
+
+
+def kv_dequant_i8(q, scales) -> np.ndarray:
+    """fp16 [rows, D] = fp16(q * scale of the element's group)."""
+    q = _c(q, np.int8)
+    rows, D = q.shape
+    out = np.empty((rows, D), np.uint16)
+    _load().wql_oracle_kv_dequant_i8(_ptr(q), _ptr(_c(scales, np.float32)), rows, D, _ptr(out))
+    return out.view(np.float16)
 
 
 def sym_int4_per_tensor(w):

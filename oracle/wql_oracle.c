@@ -21,6 +21,8 @@
  *          matmul_kernel_dynamic_quant: int32 accumulator, c = c * rms_scale * linear_scale),
  *          and its fp8 variant (quant_dtype fp8 = float8_e4m3fn, Q_MAX from torch.finfo, values
  *          cast instead of rounded to integers, fp32 accumulator).
+ *   [FastLLM] "FastLLM architecture" article, section 5.2 (KV cache quantised to int8 in groups of
+ *          128, dequantised when read).
  *
  * Readings taken where the pages are silent (each one is listed in the design notes):
  *   - zero point is an integer z in [0,15] stored 8 per uint32 like the codes; w ~ (q - z) * s;
@@ -548,6 +550,43 @@ void wql_oracle_fp8_epilogue_f64(const double* acc, const float* xs, const float
       if (bias) u += (double)wql_oracle_half_to_float(bias[n]);
       if (residual) u += (double)wql_oracle_half_to_float(residual[(size_t)i * N + n]);
       y[(size_t)i * N + n] = u;
+    }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * [FastLLM] section 5.2: the KV cache quantised from fp16 to int8 in groups of 128, with the
+ * dequantisation done when the cache is read.  The page fixes the width (int8) and the group size
+ * (128) only.  Reading: a group is 128 consecutive channels of one row (one token's K or V
+ * vector), symmetric like the pages' per-token int8 -- s = absmax / 127 in fp32 (1.0 for an
+ * all-zero group), q = clamp(rint(x / s), -128, 127) -- and the cache entry is x' = fp16(q * s).
+ * kv is [rows, D] fp16 with D a multiple of 128; q is [rows, D]; scales is [rows, D / 128].
+ * ------------------------------------------------------------------------------------- */
+void wql_oracle_kv_quant_i8(const uint16_t* kv, int64_t rows, int D, int8_t* q, float* scales) {
+  const int groups = D / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int g = 0; g < groups; ++g) {
+      const uint16_t* x = kv + r * D + (int64_t)g * 128;
+      float amax = 0.0f;
+      for (int k = 0; k < 128; ++k) {
+        float a = fabsf(wql_oracle_half_to_float(x[k]));
+        if (a > amax) amax = a;
+      }
+      float s = amax / 127.0f;
+      if (amax == 0.0f) s = 1.0f;
+      scales[r * groups + g] = s;
+      for (int k = 0; k < 128; ++k)
+        q[r * D + (int64_t)g * 128 + k] = (int8_t)clamp_rint(wql_oracle_half_to_float(x[k]) / s, -128.0f, 127.0f);
+    }
+}
+
+void wql_oracle_kv_dequant_i8(const int8_t* q, const float* scales, int64_t rows, int D, uint16_t* out) {
+  const int groups = D / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int k = 0; k < D; ++k) {
+      float v = (float)q[r * D + k] * scales[r * groups + k / 128];
+      out[r * D + k] = wql_oracle_float_to_half(v);
     }
 }
 

@@ -587,3 +587,53 @@ def test_fp8_epilogue_terms():
     assert np.allclose(both - base, bias.astype(np.float64)[None, :] + res.astype(np.float64), rtol=0, atol=1e-9)
     only_b = oracle.fp8_epilogue_f64(acc, xs, ws, bias=bias)
     assert np.allclose(only_b - base, np.broadcast_to(bias.astype(np.float64), (3, 8)), rtol=0, atol=1e-9)
+
+
+# ------------------------------------------------------------------------------------------------
+# KV-cache int8, groups of 128 channels
+# ------------------------------------------------------------------------------------------------
+
+def test_kv_quant_recovers_exactly_representable_groups():
+    # every group is c * 2^-7 with integer codes c in [-127, 127] and |c| = 127 present: the scale is
+    # 127 * 2^-7 / 127 = 2^-7 exactly, so the codes come back as c and the cache entry as x itself
+    rng = np.random.default_rng(50)
+    rows, D = 6, 512
+    c = rng.integers(-127, 128, size=(rows, D))
+    for g in range(D // 128):
+        c[:, 128 * g + (g * 7) % 128] = np.where(np.arange(rows) % 2 == 0, 127, -127)
+    x = (c * 2.0 ** -7).astype(np.float16)
+    q, s = oracle.kv_quant_i8(x)
+    assert np.all(s == np.float32(2.0 ** -7))
+    assert np.array_equal(q.astype(np.int64), c)
+    assert np.array_equal(oracle.kv_dequant_i8(q, s).view(np.uint16), x.view(np.uint16))
+
+
+def test_kv_quant_groups_bounds_and_zero_group():
+    rng = np.random.default_rng(51)
+    rows, D = 40, 1024
+    x = (rng.standard_normal((rows, D)) * rng.uniform(0.01, 50, size=(rows, 1))).astype(np.float16)
+    x[3, 256:384] = 0  # one all-zero group
+    x[7, 128:256] *= np.float16(0.001)  # a small group next to large ones
+    q, s = oracle.kv_quant_i8(x)
+    assert q.shape == (rows, D) and s.shape == (rows, D // 128)
+    xf = x.astype(np.float32)
+    for g in range(D // 128):
+        amax = np.abs(xf[:, 128 * g:128 * (g + 1)]).max(axis=1)
+        want = np.where(amax == 0, np.float32(1.0), amax / np.float32(127.0)).astype(np.float32)
+        assert np.array_equal(s[:, g].view(np.uint32), want.view(np.uint32)), g  # each group's own absmax
+        qg = q[:, 128 * g:128 * (g + 1)].astype(np.int64)
+        nz = amax > 0
+        assert np.all(np.abs(qg[nz]).max(axis=1) == 127)  # the group's absmax lands on 127
+        err = np.abs(qg * s[:, g:g + 1].astype(np.float64) - xf[:, 128 * g:128 * (g + 1)])
+        assert np.all(err <= s[:, g:g + 1] * (0.5 + 1e-5))  # round to nearest: half a step
+    assert s[3, 2] == 1.0 and np.all(q[3, 256:384] == 0)
+
+
+def test_kv_dequant_is_one_fp16_rounding_of_the_fp32_product():
+    rng = np.random.default_rng(52)
+    q = rng.integers(-128, 128, size=(9, 384)).astype(np.int8)
+    s = rng.uniform(1e-6, 10, size=(9, 3)).astype(np.float32)
+    s[0, 0] = 1e-9  # products in the fp16 subnormal range
+    out = oracle.kv_dequant_i8(q, s)
+    prod = q.astype(np.float32) * np.repeat(s, 128, axis=1)  # the fp32 product, rounded once (IEEE)
+    assert np.array_equal(out.view(np.uint16), prod.astype(np.float16).view(np.uint16))  # numpy's rounding
