@@ -648,6 +648,18 @@ def run_sweep(args):
         W = weight(4096, 11008, False)
         sec = timed(lambda: wql.per_channel_quant_i8(W), 1, 10)
         emit("a5_per_channel_quant_i8", "K4096N11008", sec, 4096 * 11008 * 5 + 11008 * 4, 0, "hbm")
+    # f4 KV cache int8 in groups of 128: Llama-7B K and V rows (2 x 32 heads x 128 channels) of
+    # 16384 tokens, 256 MB of fp16, larger than L2
+    if want("f4"):
+        nkv, D = 16384, 8192
+        kv = torch.from_numpy(inputs.activations(nkv, D, seed=4)).to(dev)
+        qk, sk = wql.kv_quant_i8(kv)
+        out16 = torch.empty_like(kv)
+        sec = timed(lambda: wql.kv_quant_i8(kv, q=qk, scales=sk), 1, 20)
+        emit("f4_kv_quant_i8", f"rows{nkv}D{D}", sec, 3 * nkv * D + 4 * nkv * (D // 128), 0, "hbm")
+        sec = timed(lambda: wql.kv_dequant_i8(qk, sk, out=out16), 1, 20)
+        emit("f4_kv_dequant_i8", f"rows{nkv}D{D}", sec, 3 * nkv * D + 4 * nkv * (D // 128), 0, "hbm")
+        del kv, qk, sk, out16
     if want("f2"):
         W = weight(4096, 11008, False)
         sec = timed(lambda: wql.per_channel_quant_fp8(W), 1, 10)

@@ -17,7 +17,8 @@
  *   [W8A8] "LMDeploy W8A8 quantisation guide": weight smoothing (smooth_ln_fcs, alpha 0.5),
  *          QRMSNorm / QLinear modules, per_token_quant_int8 (scale = absmax / 127),
  *          per_channel_quant (fp32 scale per output channel), matmul_kernel_dynamic_quant
- *          (int32 accumulator, c = c * rms_scale * linear_scale).
+ *          (int32 accumulator, c = c * rms_scale * linear_scale), and its fp8 variant.
+ *   [FastLLM] "FastLLM architecture" article, section 5.2: KV cache int8 in groups of 128.
  *
  * Conventions for every entry point:
  *   - Matrices are row-major and dense (no strides).  K = input features, N = output
@@ -250,6 +251,23 @@ wql_status wql_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, 
 wql_status wql_w8a8_gemm_fp8(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws,
                              const uint16_t* bias, const uint16_t* residual, int M, int K, int N,
                              uint16_t* y, float* acc_out, void* stream);
+
+/* ========================================================================================
+ * KV cache int8 in groups of 128 ([FastLLM] section 5.2: the K and V cache stored as int8 with
+ * group size 128, dequantised when read).  The page fixes the width and the group size only.
+ * Reading: a group is 128 consecutive channels of one row (one token's K or V vector),
+ * symmetric like [W8A8]'s per-token int8:
+ *     scales[r, g] = max_{k in group g} |kv[r, k]| / 127      (fp32; 1.0 for an all-zero group)
+ *     q[r, k]      = clamp(round_half_even(kv[r, k] / scales[r, k / 128]), -128, 127)
+ * and the cache entry read back is out[r, k] = fp16(float(q[r, k]) * scales[r, k / 128]).
+ * kv and out are [rows, D] fp16, q is [rows, D] int8, scales [rows, D / 128] fp32, all row-major
+ * and contiguous (rows may count tokens x layers; a row is any run of D channels).
+ * Requires D % 128 == 0, rows >= 0 (0 is a no-op); pointers 16-byte aligned (scales: 4-byte).
+ * ======================================================================================== */
+wql_status wql_kv_quant_i8(const uint16_t* kv, int64_t rows, int D, int8_t* q, float* scales,
+                           void* stream);
+wql_status wql_kv_dequant_i8(const int8_t* q, const float* scales, int64_t rows, int D,
+                             uint16_t* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -45,6 +45,8 @@ SIGNATURES = {
     "wql_add_qrmsnorm_quant_fp8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
     "wql_per_channel_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "wql_w8a8_gemm_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "wql_kv_quant_i8": (_I, [_P, ctypes.c_int64, _I, _P, _P, _P]),
+    "wql_kv_dequant_i8": (_I, [_P, _P, ctypes.c_int64, _I, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -397,4 +399,34 @@ def w8a8_gemm_fp8(q: torch.Tensor, xs: torch.Tensor, qw: torch.Tensor, ws: torch
         _need(acc_out, "acc_out", torch.float32, (M, N))
     _check(load().wql_w8a8_gemm_fp8(_ptr(q), _ptr(xs), _ptr(qw), _ptr(ws), _ptr(bias), _ptr(residual), M, K, N,
                                     _ptr(out), _ptr(acc_out), _stream(q.device)), "wql_w8a8_gemm_fp8")
+    return out
+
+
+# ---- KV cache int8, groups of 128 channels ------------------------------------------------------
+
+def kv_quant_i8(kv: torch.Tensor, q: torch.Tensor | None = None, scales: torch.Tensor | None = None):
+    """kv [..., D] fp16 (D % 128 == 0) -> (q int8 [..., D], scales fp32 [..., D / 128]); s = absmax / 127."""
+    D = kv.shape[-1]
+    rows = kv.numel() // D if D else 0
+    _need(kv, "kv", torch.float16, tuple(kv.shape))
+    if q is None:
+        q = torch.empty(kv.shape, dtype=torch.int8, device=kv.device)
+    if scales is None:
+        scales = torch.empty(tuple(kv.shape[:-1]) + (D // 128,), dtype=torch.float32, device=kv.device)
+    _need(q, "q", torch.int8, tuple(kv.shape))
+    _need(scales, "scales", torch.float32, tuple(kv.shape[:-1]) + (D // 128,))
+    _check(load().wql_kv_quant_i8(_ptr(kv), rows, D, _ptr(q), _ptr(scales), _stream(kv.device)), "wql_kv_quant_i8")
+    return q, scales
+
+
+def kv_dequant_i8(q: torch.Tensor, scales: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp16 [..., D] = fp16(q * the scale of the element's group of 128)."""
+    D = q.shape[-1]
+    rows = q.numel() // D if D else 0
+    _need(q, "q", torch.int8, tuple(q.shape))
+    _need(scales, "scales", torch.float32, tuple(q.shape[:-1]) + (D // 128,))
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float16, device=q.device)
+    _need(out, "out", torch.float16, tuple(q.shape))
+    _check(load().wql_kv_dequant_i8(_ptr(q), _ptr(scales), rows, D, _ptr(out), _stream(q.device)), "wql_kv_dequant_i8")
     return out

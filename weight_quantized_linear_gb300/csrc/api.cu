@@ -365,4 +365,34 @@ wql_status wql_per_channel_quant_fp8(const float* w, int K, int N, uint8_t* qw, 
                      "wql_per_channel_quant_fp8");
 }
 
+wql_status wql_kv_quant_i8(const uint16_t* kv, int64_t rows, int D, int8_t* q, float* scales, void* stream) {
+  WQL_REQUIRE(D >= 128 && D % 128 == 0, "D must be a positive multiple of 128");
+  WQL_REQUIRE(rows >= 0, "rows must be >= 0");
+  if (rows == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(kv);
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE(scales != nullptr && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0,
+              "scales must be a 4-byte aligned device pointer");
+  return cuda_status(wql::launch_kv_quant_i8(kv, rows, D, q, scales, static_cast<cudaStream_t>(stream)),
+                     "wql_kv_quant_i8");
+}
+
+wql_status wql_kv_dequant_i8(const int8_t* q, const float* scales, int64_t rows, int D, uint16_t* out, void* stream) {
+  WQL_REQUIRE(D >= 128 && D % 128 == 0, "D must be a positive multiple of 128");
+  WQL_REQUIRE(rows >= 0, "rows must be >= 0");
+  if (rows == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE_PTR(out);
+  WQL_REQUIRE(scales != nullptr && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0,
+              "scales must be a 4-byte aligned device pointer");
+  return cuda_status(wql::launch_kv_dequant_i8(q, scales, rows, D, out, static_cast<cudaStream_t>(stream)),
+                     "wql_kv_dequant_i8");
+}
+
 }  // extern "C"

@@ -300,6 +300,36 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// int8 codes of per-row / per-group symmetric quantisation (s = absmax / 127)
+// ---------------------------------------------------------------------------------------------
+
+// Round to the nearest integer (ties to even) and saturate to [-128, 127], in one conversion.
+__device__ __forceinline__ int cvt_rni_sat_s8(float f) {
+  int r;
+  asm("{\n .reg .s8 t;\n cvt.rni.sat.s8.f32 t, %1;\n cvt.s32.s8 %0, t;\n}" : "=r"(r) : "f"(f));
+  return r;
+}
+
+// clamp(round_half_even(fl(y / s)), -128, 127), without a division in the common case.
+// t = fl(y * inv) with inv = fl(1 / s) lies within 2.3e-5 of fl(y / s) when |y / s| <= 127.5
+// (two roundings of relative size 2^-24 each, plus fl(y / s)'s own half ulp), so whenever t is
+// more than 5e-5 from a half-integer (|t - rint(t)| < 0.49995), both round to the same integer.
+// quant_fast returns rint(t) saturated and sets `exact` when that is not guaranteed; quant_exact
+// then divides.
+__device__ __forceinline__ int quant_fast(float y, float inv, bool& exact) {
+  const float t = __fmul_rn(y, inv);
+  const float rt = rintf(t);
+  exact |= !(fabsf(__fsub_rn(t, rt)) < 0.49995f);
+  return cvt_rni_sat_s8(rt);
+}
+__device__ __forceinline__ int quant_exact(float y, float s, float inv) {
+  const float t = __fmul_rn(y, inv);
+  const float rt = rintf(t);
+  if (fabsf(__fsub_rn(t, rt)) < 0.49995f) return cvt_rni_sat_s8(rt);
+  return cvt_rni_sat_s8(__fdiv_rn(y, s));
+}
+
+// ---------------------------------------------------------------------------------------------
 // float8 e4m3 ("fn": finite only, largest value 448)
 // ---------------------------------------------------------------------------------------------
 

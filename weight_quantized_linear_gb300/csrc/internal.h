@@ -110,4 +110,9 @@ cudaError_t launch_fp8_decode(const uint8_t* q, const float* xs, const uint8_t* 
                               int N, uint16_t* y, float* acc_out, const uint16_t* bias, const uint16_t* residual,
                               unsigned* dev_err, cudaStream_t stream, std::string* err);
 
+// KV cache int8 in groups of 128 channels: kv [rows, D] fp16, D % 128 == 0.
+cudaError_t launch_kv_quant_i8(const uint16_t* kv, long long rows, int D, int8_t* q, float* scales, cudaStream_t s);
+cudaError_t launch_kv_dequant_i8(const int8_t* q, const float* scales, long long rows, int D, uint16_t* out,
+                                 cudaStream_t s);
+
 }  // namespace wql
