@@ -60,6 +60,7 @@ _SIGS = {
     "wql_oracle_per_channel_quant_fp8": (None, [_P, _I, _I, _P, _P]),
     "wql_oracle_fp8_acc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "wql_oracle_fp8_epilogue_f64": (None, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "wql_oracle_silu_mul_f64": (None, [_P, _I64, _I, _P]),
     "wql_oracle_kv_quant_i8": (None, [_P, _I64, _I, _P, _P]),
     "wql_oracle_kv_dequant_i8": (None, [_P, _P, _I64, _I, _P]),
 }
@@ -368,6 +369,18 @@ def fp8_epilogue_f64(acc, xs, ws, bias=None, residual=None) -> np.ndarray:
     _load().wql_oracle_fp8_epilogue_f64(_ptr(acc), _ptr(_c(xs, np.float32)), _ptr(_c(ws, np.float32)),
                                         None if b is None else _ptr(b), None if r is None else _ptr(r), R, N, _ptr(y))
     return y
+
+
+# ---- fused gate/up: SiLU(gate) * up ------------------------------------------------------------
+
+def silu_mul_f64(y) -> np.ndarray:
+    """y [R, N] fp64 with gate j at column 2j and up j at 2j + 1 -> silu(gate) * up, [R, N / 2] fp64."""
+    y = _c(y, np.float64)
+    R, N = y.shape
+    assert N % 2 == 0
+    out = np.empty((R, N // 2), np.float64)
+    _load().wql_oracle_silu_mul_f64(_ptr(y), R, N, _ptr(out))
+    return out
 
 
 # ---- KV-cache int8, groups of 128 ------------------------------------------------------------

@@ -21,8 +21,8 @@
  *          matmul_kernel_dynamic_quant: int32 accumulator, c = c * rms_scale * linear_scale),
  *          and its fp8 variant (quant_dtype fp8 = float8_e4m3fn, Q_MAX from torch.finfo, values
  *          cast instead of rounded to integers, fp32 accumulator).
- *   [FastLLM] "FastLLM architecture" article, section 5.2 (KV cache quantised to int8 in groups of
- *          128, dequantised when read).
+ *   [FastLLM] "FastLLM architecture" article, section 2 (fused gate/up GEMM followed by SiLU * up)
+ *          and section 5.2 (KV cache quantised to int8 in groups of 128, dequantised when read).
  *
  * Readings taken where the pages are silent (each one is listed in the design notes):
  *   - zero point is an integer z in [0,15] stored 8 per uint32 like the codes; w ~ (q - z) * s;
@@ -550,6 +550,22 @@ void wql_oracle_fp8_epilogue_f64(const double* acc, const float* xs, const float
       if (bias) u += (double)wql_oracle_half_to_float(bias[n]);
       if (residual) u += (double)wql_oracle_half_to_float(residual[(size_t)i * N + n]);
       y[(size_t)i * N + n] = u;
+    }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * [FastLLM] section 2: the gate and up projections of an MLP run as one fused GEMM, followed by
+ * SiLU(gate) * up.  Reading: the fused weight interleaves the two projections by output channel
+ * (channel 2j = gate j, channel 2j + 1 = up j), and out[r, j] = silu(y[r, 2j]) * y[r, 2j + 1] with
+ * silu(g) = g / (1 + exp(-g)).  Here in fp64 on the fp64 GEMM output, without rounding (the
+ * reference the fused kernel is compared with, within the W4A16 tolerance).
+ * ------------------------------------------------------------------------------------- */
+void wql_oracle_silu_mul_f64(const double* y, int64_t rows, int N, double* out) {
+  const int J = N / 2;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int j = 0; j < J; ++j) {
+      const double g = y[r * N + 2 * j], u = y[r * N + 2 * j + 1];
+      out[r * J + j] = g / (1.0 + exp(-g)) * u;
     }
 }
 

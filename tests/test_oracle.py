@@ -637,3 +637,30 @@ def test_kv_dequant_is_one_fp16_rounding_of_the_fp32_product():
     out = oracle.kv_dequant_i8(q, s)
     prod = q.astype(np.float32) * np.repeat(s, 128, axis=1)  # the fp32 product, rounded once (IEEE)
     assert np.array_equal(out.view(np.uint16), prod.astype(np.float16).view(np.uint16))  # numpy's rounding
+
+
+# ------------------------------------------------------------------------------------------------
+# fused gate/up activation: SiLU(gate) * up on interleaved channels
+# ------------------------------------------------------------------------------------------------
+
+def test_silu_mul_against_scipy_and_closed_forms():
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(60)
+    y = rng.standard_normal((5, 64)) * 6
+    y[0, 0], y[0, 2], y[0, 4] = 0.0, 800.0, -800.0  # silu(0) = 0; silu(x) -> x and -> 0 far out
+    out = oracle.silu_mul_f64(y)
+    g, u = y[:, 0::2], y[:, 1::2]
+    ref = g * special.expit(g) * u  # silu(g) = g * sigmoid(g), scipy's logistic
+    assert np.allclose(out, ref, rtol=1e-14, atol=0)
+    assert out[0, 0] == 0.0
+    assert out[0, 1] == pytest.approx(800.0 * y[0, 3], rel=1e-15)
+    assert abs(out[0, 2]) < 1e-300
+    # the pairing: gate j is column 2j, up j is column 2j + 1 (swapping them changes the result)
+    sw = y.copy()
+    sw[:, 0::2], sw[:, 1::2] = y[:, 1::2], y[:, 0::2]
+    assert not np.allclose(oracle.silu_mul_f64(sw), out)
+    # silu(-x) = silu(x) - x
+    x = rng.standard_normal(32) * 3
+    pos = oracle.silu_mul_f64(np.stack([x, np.ones_like(x)], axis=1).reshape(1, -1))[0]
+    neg = oracle.silu_mul_f64(np.stack([-x, np.ones_like(x)], axis=1).reshape(1, -1))[0]
+    assert np.allclose(neg, pos - x, rtol=0, atol=1e-12)
