@@ -648,6 +648,38 @@ def run_sweep(args):
         W = weight(4096, 11008, False)
         sec = timed(lambda: wql.per_channel_quant_i8(W), 1, 10)
         emit("a5_per_channel_quant_i8", "K4096N11008", sec, 4096 * 11008 * 5 + 11008 * 4, 0, "hbm")
+    # f3 fused gate/up projection with SiLU(gate) * up in the epilogue (Llama-7B gate_up: K = 4096,
+    # N = 2 x 11008 interleaved, G = 128), against the plain GEMM of the same weight
+    if want("f3"):
+        K, N, G = 4096, 22016, 128
+        qw, s3, qz = wql.awq_pack(weight(K, N, True), G)
+        per = w4a16_bytes(0, K, N, G)
+        copies = int(max(2, min(64, -(-3 * l2 // per))))
+        stack = [(qw, s3, qz)] + [(qw.clone(), s3.clone(), qz.clone()) for _ in range(copies - 1)]
+        for M in (1, 8, 32, 128, 256, 2048):
+            x = torch.from_numpy(inputs.activations(M, K, seed=0)).to(dev)
+            y2 = torch.empty((M, N), dtype=torch.float16, device=dev)
+            y1 = torch.empty((M, N // 2), dtype=torch.float16, device=dev)
+
+            def plain(stack=stack, x=x, y=y2):
+                for (a, b, z) in stack:
+                    wql.w4a16_gemm(x, a, b, z, G, out=y)
+
+            def fused(stack=stack, x=x, y=y1):
+                for (a, b, z) in stack:
+                    wql.w4a16_gemm_silu_mul(x, a, b, z, G, out=y)
+
+            flops = gemm_flops(M, K, N)
+            reps = 20 if flops * copies < 5e12 else 3
+            tp = timed(plain, copies, reps)
+            tf = timed(fused, copies, reps)
+            nbytes = w4a16_bytes(M, K, N, G) - M * N  # y is [M, N / 2]
+            bound = "tensor" if flops / (bf16 * 1e12) > nbytes / (hbm * 1e9) else "hbm"
+            emit("f3_w4a16_gate_up_silu", f"M{M}K{K}N{N}G{G}", tf, nbytes, flops, bound,
+                 {"plain_gemm_us": round(tp * 1e6, 3), "kernel": wql.w4a16_kernel_for(M, K, N)})
+            del x, y1, y2
+        del stack, qw, s3, qz
+
     # f4 KV cache int8 in groups of 128: Llama-7B K and V rows (2 x 32 heads x 128 channels) of
     # 16384 tokens, 256 MB of fp16, larger than L2
     if want("f4"):

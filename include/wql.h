@@ -97,6 +97,21 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
                           void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * w4a16_gemm_silu_mul  [FastLLM] section 2: the gate and up projections of an MLP as one GEMM,
+ * with SiLU(gate) * up fused into its epilogue.  Reading: the packed weight (wql_awq_pack of a
+ * [K, N] matrix) interleaves the projections by output channel -- channel 2j is gate j and
+ * channel 2j + 1 is up j -- and
+ *     y[m, j] = fp16(silu(g) * u),  g = fp16(gemm[m, 2j]),  u = fp16(gemm[m, 2j + 1]),
+ *     silu(g) = g / (1 + exp(-g))   (fp32; IEEE division, expf)
+ * i.e. exactly the unfused GEMM's fp16 outputs followed by the activation, without writing them.
+ * x [M, K] fp16; y [M, N / 2] fp16.  Same kernels and requirements as wql_w4a16_gemm, and
+ * N % 64 == 0.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_w4a16_gemm_silu_mul(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                                   const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                   void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * w4a16_kernel_for: the kernel wql_w4a16_gemm runs for an M x K x N call on the current
  * device: 0 = the weight-streaming decode kernel, 1 = the tcgen05 tensor-core kernel.  Up to
  * 16 tokens it is always 0 and from 33 on always 1; in between it depends on N and K.

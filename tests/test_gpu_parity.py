@@ -323,3 +323,34 @@ def test_w8a8_decode_back_to_back_stress(wql):
     wql.device_status()
     for y in ys:
         assert torch.equal(y, ref)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_split_k_repeatable_at_many_strips(wql, M):
+    """N = 22016 gives 172 strips and a 3-way cluster split-K: every call must give the same bits.
+    (Before the consumers fenced their generic-proxy reads of a stage ahead of its TMA refill, 1-4 %
+    of such calls came out with one column group's partial sums computed from a refilled stage.)"""
+    K, N, G = 4096, 22016, 128
+    W = inputs.weight(K, N, seed=M + N, outliers=True)
+    x = dev(inputs.activations(M, K, seed=M + N, outlier_channels=True))
+    qw, s, qz = wql.awq_pack(dev(W), G)
+    ref = wql.w4a16_gemm(x, qw, s, qz, G).clone()
+    y = torch.empty_like(ref)
+    bad = 0
+    for _ in range(300):
+        wql.w4a16_gemm(x, qw, s, qz, G, out=y)
+        bad += int(not torch.equal(y, ref))
+    assert bad == 0, f"{bad} of 300 calls differ"
+    rng = np.random.default_rng(M)
+    q = dev(rng.integers(-128, 128, size=(M, K), dtype=np.int8))
+    xs = dev(rng.uniform(1e-3, 1e-2, M).astype(np.float32))
+    qW = dev(rng.integers(-127, 128, size=(N, K), dtype=np.int8))
+    ws = dev(rng.uniform(1e-4, 1e-3, N).astype(np.float32))
+    ref8 = wql.w8a8_gemm(q, xs, qW, ws).clone()
+    y8 = torch.empty_like(ref8)
+    bad8 = 0
+    for _ in range(300):
+        wql.w8a8_gemm(q, xs, qW, ws, out=y8)
+        bad8 += int(not torch.equal(y8, ref8))
+    assert bad8 == 0, f"{bad8} of 300 int8 calls differ"
+    wql.device_status()

@@ -32,6 +32,7 @@ SIGNATURES = {
     "wql_awq_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),
+    "wql_w4a16_gemm_silu_mul": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_add_qrmsnorm_quant_i8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
     "wql_w8a8_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -142,6 +143,32 @@ def w4a16_gemm(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, qze
     _check(load().wql_w4a16_gemm(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(qzeros), M, K, N, group, _ptr(out),
                                  _stream(x.device)), "wql_w4a16_gemm")
     return out
+
+
+def w4a16_gemm_silu_mul(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor,
+                        group: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused gate/up projection: the packed weight has N = 2I channels with gate j at channel 2j and
+    up j at 2j + 1; returns y [M, I] fp16 = fp16(silu(g) * u) of the GEMM's fp16 gate and up."""
+    M, K = x.shape
+    N = qweight.shape[1] * 8
+    _need(x, "x", torch.float16, (M, K))
+    _need(qweight, "qweight", torch.int32, (K, N // 8))
+    _need(scales, "scales", torch.float16, (K // group, N))
+    _need(qzeros, "qzeros", torch.int32, (K // group, N // 8))
+    if out is None:
+        out = torch.empty((M, N // 2), dtype=torch.float16, device=x.device)
+    _need(out, "out", torch.float16, (M, N // 2))
+    _check(load().wql_w4a16_gemm_silu_mul(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(qzeros), M, K, N, group,
+                                          _ptr(out), _stream(x.device)), "wql_w4a16_gemm_silu_mul")
+    return out
+
+
+def interleave_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor:
+    """[K, I] gate and up weights -> the [K, 2I] fused weight that w4a16_gemm_silu_mul expects
+    (column 2j = gate j, column 2j + 1 = up j); pack it with awq_pack."""
+    if w_gate.shape != w_up.shape or w_gate.dim() != 2:
+        raise ValueError("gate and up weights must both be [K, I]")
+    return torch.stack([w_gate, w_up], dim=2).reshape(w_gate.shape[0], 2 * w_gate.shape[1]).contiguous()
 
 
 # ---------------------------------------------------------------------------------------------

@@ -113,11 +113,15 @@ wql_status wql_awq_pack(const float* w, int K, int N, int group, uint32_t* qweig
                      "wql_awq_pack");
 }
 
-wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
-                          const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, void* stream) {
+namespace {
+
+// wql_w4a16_gemm and wql_w4a16_gemm_silu_mul: one validation and dispatch path.
+wql_status w4a16_gemm(const char* fn, const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                      const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act, void* stream) {
   WQL_REQUIRE(valid_group(group), "group must be 32, 64 or 128");
   WQL_REQUIRE(K >= group && K % group == 0, "K must be a positive multiple of the group size");
   WQL_REQUIRE(N >= 32 && N % 32 == 0, "N must be a positive multiple of 32");
+  WQL_REQUIRE(!act || N % 64 == 0, "N must be a multiple of 64 for the gate/up activation");
   WQL_REQUIRE(M >= 0, "M must be >= 0");
   if (M == 0) {
     g_last_error.clear();
@@ -134,12 +138,25 @@ wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint
   const bool prefill = force && strcmp(force, "decode") == 0   ? false
                        : force && strcmp(force, "prefill") == 0 ? true
                                                                 : wql::w4a16_use_prefill(M, K, N);
-  cudaError_t e = prefill ? wql::launch_w4a16_prefill(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
+  cudaError_t e = prefill ? wql::launch_w4a16_prefill(x, qweight, scales, qzeros, M, K, N, group, y, act, dev_err,
                                                       static_cast<cudaStream_t>(stream), &err)
-                          : wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, dev_err,
+                          : wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, act, dev_err,
                                                      static_cast<cudaStream_t>(stream), &err);
-  if (!err.empty()) return fail(WQL_ECUDA, "wql_w4a16_gemm: " + err);
-  return cuda_status(e, "wql_w4a16_gemm");
+  if (!err.empty()) return fail(WQL_ECUDA, std::string(fn) + ": " + err);
+  return cuda_status(e, fn);
+}
+
+}  // namespace
+
+wql_status wql_w4a16_gemm(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                          const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, void* stream) {
+  return w4a16_gemm("wql_w4a16_gemm", x, qweight, scales, qzeros, M, K, N, group, y, 0, stream);
+}
+
+wql_status wql_w4a16_gemm_silu_mul(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
+                                   const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                   void* stream) {
+  return w4a16_gemm("wql_w4a16_gemm_silu_mul", x, qweight, scales, qzeros, M, K, N, group, y, 1, stream);
 }
 
 int wql_w4a16_kernel_for(int M, int K, int N) { return wql::w4a16_use_prefill(M, K, N) ? 1 : 0; }

@@ -375,6 +375,16 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint
       : "r"(v));
 }
 
+// The activation of a fused gate/up projection ("FastLLM architecture" article, section 2): from the
+// GEMM's fp32 gate and up values g and u of one output, fp16(silu(g16) * u16) with g16, u16 the fp16
+// outputs the unfused GEMM would have written and silu(g) = g / (1 + exp(-g)) in fp32 (IEEE
+// division; expf as the CUDA math library provides it).
+__device__ __forceinline__ __half silu_mul_h(float g, float u) {
+  const float g16 = __half2float(__float2half_rn(g)), u16 = __half2float(__float2half_rn(u));
+  const float sg = __fdiv_rn(g16, __fadd_rn(1.0f, expf(-g16)));
+  return __float2half_rn(__fmul_rn(sg, u16));
+}
+
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
 __device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(

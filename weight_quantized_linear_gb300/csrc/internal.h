@@ -39,12 +39,14 @@ int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int
 cudaError_t launch_awq_pack(const float* w, int K, int N, int group, uint32_t* qweight,
                             uint16_t* scales, uint32_t* qzeros, cudaStream_t s);
 
+// act = 0: y [M, N]; act = 1: the gate/up activation, y [M, N / 2] with y[m, j] =
+// fp16(silu(fp16(y2[m, 2j])) * fp16(y2[m, 2j + 1])) of the GEMM's output y2.
 cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
-                                const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,
                                 unsigned* dev_err, cudaStream_t s, std::string* err);
 
 cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
-                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,
                                  unsigned* dev_err, cudaStream_t s, std::string* err);
 
 // Token count from which w4a16_gemm always uses the tcgen05 kernel instead of the streaming decode

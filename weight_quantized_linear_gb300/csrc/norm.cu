@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) 
         }
       }
     }
+    // the slot was read through the generic proxy and thread 0 refills it with a bulk copy (async
+    // proxy) after the next barrier: a proxy fence orders the reads before that write
+    fence_proxy_async_smem();
     float ss;
     if (!row_sum_vote(p, ok, red, ss)) {
       if (tid == 0) report_error(err, kErrTimeoutFull);

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 128}, SW64
                         const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
-                        int M, int N, int kblocks, int x3d, __half* __restrict__ y, unsigned* err) {
+                        int M, int N, int kblocks, int x3d, __half* __restrict__ y, int act, unsigned* err) {
   using L = Layout<MT, LG>;
   constexpr int kLanes = L::kLanes;
   constexpr int kConsumerWarps = Warps<MT>::kConsumerWarps;
@@ -341,6 +341,12 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
               tot[j][mt][e] = fmaf(ca[cc], acc[j][mt][e], fmaf(-cb[cc], sx[mt][e & 1], tot[j][mt][e]));
             }
       }
+      // The stage was read through ordinary shared-memory loads (the generic proxy); TMA refills it
+      // through the async proxy once the producer sees this release.  An mbarrier release alone does
+      // not order generic-proxy reads before async-proxy writes: without this fence a refill could
+      // land while an earlier read was still being performed (seen as 1-4 % of back-to-back calls
+      // with wrong partial sums at N = 22016 under cluster split-K).
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -401,11 +407,16 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
       const int row = (4 * f) / kStripCols, col = (4 * f) % kStripCols;
       const int m = m0 + row, n = strip * kStripCols + col;
       if (m < M && n < N) {
-        __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&h01);
-        pk.y = *reinterpret_cast<uint32_t*>(&h23);
-        *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = pk;
+        if (act) {  // channels n, n + 1 and n + 2, n + 3 are (gate, up) pairs: outputs n / 2, n / 2 + 1
+          *reinterpret_cast<__half2*>(y + (size_t)m * (N / 2) + n / 2) =
+              __halves2half2(silu_mul_h(v.x, v.y), silu_mul_h(v.z, v.w));
+        } else {
+          __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&h01);
+          pk.y = *reinterpret_cast<uint32_t*>(&h23);
+          *reinterpret_cast<uint2*>(y + (size_t)m * N + n) = pk;
+        }
       }
     }
   }
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
 
 template <int MT, int LG>
 cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, const CUtensorMap& ts,
-                      const CUtensorMap& tz, int M, int N, int kblocks, __half* y, unsigned* dev_err,
+                      const CUtensorMap& tz, int M, int N, int kblocks, __half* y, int act, unsigned* dev_err,
                       cudaStream_t stream) {
   using L = Layout<MT, LG>;
   constexpr int kThreads = Warps<MT>::kThreads;
@@ -451,26 +462,27 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, kblocks, x3d, y, dev_err);
+  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, kblocks, x3d, y, act, dev_err);
 }
 
 template <int MT>
 cudaError_t launch_g(int group, const CUtensorMap& tx, int x3d, const CUtensorMap& tq, const CUtensorMap& ts,
-                     const CUtensorMap& tz, int M, int N, int kblocks, __half* y, unsigned* dev_err, cudaStream_t s) {
+                     const CUtensorMap& tz, int M, int N, int kblocks, __half* y, int act, unsigned* dev_err,
+                     cudaStream_t s) {
   switch (group) {
     case 32:
-      return launch_mt<MT, 5>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+      return launch_mt<MT, 5>(tx, x3d, tq, ts, tz, M, N, kblocks, y, act, dev_err, s);
     case 64:
-      return launch_mt<MT, 6>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+      return launch_mt<MT, 6>(tx, x3d, tq, ts, tz, M, N, kblocks, y, act, dev_err, s);
     default:
-      return launch_mt<MT, 7>(tx, x3d, tq, ts, tz, M, N, kblocks, y, dev_err, s);
+      return launch_mt<MT, 7>(tx, x3d, tq, ts, tz, M, N, kblocks, y, act, dev_err, s);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
-                                const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,
                                 unsigned* dev_err, cudaStream_t stream, std::string* err) {
   const int MT = M <= 8 ? 1 : 2;  // larger M runs as several 16-token blocks
   const int GR = group >= kBK ? 1 : kBK / group;
@@ -493,8 +505,8 @@ cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, cons
   }
   const int kblocks = (K + kBK - 1) / kBK;
   __half* yh = reinterpret_cast<__half*>(y);
-  if (MT == 1) return launch_g<1>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, dev_err, stream);
-  return launch_g<2>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, dev_err, stream);
+  if (MT == 1) return launch_g<1>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, act, dev_err, stream);
+  return launch_g<2>(group, tx, x3d, tq, ts, tz, M, N, kblocks, yh, act, dev_err, stream);
 }
 
 }  // namespace wql

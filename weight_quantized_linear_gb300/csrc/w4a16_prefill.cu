@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                      // 3D {N/8, K/4, 4} box {16, 32, 4}, SW64
                          const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                          const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
-                         int M, int N, int K, __half* __restrict__ y, unsigned* err) {
+                         int M, int N, int K, __half* __restrict__ y, int act, unsigned* err) {
   using L = PLayout<BN, LG>;
   constexpr int kStages = L::kStages, kBK = L::kBK;
   extern __shared__ uint8_t smem_raw[];
@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_16x256b_x4(taddr1 + stage * 64, r1);
         tmem_st_wait();
         tc_fence_before_sync();  // the stores are ordered before the MMA thread's wait on afull
+        // the packed tile was read through the generic proxy; its TMA refill (async proxy) follows
+        // this release, and only a proxy fence orders the two
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[stage]);
         if (++stage == kStages) {
@@ -410,6 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // shared memory, rows follow the chunk order n0 n4 n1 n5 ...
     const int col_in_tile = L::kTA ? 32 * (i >> 5) + 4 * (i & 7) + ((i >> 3) & 3)
                                    : 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);
+    // with the gate/up activation (act), channel pairs (2j, 2j + 1) meet in lanes differing in bit 3
+    // (A in TMEM) or bit 1 (A in shared memory); the lane of the even channel writes output j
+    const int pair_mask = L::kTA ? 8 : 2;
+    const int NO = act ? N / 2 : N;  // output row length
     grid_dependency_wait();  // y may still be read by the preceding kernel
     if (S == 1) {
       int it = 0;
@@ -429,7 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(taddr + cc, r);
           tmem_ld_wait();
           const int mbase = mt * BN + cc;
-          if (n < N) {
+          if (act) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float v = __uint_as_float(r[k]);
+              const float pv = __shfl_xor_sync(0xffffffffu, v, pair_mask);
+              if (n < N && (n & 1) == 0 && mbase + k < M) y[(size_t)(mbase + k) * NO + n / 2] = silu_mul_h(v, pv);
+            }
+          } else if (n < N) {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               if (mbase + k < M) y[(size_t)(mbase + k) * N + n] = __float2half_rn(__uint_as_float(r[k]));
@@ -469,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       cluster_phase();  // (2) every partial has landed in its owner's receive buffer
       const int n = nt * kBM + col_in_tile;
-      if (n < N) {
+      if (act || n < N) {  // (with act every lane takes part in the pair shuffles)
 #pragma unroll 1
         for (int cl = 0; cl < CW; cl += 4) {
           float4 acc = lds_f4(recv + (uint32_t)((i * rstride + cl) * 4));
@@ -482,9 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int m = mt * BN + split * CW + cl;
           const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+          if (act) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
+            for (int e = 0; e < 4; ++e) {
+              const float pv = __shfl_xor_sync(0xffffffffu, v[e], pair_mask);
+              if (n < N && (n & 1) == 0 && m + e < M) y[(size_t)(m + e) * NO + n / 2] = silu_mul_h(v[e], pv);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
+          }
         }
       }
     }
@@ -503,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int LG>
 cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
-                     int M, int N, int K, __half* y, unsigned* dev_err, cudaStream_t stream) {
+                     int M, int N, int K, __half* y, int act, unsigned* dev_err, cudaStream_t stream) {
   using L = PLayout<BN, LG>;
   auto kern = w4a16_prefill_kernel<BN, LG>;
   static bool attr_set[64] = {false};
@@ -538,26 +560,27 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = S == 1 ? 1 : 2;
-  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, K, y, dev_err);
+  return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, K, y, act, dev_err);
 }
 
 template <int BN>
 cudaError_t launch_pg(int group, const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts,
-                      const CUtensorMap& tz, int M, int N, int K, __half* y, unsigned* dev_err, cudaStream_t s) {
+                      const CUtensorMap& tz, int M, int N, int K, __half* y, int act, unsigned* dev_err,
+                      cudaStream_t s) {
   switch (group) {
     case 32:
-      return launch_p<BN, 5>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+      return launch_p<BN, 5>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
     case 64:
-      return launch_p<BN, 6>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+      return launch_p<BN, 6>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
     default:
-      return launch_p<BN, 7>(tx, tq, ts, tz, M, N, K, y, dev_err, s);
+      return launch_p<BN, 7>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
-                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y,
+                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,
                                  unsigned* dev_err, cudaStream_t stream, std::string* err) {
   // Token tile: the smallest of 32 / 64 / 128 that holds M; beyond that 256, except up to M = 512
   // where 128-token tiles still fit one wave on the SMs, or where M would leave a 256-tile mostly
@@ -582,10 +605,10 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
     return cudaErrorInvalidValue;
   }
   __half* yh = reinterpret_cast<__half*>(y);
-  if (BN == 32) return launch_pg<32>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
-  if (BN == 64) return launch_pg<64>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
-  if (BN == 128) return launch_pg<128>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
-  return launch_pg<256>(group, tx, tq, ts, tz, M, N, K, yh, dev_err, stream);
+  if (BN == 32) return launch_pg<32>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 64) return launch_pg<64>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 128) return launch_pg<128>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  return launch_pg<256>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
 }
 
 }  // namespace wql

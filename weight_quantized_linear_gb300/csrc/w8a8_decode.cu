@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1)
           for (int mt = 0; mt < MT; ++mt) mma_f16_16816(acc[a][mt], A, bx[mt][0], bx[mt][1]);
         }
       }
+      // generic-proxy reads of the stage are ordered before its TMA refill (async proxy) only by
+      // a proxy fence; the mbarrier release alone does not do it
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (!FP8 && (it + 1) % kFoldStages == 0) fold();

@@ -258,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_32x32b_x32(lane_addr + aslot * 64, a);
         tmem_st_wait();
         tc_fence_before_sync();
+        // the int8 tile was read through the generic proxy; its TMA refill (async proxy) follows this
+        // release, and only a proxy fence orders the two
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[aslot]);
         if (++stage == kStages) {
