@@ -414,7 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_in_tile = L::kTA ? 32 * (i >> 5) + 4 * (i & 7) + ((i >> 3) & 3)
                                    : 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);
     // with the gate/up activation (act), channel pairs (2j, 2j + 1) meet in lanes differing in bit 3
-    // (A in TMEM) or bit 1 (A in shared memory); the lane of the even channel writes output j
+    // (A in TMEM) or bit 1 (A in shared memory).  The two lanes of a pair split the tokens: for
+    // tokens k, k + 1 the even-channel lane computes output (k, j) from its gate and the partner's up,
+    // the odd-channel lane output (k + 1, j) from the partner's gate and its own up -- one shuffle
+    // carries both, and every lane evaluates the activation once per two tokens
     const int pair_mask = L::kTA ? 8 : 2;
     const int NO = act ? N / 2 : N;  // output row length
     grid_dependency_wait();  // y may still be read by the preceding kernel
@@ -437,11 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           const int mbase = mt * BN + cc;
           if (act) {
+            const bool even = (n & 1) == 0;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const float v = __uint_as_float(r[k]);
-              const float pv = __shfl_xor_sync(0xffffffffu, v, pair_mask);
-              if (n < N && (n & 1) == 0 && mbase + k < M) y[(size_t)(mbase + k) * NO + n / 2] = silu_mul_h(v, pv);
+            for (int k = 0; k < 32; k += 2) {
+              const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+              const float got = __shfl_xor_sync(0xffffffffu, even ? v1 : v0, pair_mask);
+              const int m = mbase + k + (even ? 0 : 1);
+              const __half o = silu_mul_h(even ? v0 : got, even ? got : v1);  // (gate, up)
+              if (n < N && m < M) y[(size_t)m * NO + n / 2] = o;
             }
           } else if (n < N) {
 #pragma unroll
@@ -497,10 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = mt * BN + split * CW + cl;
           const float v[4] = {acc.x, acc.y, acc.z, acc.w};
           if (act) {
+            const bool even = (n & 1) == 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float pv = __shfl_xor_sync(0xffffffffu, v[e], pair_mask);
-              if (n < N && (n & 1) == 0 && m + e < M) y[(size_t)(m + e) * NO + n / 2] = silu_mul_h(v[e], pv);
+            for (int e = 0; e < 4; e += 2) {
+              const float got = __shfl_xor_sync(0xffffffffu, even ? v[e + 1] : v[e], pair_mask);
+              const int mm = m + e + (even ? 0 : 1);
+              const __half o = silu_mul_h(even ? v[e] : got, even ? got : v[e + 1]);  // (gate, up)
+              if (n < N && mm < M) y[(size_t)mm * NO + n / 2] = o;
             }
           } else {
 #pragma unroll
