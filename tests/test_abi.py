@@ -64,6 +64,21 @@ def test_validation_rejects_bad_arguments_without_a_gpu(wql_lib):
     assert lib.wql_w8a8_gemm(None, None, None, None, 0, 4096, 4096, None, None, None, 0, None) == 0
     # K not a multiple of 16 for the int8 GEMM
     assert lib.wql_w8a8_gemm(fake, fake, fake, fake, 1, 4100, 4096, fake, None, None, 0, None) == 1
+    # the follow-up entry points validate the same way
+    assert lib.wql_w4a16_gemm_silu_mul(fake, fake, fake, fake, 1, 4096, 96, 128, fake, None) == 1  # N % 64
+    assert b"64" in lib.wql_last_error()
+    assert lib.wql_w8a8_gemm_fp8(fake, fake, fake, fake, None, None, 1, 4100, 4096, fake, None, None) == 1
+    assert lib.wql_w8a8_gemm_fp8(None, None, None, None, None, None, 0, 4096, 4096, None, None, None) == 0
+    bad_bias = ctypes.c_void_p((1 << 20) + 8)  # bias must be 16-byte aligned
+    assert lib.wql_w8a8_gemm_fused(fake, fake, fake, fake, bad_bias, None, 1, 4096, 4096, fake, None, None, 0,
+                                   None) == 1
+    assert lib.wql_kv_quant_i8(fake, 4, 192, fake, fake, None) == 1  # D % 128
+    assert lib.wql_kv_quant_i8(None, 0, 256, None, None, None) == 0
+    assert lib.wql_kv_dequant_i8(fake, fake, -1, 256, fake, None) == 1
+    assert lib.wql_qrmsnorm_quant_fp8(fake, fake, ctypes.c_float(1e-6), 1, 32768, fake, fake, None) == 2
+    assert lib.wql_add_qrmsnorm_quant_fp8(fake, None, fake, ctypes.c_float(1e-6), 1, 4096, fake, fake, fake,
+                                          None) == 1  # residual required
+    assert lib.wql_per_channel_quant_fp8(fake, 4096, 48, fake, fake, None) == 1  # N % 32
 
 
 def test_binding_raises_without_library(tmp_path):

@@ -7,8 +7,9 @@
 // Both kernels are streams over HBM: a half-warp owns a group (each lane 8 channels, one 16-byte
 // load), the group's absmax is a 4-step shuffle within the half-warp, and each lane writes its 8
 // codes as one 8-byte store (the half-warp's 128 codes are contiguous).  Persistent grid-stride
-// warps; each iteration a warp takes four groups (two per half-warp), so that every thread has two
-// loads in flight.
+// warps; each iteration a warp takes kKvGroupsPerHalf groups per half-warp, all loaded before any
+// is quantised, so that every thread keeps that many 16-byte loads in flight (2 -> 4 groups on
+// 16384 x 8192 fp16: 95 -> 91 us).
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,6 +17,7 @@ namespace wql {
 namespace {
 
 constexpr int kKvThreads = 256;
+constexpr int kKvGroupsPerHalf = 4;  // groups per half-warp per iteration
 
 // Eight fp16 (one uint4) widened to fp32.
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -61,21 +63,28 @@ __device__ __forceinline__ void quant_part(const uint4& raw, bool valid, long lo
   if (sub == 0) scales[g] = s;
 }
 
-// Groups are contiguous: group g covers kv elements [128 g, 128 g + 128).  Warp w takes groups
-// 4w .. 4w + 3, then 4(w + W) .., with half-warp h holding groups base + h and base + 2 + h.
+// Groups are contiguous: group g covers kv elements [128 g, 128 g + 128).  With P =
+// kKvGroupsPerHalf, warp w takes groups 2P w .. 2P w + 2P - 1, then 2P (w + W) .., half-warp h holding
+// groups base + h + 2t (t < P).
 __global__ void __launch_bounds__(kKvThreads) kv_quant_i8_kernel(const __half* __restrict__ kv, long long ngroups,
                                                                  int8_t* __restrict__ q, float* __restrict__ scales) {
+  constexpr int P = kKvGroupsPerHalf;
   const int lane = threadIdx.x & 31, sub = lane & 15, h = lane >> 4;
   const long long warp = ((long long)blockIdx.x * kKvThreads + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * kKvThreads) >> 5;
   const uint4* src = reinterpret_cast<const uint4*>(kv);
-  for (long long base = 4 * warp; base < ngroups; base += 4 * nwarps) {  // uniform over the warp
-    const long long ga = base + h, gb = base + 2 + h;
-    const bool va = ga < ngroups, vb = gb < ngroups;
-    const uint4 ra = va ? __ldcs(src + ga * 16 + sub) : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 rb = vb ? __ldcs(src + gb * 16 + sub) : make_uint4(0u, 0u, 0u, 0u);
-    quant_part(ra, va, ga, sub, q, scales);
-    quant_part(rb, vb, gb, sub, q, scales);
+  for (long long base = 2 * P * warp; base < ngroups; base += 2 * P * nwarps) {  // uniform over the warp
+    uint4 raw[P];
+#pragma unroll
+    for (int t = 0; t < P; ++t) {
+      const long long g = base + h + 2 * t;
+      raw[t] = g < ngroups ? __ldcs(src + g * 16 + sub) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int t = 0; t < P; ++t) {
+      const long long g = base + h + 2 * t;
+      quant_part(raw[t], g < ngroups, g, sub, q, scales);
+    }
   }
 }
 
@@ -111,7 +120,7 @@ int kv_grid(long long units_per_cta, long long units) {
 cudaError_t launch_kv_quant_i8(const uint16_t* kv, long long rows, int D, int8_t* q, float* scales, cudaStream_t s) {
   const long long ngroups = rows * (D / 128);
   if (ngroups == 0) return cudaSuccess;
-  kv_quant_i8_kernel<<<kv_grid(kKvThreads / 16 * 2, ngroups), kKvThreads, 0, s>>>(
+  kv_quant_i8_kernel<<<kv_grid(kKvThreads / 16 * kKvGroupsPerHalf, ngroups), kKvThreads, 0, s>>>(
       reinterpret_cast<const __half*>(kv), ngroups, q, scales);
   return cudaGetLastError();
 }
