@@ -41,7 +41,8 @@ struct FLayout {
   static constexpr int kWBytes = kBM * kBK;  // 128 channel rows x 128 B, 128-byte swizzle
   static constexpr int kXBytes = BN * kBK;   // BN token rows x 128 B
   static constexpr int kStage = kWBytes + kXBytes;
-  static constexpr int kStages = CTAS == 2 ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  static_assert(BN == 64 || BN == 128, "token tiles of 64 or 128");
+  static constexpr int kStages = CTAS == 2 ? 3 : (BN == 128 ? 6 : 8);  // 192 KB of stages with one CTA
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
   static constexpr int kBox = 32 * 32 * 2;                     // one 32 tokens x 32 channels fp16 box
   static constexpr int kBufs = CTAS == 2 ? 2 : 4;              // output boxes per epilogue warp
