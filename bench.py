@@ -708,8 +708,9 @@ def run_sweep(args):
 def run_profile_case(args):
     """A few calls of one operation on one shape, for a profiler to capture.
 
-    ``w4a16:M,K,N,G``, ``w8a8:M,K,N``, ``fp8:M,K,N``, ``norm:M,K``, ``normfp8:M,K`` or ``prep:K,N``
-    (awq_pack with G = 128, then per_channel_quant_i8).  Each operation is called ``--calls`` times on synthetic inputs.
+    ``w4a16:M,K,N,G``, ``w8a8:M,K,N[,1]``, ``fp8:M,K,N[,1]`` (``,1``: with bias and residual),
+    ``norm:M,K``, ``normfp8:M,K``, ``kv:rows,D`` (quantise then dequantise) or ``prep:K,N`` (awq_pack
+    with G = 128, then per_channel_quant_i8).  Each operation is called ``--calls`` times on synthetic inputs.
     """
     import numpy as np
     import torch
@@ -729,15 +730,26 @@ def run_profile_case(args):
         for _ in range(calls):
             wql.w4a16_gemm(x, qw, s, qz, G, out=y)
     elif op == "w8a8":
-        M, K, N = d
+        M, K, N = d[:3]
+        fused = len(d) > 3 and d[3] == 1  # w8a8:M,K,N,1 adds a bias and a residual in the epilogue
         rng = np.random.default_rng(0)
         q = torch.from_numpy(rng.integers(-128, 128, size=(M, K), dtype=np.int8)).to(dev)
         qW = torch.from_numpy(rng.integers(-127, 128, size=(N, K), dtype=np.int8)).to(dev)
         xs = torch.full((M,), 0.01, device=dev)
         ws = torch.full((N,), 0.001, device=dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        bias = torch.zeros((N,), dtype=torch.float16, device=dev) if fused else None
+        res = torch.ones((M, N), dtype=torch.float16, device=dev) if fused else None
         for _ in range(calls):
-            wql.w8a8_gemm(q, xs, qW, ws, out=y)
+            wql.w8a8_gemm_fused(q, xs, qW, ws, bias, res, out=y)
+    elif op == "kv":
+        R, D = d
+        kv = torch.from_numpy(inputs.activations(R, D, seed=4)).to(dev)
+        qk, sk = wql.kv_quant_i8(kv)
+        out = torch.empty_like(kv)
+        for _ in range(calls):
+            wql.kv_quant_i8(kv, q=qk, scales=sk)
+            wql.kv_dequant_i8(qk, sk, out=out)
     elif op == "fp8":
         M, K, N = d[:3]
         fused = len(d) > 3 and d[3] == 1  # fp8:M,K,N,1 adds a bias and a residual in the epilogue
@@ -788,8 +800,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None, help="measure every hot-path row; JSON lines to this file")
     ap.add_argument("--profile-case", default=None,
-                    help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N | fp8:M,K,N | norm:M,K | "
-                         "normfp8:M,K | prep:K,N")
+                    help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N[,1] | fp8:M,K,N[,1] | "
+                         "norm:M,K | normfp8:M,K | kv:rows,D | prep:K,N")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--rows", default=None,
                     help="with --sweep: comma-separated row families to measure (e.g. a6,f2); default all")
