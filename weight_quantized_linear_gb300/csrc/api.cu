@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/wql.h: argument validation, kernel
 // selection by shape, launch-error reporting and the per-device error word of bounded waits.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -17,15 +18,17 @@ thread_local std::string g_last_error;
 __device__ unsigned g_wql_device_error;
 
 unsigned* device_error_word() {
-  static unsigned* cache[64] = {nullptr};
+  static std::atomic<unsigned*> cache[64];  // racing first calls store the same address
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  unsigned* w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_wql_device_error) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned*>(p);
+    w = static_cast<unsigned*>(p);
+    cache[dev].store(w, std::memory_order_release);
   }
-  return cache[dev];
+  return w;
 }
 
 wql_status fail(wql_status st, const std::string& msg) {

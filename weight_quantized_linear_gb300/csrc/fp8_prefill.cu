@@ -23,6 +23,8 @@
 // its barrier round trips and commits leave gaps that deeper stages or 256-k stages do not close).
 // When there are more tiles than SMs, two CTAs of three stages share each SM and fill each other's
 // gaps: M = 8192, N = 4096: 143 -> 107 us; M = 4096, N = 11008: 184 -> 144 us.
+#include <atomic>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
@@ -257,13 +259,13 @@ cudaError_t launch_f(const CUtensorMap& tx, const CUtensorMap& tw, const CUtenso
                      unsigned* dev_err, cudaStream_t stream) {
   using L = FLayout<BN, CTAS>;
   auto kern = fp8_prefill_kernel<BN, CTAS>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int grid = ntiles < CTAS * num_sms() ? ntiles : CTAS * num_sms();

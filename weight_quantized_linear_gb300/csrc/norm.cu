@@ -10,6 +10,8 @@
 // c mod 256, which adds its elements in increasing k; the 256 partial sums are then folded
 // pairwise (t, t+128), (t, t+64), ..., (t, t+1)), so int8 codes are reproducible bit for bit.
 // Every float operation uses an explicitly rounded intrinsic: nothing is contracted into FMA.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -271,25 +273,34 @@ cudaError_t launch_rows(const __half* x, const __half* residual, const __half* g
                         uint8_t* q, float* xs, float* absmax, __half* h_out, unsigned* err, cudaStream_t s) {
   auto kern = qrmsnorm_kernel<CPT, MODE>;
   const size_t smem = (size_t)norm_slots(CPT, MODE) * norm_rows_per_slot(MODE) * 2 * K;
-  static int set_bytes[64] = {0};   // dynamic shared memory limit set on the kernel, per device
-  static int fit_bytes[64] = {0};   // ring size of the cached occupancy
+  // Per device: the dynamic shared-memory limit set on this kernel, and the occupancy of the ring
+  // size last asked for.  They change together and only when a row length needs a larger ring, so
+  // one mutex keeps them consistent across host threads (an uncontended lock per call).
+  static std::mutex mu;
+  static int set_bytes[64] = {0};
+  static int fit_bytes[64] = {0};
   static int fit_ctas[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (set_bytes[dev] < (int)smem) {  // a longer row needs a larger ring: raise the limit
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    set_bytes[dev] = (int)smem;
+  int ctas = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (set_bytes[dev] < (int)smem) {  // a longer row needs a larger ring: raise the limit
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      set_bytes[dev] = (int)smem;
+    }
+    if (fit_bytes[dev] != (int)smem) {
+      int fit = 0;
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, kNormThreads, smem);
+      if (e != cudaSuccess) return e;
+      fit_bytes[dev] = (int)smem;
+      fit_ctas[dev] = fit > 0 ? fit : 1;
+    }
+    ctas = fit_ctas[dev];
   }
-  if (fit_bytes[dev] != (int)smem) {
-    int fit = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, kNormThreads, smem);
-    if (e != cudaSuccess) return e;
-    fit_bytes[dev] = (int)smem;
-    fit_ctas[dev] = fit > 0 ? fit : 1;
-  }
-  const long long cap = (long long)fit_ctas[dev] * num_sms();
+  const long long cap = (long long)ctas * num_sms();
   const dim3 grid((unsigned)(M < cap ? M : cap)), block(kNormThreads);
   return launch_pdl(kern, grid, block, smem, s, x, residual, gamma, eps, M, K, q, xs, absmax, h_out, err);
 }

@@ -1,5 +1,6 @@
 // tensormap.cu -- host helpers: TMA descriptor encoding (driver entry point looked up through the
 // runtime, so the library does not link libcuda directly) and cached device properties.
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -75,16 +76,18 @@ bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
 }
 
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // racing first calls store the same count
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = v > 0 ? v : 148;
+    n = v > 0 ? v : 148;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 int pick_k_split(const void* kernel, int threads, int smem_bytes, int units, int kblocks, bool pow2, bool balanced) {

@@ -27,6 +27,8 @@
 //     Deterministic and free of global scratch.  Cluster barrier phase 0 (arrive at start, wait
 //     before the first remote store) guarantees every peer is initialised; phase 1 (arrive once
 //     the own slice is complete, wait before exit) keeps every CTA alive until all stores landed.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -86,7 +88,8 @@ struct Layout {
 // of the sequence (measured: 48 q_proj layers at M = 1 then 48 at M = 16, 479 -> 402 us).
 template <int LG>
 int common_footprint() {
-  static int bytes = -1;
+  static std::atomic<int> cached{-1};  // racing first calls store the same value
+  int bytes = cached.load(std::memory_order_relaxed);
   if (bytes < 0) {
     int f = 0;
     for (int S = 1; S <= 8; ++S) {
@@ -98,6 +101,7 @@ int common_footprint() {
     cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     bytes = 2 * (f + reserved) <= per_sm ? f : 0;
+    cached.store(bytes, std::memory_order_relaxed);
   }
   return bytes;
 }
@@ -431,17 +435,17 @@ cudaError_t launch_mt(const CUtensorMap& tx, int x3d, const CUtensorMap& tq, con
   using L = Layout<MT, LG>;
   constexpr int kThreads = Warps<MT>::kThreads;
   auto kern = w4a16_decode_kernel<MT, LG>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
   const int common = common_footprint<LG>();
   int max_bytes = common;  // otherwise the largest over the cluster sizes (the receive buffer varies)
   if (!common)
     for (int S = 1; S <= 8; ++S) max_bytes = L::bytes(S) > max_bytes ? L::bytes(S) : max_bytes;
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int strips = (N + kStripCols - 1) / kStripCols;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);

@@ -26,6 +26,8 @@
 //     partials in split order, so the result does not depend on timing.
 // Launched with programmatic dependent launch: the packed weights of the first stages are
 // requested before waiting for the preceding kernel, whose output may be x.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -537,13 +539,13 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
                      int M, int N, int K, __half* y, int act, unsigned* dev_err, cudaStream_t stream) {
   using L = PLayout<BN, LG>;
   auto kern = w4a16_prefill_kernel<BN, LG>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int nkb = (K + L::kBK - 1) / L::kBK;

@@ -17,6 +17,8 @@
 // The fp8 variant (the page's quant_dtype fp8, float8_e4m3fn codes, fp32 accumulator) runs the same
 // pipeline: every e4m3 value is an fp16 value, so one cvt per pair of codes feeds the same fp16
 // MMA; its fp32 sums are not folded, and the split-K partials are added in fp32 in rank order.
+#include <atomic>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
@@ -287,13 +289,13 @@ cudaError_t launch8(const CUtensorMap& tx, const CUtensorMap& tw, const float* x
   // launch; with unequal footprints some SMs held two CTAs of one layer)
   const int bytes = MT <= 2 ? (Layout8<1>::kBytes > Layout8<2>::kBytes ? Layout8<1>::kBytes : Layout8<2>::kBytes)
                             : L::kBytes;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(w8a8_decode_kernel<MT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int strips = (N + kRows - 1) / kRows;
   const int mblocks = (M + 8 * MT - 1) / (8 * MT);

@@ -22,6 +22,8 @@
 //     and stored by TMA; a fused residual arrives the same way: TMA loads all of the tile's residual
 //     boxes while its last chunk's MMAs run (scalar residual loads on the epilogue's path made the
 //     M = 4096, N = 11008 block 1.9x slower).
+#include <atomic>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
@@ -351,13 +353,13 @@ cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const CUtenso
                      unsigned* dev_err, cudaStream_t stream) {
   using L = QLayout<BN>;
   auto kern = w8a8_prefill_kernel<BN>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
