@@ -291,8 +291,7 @@ cudaError_t launch_bn(const void* q, const void* qw, const float* xs, const floa
   // two CTAs per SM only when every SM gets at least one tile: with fewer tiles than SMs the block
   // scheduler may pair CTAs on some SMs while others stay idle (M = 512, N = 4096: 19.6 -> 20.5 us)
   const long long ntiles = (long long)((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  if constexpr (BN == 128)
-    if (ntiles > num_sms()) return launch_f<BN, 2>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
+  if (ntiles > num_sms()) return launch_f<BN, 2>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
   return launch_f<BN, 1>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
 }
 
@@ -301,9 +300,13 @@ cudaError_t launch_bn(const void* q, const void* qw, const float* xs, const floa
 // Token tile for an fp8 GEMM of M tokens: 64 up to 64 tokens, else 128.  A 256-token tile (fewer,
 // longer tiles, four stages) measured slower at every shape tried on GB300 (K = 4096, N = 4096 and
 // 11008, M = 128 .. 8192: e.g. M = 4096, N = 11008: 198 vs 182 us; M = 512, N = 4096: 28.4 vs 19.8 us).
+// When 128-token tiles would leave SMs idle but 64-token tiles outnumber the SMs, the smaller tiles
+// run two CTAs per SM instead.
 int fp8_prefill_tile_n(int M, int N) {
-  (void)N;
-  return M <= 64 ? 64 : 128;
+  if (M <= 64) return 64;
+  const long long ntn = (N + kBM - 1) / kBM, sms = num_sms();
+  if (ntn * ((M + 127) / 128) <= sms && ntn * ((M + 63) / 64) > sms) return 64;
+  return 128;
 }
 
 cudaError_t launch_fp8_prefill(const uint8_t* q, const float* xs, const uint8_t* qw, const float* ws, int M, int K,
