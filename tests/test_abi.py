@@ -105,3 +105,18 @@ def test_inputs_recipe_counts():
     assert np.count_nonzero(np.any(X != X0, axis=0)) == 10
     assert np.array_equal(inputs.gamma(64, seed=1), inputs.gamma(64, seed=1))
     assert len(inputs.sweep_cases()) == 45 and len(inputs.w8a8_cases()) == 8 and len(inputs.prefill_cases()) == 6
+
+
+def test_header_is_plain_c99(tmp_path):
+    """The boundary is a C ABI: include/wql.h must compile as strict C99 with no warnings."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_wql.c"
+    src.write_text('#include "wql.h"\nint main(void) { return wql_version() > 0 ? 0 : 1; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src),
+                        "-o", str(tmp_path / "use_wql.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
