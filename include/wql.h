@@ -68,6 +68,13 @@ int wql_version(void);
  * the synchronisation itself failed, WQL_OK otherwise. */
 wql_status wql_device_status(void* stream);
 
+/* Diagnostic of the failure path: launches one thread that waits on an on-chip barrier which
+ * nothing completes.  Its bounded wait gives up after the same time limit as every kernel's
+ * (about 2 s) and records the same device-side error, so the next wql_device_status() returns
+ * WQL_ETIMEOUT (and clears it); the context stays usable.  Launches nothing else and touches no
+ * caller memory.  Returns WQL_ECUDA if the launch fails. */
+wql_status wql_diag_expire_wait(void* stream);
+
 /* ----------------------------------------------------------------------------------------
  * awq_pack  [AWQ] section 2; [AUQ] sections 3.3 and 5.4.
  * Quantise fp32 weights w [K, N] to asymmetric int4, per group of G consecutive input

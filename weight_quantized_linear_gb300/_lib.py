@@ -29,6 +29,7 @@ SIGNATURES = {
     "wql_last_error": (ctypes.c_char_p, []),
     "wql_version": (_I, []),
     "wql_device_status": (_I, [_P]),
+    "wql_diag_expire_wait": (_I, [_P]),
     "wql_awq_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),
@@ -340,6 +341,13 @@ def device_status(device: torch.device | None = None) -> None:
     """Synchronise the current stream and raise if a kernel abandoned a bounded wait."""
     dev = device or torch.device("cuda", torch.cuda.current_device())
     _check(load().wql_device_status(_stream(dev)), "wql_device_status")
+
+
+def diag_expire_wait(device: torch.device | None = None) -> None:
+    """Launch the failure-path diagnostic: a bounded wait that gives up (about 2 s); the next
+    device_status() then raises WQLError with WQL_ETIMEOUT."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    _check(load().wql_diag_expire_wait(_stream(dev)), "wql_diag_expire_wait")
 
 
 # ---- fp8 (float8_e4m3fn) variant of W8A8 ------------------------------------------------------

@@ -31,6 +31,15 @@ unsigned* device_error_word() {
   return w;
 }
 
+// One thread waits on an mbarrier that nothing will complete.  The bounded wait gives up after its
+// time limit and records kErrTimeoutFull, exactly as a real kernel does when a copy never lands.
+__global__ void expire_wait_kernel(unsigned* err) {
+  __shared__ __align__(8) uint64_t bar;
+  wql::mbar_init(&bar, 1);  // one arrival expected, none will come
+  wql::fence_mbarrier_init();
+  if (!wql::mbar_wait_bounded(&bar, 0)) wql::report_error(err, wql::kErrTimeoutFull);
+}
+
 wql_status fail(wql_status st, const std::string& msg) {
   g_last_error = msg;
   return st;
@@ -413,6 +422,13 @@ wql_status wql_kv_dequant_i8(const int8_t* q, const float* scales, int64_t rows,
               "scales must be a 4-byte aligned device pointer");
   return cuda_status(wql::launch_kv_dequant_i8(q, scales, rows, D, out, static_cast<cudaStream_t>(stream)),
                      "wql_kv_dequant_i8");
+}
+
+wql_status wql_diag_expire_wait(void* stream) {
+  unsigned* dev_err = device_error_word();
+  if (!dev_err) return fail(WQL_ECUDA, "wql_diag_expire_wait: cannot locate the device error word");
+  expire_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dev_err);
+  return cuda_status(cudaGetLastError(), "wql_diag_expire_wait");
 }
 
 }  // extern "C"
