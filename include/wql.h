@@ -35,6 +35,20 @@
  *     they then record a device-side error that wql_device_status() returns as WQL_ETIMEOUT.
  *   - M = 0 is a valid empty call: it returns WQL_OK and launches nothing.
  *   - The library holds no per-call state; calls on different streams may run concurrently.
+ *   - Weight prefetch (programmatic dependent launch): the W4A16 GEMMs and the decode path of the
+ *     W8A8 GEMMs (int8 and fp8, up to 16 tokens) are launched so that they may start while the
+ *     kernel enqueued just before them on the stream is still running, and they begin copying
+ *     their WEIGHT operands (qweight / scales / qzeros, or qw) before that kernel has finished;
+ *     only the activations and the outputs wait for it.  So the weight buffers must already
+ *     hold their final contents when the preceding kernel on the stream starts finishing:
+ *       * the library's own weight writers (wql_awq_pack, wql_per_channel_quant_i8/_fp8) make
+ *         their writes visible device-wide before they exit, so pack-then-GEMM on one stream
+ *         with nothing in between is safe;
+ *       * a caller's kernel that writes weight buffers and is enqueued directly before one of
+ *         these GEMMs must end each thread's writes with a device-scope fence (__threadfence()),
+ *         or the two must be separated by something that is not a kernel launch (an event
+ *         record/wait, a memcpy, a stream synchronisation).
+ *     Writes to a GEMM's weights from other streams must be ordered by the caller as usual.
  */
 #ifndef WQL_H_
 #define WQL_H_

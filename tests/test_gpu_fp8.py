@@ -18,6 +18,8 @@ from weight_quantized_linear_gb300 import inputs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+from _gpu_util import Guarded, tile_rows  # noqa: E402
+
 
 @pytest.fixture(scope="module")
 def wql(wql_lib):
@@ -184,10 +186,14 @@ def test_fp8_gemm_within_fp32_summation_bound(wql, M, K, N):
     qW = _fp8_codes(rng, (N, K), 60.0)
     xs = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
     ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
-    acc = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    y = wql.w8a8_gemm_fp8(dev8(q), dev(xs), dev8(qW), dev(ws), acc_out=acc)
-    rows = sample_rows(M, 24)
-    check_fp8_gemm(host(y), host(acc), q, qW, xs, ws, K, rows)
+    acc = Guarded((M, N), torch.float32)
+    yg = Guarded((M, N), torch.float16)
+    y = wql.w8a8_gemm_fp8(dev8(q), dev(xs), dev8(qW), dev(ws), out=yg.t, acc_out=acc.t)
+    acc.check()
+    yg.check()
+    assert np.isfinite(host(y)).all() and np.isfinite(host(acc.t)).all()  # every element written
+    rows = tile_rows(M, 8)
+    check_fp8_gemm(host(y), host(acc.t), q, qW, xs, ws, K, rows)
     # deterministic: a second call gives the same bits
     y2 = wql.w8a8_gemm_fp8(dev8(q), dev(xs), dev8(qW), dev(ws))
     assert torch.equal(y, y2)

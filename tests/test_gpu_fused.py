@@ -4,6 +4,8 @@ Residual-fused QRMSNorm (h = fp16(x + r), then QRMSNorm + per-token int8 of h) a
 epilogue with an optional bias and residual (y = fp16(((acc * xs) * ws + bias) + residual)) must
 match the oracle bit for bit: the new residual h, the codes, the per-token scales and the fp16
 outputs, on both GEMM kernels (decode up to 16 tokens, tcgen05 from 17), in place or not.
+GEMM outputs not written in place go into NaN-poisoned buffers with guard bands: every element must
+be written and neither guard touched.
 """
 import numpy as np
 import pytest
@@ -13,6 +15,8 @@ from weight_quantized_linear_gb300 import inputs
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
+
+from _gpu_util import Guarded, tile_rows  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -72,14 +76,18 @@ def test_w8a8_fused_epilogue_bit_exact(wql, M, K, N, terms):
     ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
     bias = rng.normal(0, 1, N).astype(np.float16) if terms in ("bias", "both") else None
     res = rng.normal(0, 2, (M, N)).astype(np.float16) if terms in ("residual", "both") else None
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    y = wql.w8a8_gemm_fused(dev(q), dev(xs), dev(qW), dev(ws), None if bias is None else dev(bias),
-                            None if res is None else dev(res), acc_out=acc)
-    rows = np.unique(np.linspace(0, M - 1, min(M, 32)).astype(np.int64))
+    acc = Guarded((M, N), torch.int32)
+    y = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm_fused(dev(q), dev(xs), dev(qW), dev(ws), None if bias is None else dev(bias),
+                        None if res is None else dev(res), out=y.t, acc_out=acc.t)
+    acc.check()
+    y.check()
+    assert acc.unwritten() == 0 and y.unwritten() == 0
+    rows = tile_rows(M, 8)
     acc_r = oracle.w8a8_acc(q, qW, rows=rows)
-    assert np.array_equal(host(acc)[rows], acc_r)
+    assert np.array_equal(host(acc.t)[rows], acc_r)
     y_r = oracle.w8a8_epilogue_fused(acc_r, xs[rows], ws, bias, None if res is None else res[rows])
-    assert np.array_equal(host(y)[rows].view(np.uint16), y_r.view(np.uint16))
+    assert np.array_equal(host(y.t)[rows].view(np.uint16), y_r.view(np.uint16))
     wql.device_status()
 
 

@@ -2,7 +2,11 @@
 
 Bars: packed weights, int8 activations and scales, per-channel weights and int32 accumulators
 bit-exact; fp16 outputs within 1e-2 of the fp64 oracle, normalised by each row's L2 norm.
+Every output of a GEMM under test is written into a NaN-poisoned buffer with guard bands on both
+sides: all of it must come out finite (no tile left unwritten) and both guards untouched.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -12,7 +16,7 @@ from weight_quantized_linear_gb300 import inputs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ROW_TOL = 1e-2  # max over rows of ||y_gpu - y_ref||_2 / ||y_ref||_2
+from _gpu_util import ROW_TOL, Guarded, tile_rows  # noqa: E402  (max over rows of ||y - y_ref|| / ||y_ref||)
 
 
 @pytest.fixture(scope="module")
@@ -84,7 +88,11 @@ def _w4a16_case(wql, M, K, N, G, w_out=True, x_out=False, seed=0, rows=None):
     W = inputs.weight(K, N, seed=seed, outliers=w_out)
     X = inputs.activations(M, K, seed=seed, outlier_channels=x_out)
     qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
-    y = host(wql.w4a16_gemm(dev(X), dev(u32_to_i32(qw_r)), dev(s_r), dev(u32_to_i32(qz_r)), G))
+    out = Guarded((M, N), torch.float16)
+    wql.w4a16_gemm(dev(X), dev(u32_to_i32(qw_r)), dev(s_r), dev(u32_to_i32(qz_r)), G, out=out.t)
+    out.check()
+    y = host(out.t)
+    assert np.isfinite(y).all(), f"{int((~np.isfinite(y)).sum())} outputs left unwritten or not finite"
     rows = np.arange(M, dtype=np.int64) if rows is None else rows
     ref = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
     return y[rows], ref
@@ -130,8 +138,10 @@ def test_w4a16_parity_layer_sweep(wql, case):
 
 
 @pytest.mark.parametrize("case", inputs.prefill_cases(), ids=lambda c: f"M{c['M']}N{c['N']}")
-def test_w4a16_parity_prefill_sampled_rows(wql, case):
-    rows = sample_rows(case["M"], 12)
+def test_w4a16_parity_prefill_every_token_tile(wql, case):
+    # the first and last row of every 32-row block: both edges of every token tile the kernel uses;
+    # the rest of the output is checked for being written (finite, guards intact)
+    rows = tile_rows(case["M"])
     y, ref = _w4a16_case(wql, case["M"], case["K"], case["N"], case["G"], w_out=False, x_out=True, rows=rows)
     assert row_rel_err(y, ref) <= ROW_TOL
 
@@ -142,6 +152,40 @@ def test_w4a16_zero_activations_give_zero(wql):
     qw, s, qz = wql.awq_pack(dev(W), G)
     y = host(wql.w4a16_gemm(torch.zeros((4, K), dtype=torch.float16, device="cuda"), qw, s, qz, G))
     assert np.all(y == 0)
+    wql.device_status()
+
+
+def test_pack_then_gemm_on_one_stream_without_sync(wql):
+    """The GEMMs copy their weights before waiting for the preceding kernel (programmatic dependent
+    launch); the packing kernel makes its writes visible before it exits, so a GEMM enqueued right
+    after it reads the new weights.  Two weights are packed alternately into the same buffers, each
+    pack followed at once by a GEMM (no synchronisation in between): every GEMM must see the weights
+    of the pack just before it, never the other ones."""
+    M, K, N, G = 4, 4096, 4096, 128
+    Ws = [dev(inputs.weight(K, N, seed=40 + i, outliers=True)) for i in range(2)]
+    x = dev(inputs.activations(M, K, seed=40))
+    qw = torch.empty((K, N // 8), dtype=torch.int32, device="cuda")
+    s = torch.empty((K // G, N), dtype=torch.float16, device="cuda")
+    qz = torch.empty((K // G, N // 8), dtype=torch.int32, device="cuda")
+    refs = []
+    for W in Ws:  # each weight's output, computed with a synchronisation in between
+        a, b, c = wql.awq_pack(W, G)
+        refs.append(wql.w4a16_gemm(x, a, b, c, G).clone())
+    torch.cuda.synchronize()
+    assert not torch.equal(refs[0], refs[1])
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(40)]
+    for i, y in enumerate(ys):
+        W = Ws[i % 2]
+        K_, N_ = W.shape
+        lib = wql.load()
+        st = torch.cuda.current_stream().cuda_stream
+        assert lib.wql_awq_pack(ctypes.c_void_p(W.data_ptr()), K_, N_, G, ctypes.c_void_p(qw.data_ptr()),
+                                ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(qz.data_ptr()),
+                                ctypes.c_void_p(st)) == 0
+        wql.w4a16_gemm(x, qw, s, qz, G, out=y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        assert torch.equal(y, refs[i % 2]), f"GEMM {i} did not see the weights packed just before it"
     wql.device_status()
 
 
@@ -196,19 +240,27 @@ def test_w8a8_prep_chain_bit_exact(wql, M, K, N):
     assert np.array_equal(got["q"], ref["q"])
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 11008), (5, 512, 96), (33, 1024, 160),
-                                   (512, 4096, 4096)])
+W8A8_BLOCK_CELLS = [(c["M"], c["K"], c["N"]) for c in inputs.w8a8_cases()]  # all eight (M, N) cells
+
+
+@pytest.mark.parametrize("M,K,N", W8A8_BLOCK_CELLS + [(5, 512, 96), (33, 1024, 160)])
 def test_w8a8_gemm_bit_exact(wql, M, K, N):
     got, ref, (q, xs, qW, ws) = _w8a8_chain(wql, M, K, N, seed=2)
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    y = wql.w8a8_gemm(q, xs, qW, ws, acc_out=acc)
-    rows = sample_rows(M, 24)
+    acc = Guarded((M, N), torch.int32)
+    yg = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm(q, xs, qW, ws, out=yg.t, acc_out=acc.t)
+    acc.check()
+    yg.check()
+    y = host(yg.t)
+    assert np.isfinite(y).all(), f"{int((~np.isfinite(y)).sum())} outputs left unwritten"
+    assert acc.unwritten() == 0  # 0x7F7F7F7F exceeds any sum of K <= 2^17 int8 products
+    rows = tile_rows(M)
     acc_r = oracle.w8a8_acc(ref["q"], ref["qW"], rows=rows)
     y_r = oracle.w8a8_epilogue(acc_r, ref["xs"][rows], ref["ws"])
-    assert np.array_equal(host(acc)[rows], acc_r)
-    assert np.array_equal(host(y)[rows].view(np.uint16), y_r.view(np.uint16))
+    assert np.array_equal(host(acc.t)[rows], acc_r)
+    assert np.array_equal(y[rows].view(np.uint16), y_r.view(np.uint16))
     y64 = oracle.w8a8_epilogue_f64(acc_r, ref["xs"][rows], ref["ws"])
-    assert row_rel_err(host(y)[rows], y64) <= ROW_TOL
+    assert row_rel_err(y[rows], y64) <= ROW_TOL
 
 
 @pytest.mark.parametrize("K", [4096, 16384])

@@ -3,6 +3,8 @@
 W4A16: fp16 output within 1e-2 of the fp64 oracle (row-relative L2), on ragged tiles.
 W8A8: int32 accumulators and fp16 outputs bit-exact, including adversarial extremes whose sums
 leave the range where fp32 holds integers exactly (checks the 1024-k chunk folding).
+GEMM outputs go into NaN-poisoned buffers with guard bands: every element must be written (finite)
+and neither guard touched.
 """
 import numpy as np
 import pytest
@@ -12,6 +14,8 @@ from weight_quantized_linear_gb300 import inputs
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
+
+from _gpu_util import Guarded, tile_rows  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -47,8 +51,11 @@ def test_w4a16_prefill_ragged(wql, monkeypatch, M, K, N, G):
     W = inputs.weight(K, N, seed=2, outliers=True)
     X = inputs.activations(M, K, seed=2, outlier_channels=True)
     qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
-    rows = np.unique(np.linspace(0, M - 1, min(M, 24)).astype(np.int64))
-    y = host(wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G))
+    rows = tile_rows(M)
+    out = Guarded((M, N), torch.float16)
+    wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G, out=out.t)
+    out.check()
+    y = host(out.t)
     ref = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
     assert np.isfinite(y).all()
     assert row_rel_err(y[rows], ref) <= 1e-2
@@ -77,12 +84,16 @@ def test_w8a8_prefill_bit_exact(wql, M, K, N):
     qW = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
     xs = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
     ws = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    y = wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), acc_out=acc)
-    rows = np.unique(np.linspace(0, M - 1, min(M, 32)).astype(np.int64))
+    acc = Guarded((M, N), torch.int32)
+    y = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), out=y.t, acc_out=acc.t)
+    acc.check()
+    y.check()
+    assert acc.unwritten() == 0 and y.unwritten() == 0
+    rows = tile_rows(M)
     acc_r = oracle.w8a8_acc(q, qW, rows=rows)
-    assert np.array_equal(host(acc)[rows], acc_r)
-    assert np.array_equal(host(y)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xs[rows], ws).view(np.uint16))
+    assert np.array_equal(host(acc.t)[rows], acc_r)
+    assert np.array_equal(host(y.t)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xs[rows], ws).view(np.uint16))
     wql.device_status()
 
 
@@ -117,13 +128,38 @@ def test_w8a8_smoothquant_block_full_size_sampled(wql):
     s, g2, W2 = wql.smooth(a, gd, Wd)
     qW, ws = wql.per_channel_quant_i8(W2)
     q, xs = wql.qrmsnorm_quant_i8(Xd, g2, inputs.EPS)
-    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    y = wql.w8a8_gemm(q, xs, qW, ws, acc_out=acc)
-    rows = np.array([0, 1, 777, 2048, 4095], dtype=np.int64)
+    acc = Guarded((M, N), torch.int32)
+    y = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm(q, xs, qW, ws, out=y.t, acc_out=acc.t)
+    acc.check()
+    y.check()
+    assert acc.unwritten() == 0 and y.unwritten() == 0
+    rows = tile_rows(M)  # first and last row of every 32-row block: both edges of every token tile
     qh, qWh, xsh, wsh = host(q), host(qW), host(xs), host(ws)
     acc_r = oracle.w8a8_acc(qh, qWh, rows=rows)
-    assert np.array_equal(host(acc)[rows], acc_r)
-    assert np.array_equal(host(y)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xsh[rows], wsh).view(np.uint16))
+    assert np.array_equal(host(acc.t)[rows], acc_r)
+    assert np.array_equal(host(y.t)[rows].view(np.uint16), oracle.w8a8_epilogue(acc_r, xsh[rows], wsh).view(np.uint16))
+    wql.device_status()
+
+
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_w8a8_prefill_most_negative_codes_fill_a_chunk(wql, K):
+    """q = qw = -128 everywhere: every product is 2^14, a 1024-k chunk sums to exactly 2^24 (the largest
+    integer range fp32 holds exactly), and K = 4096 folds four such chunks into 2^26 in int32."""
+    M, N = 40, 96
+    q = np.full((M, K), -128, np.int8)
+    qW = np.full((N, K), -128, np.int8)
+    xs = np.full((M,), 1e-3, np.float32)
+    ws = np.full((N,), 1e-4, np.float32)
+    acc = Guarded((M, N), torch.int32)
+    y = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), out=y.t, acc_out=acc.t)
+    acc.check()
+    y.check()
+    ref = oracle.w8a8_acc(q, qW)
+    assert int(ref[0, 0]) == K * 16384
+    assert np.array_equal(host(acc.t), ref)
+    assert np.array_equal(host(y.t).view(np.uint16), oracle.w8a8_epilogue(ref, xs, ws).view(np.uint16))
     wql.device_status()
 
 
@@ -152,7 +188,11 @@ def test_w4a16_both_kernels_across_the_dispatch_threshold(wql, monkeypatch, kern
     W = inputs.weight(K, N, seed=3, outliers=True)
     X = inputs.activations(M, K, seed=3, outlier_channels=True)
     qw_r, s_r, qz_r = oracle.awq_quantize(W, G)
-    y = host(wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G))
-    rows = np.unique(np.linspace(0, M - 1, min(M, 16)).astype(np.int64))
+    out = Guarded((M, N), torch.float16)
+    wql.w4a16_gemm(dev(X), dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32)), G, out=out.t)
+    out.check()
+    y = host(out.t)
+    assert np.isfinite(y).all()
+    rows = tile_rows(M, 8)
     assert row_rel_err(y[rows], oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)) <= 1e-2
     wql.device_status()

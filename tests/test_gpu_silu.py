@@ -17,6 +17,8 @@ from weight_quantized_linear_gb300 import inputs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+from _gpu_util import Guarded  # noqa: E402
+
 ROW_TOL = 1e-2
 
 
@@ -43,19 +45,25 @@ def sample_rows(M, n=12):
 
 
 def _case(wql, M, K, N, G, seed):
+    """The weights in the oracle's packing (nothing the oracle sees comes from the CUDA path), and the
+    same packed tensors on the device for the kernels under test."""
     W = inputs.weight(K, N, seed=seed, outliers=True)  # columns 2j / 2j + 1 act as gate j / up j
     X = inputs.activations(M, K, seed=seed, outlier_channels=True)
-    qw, s, qz = wql.awq_pack(dev(W), G)
-    return X, qw, s, qz
+    packed = oracle.awq_quantize(W, G)
+    qw_r, s_r, qz_r = packed
+    return X, packed, dev(qw_r.view(np.int32)), dev(s_r), dev(qz_r.view(np.int32))
 
 
-def _check(wql, X, qw, s, qz, G, M, N):
+def _check(wql, X, packed, qw, s, qz, G, M, N):
     x = dev(X)
-    y = wql.w4a16_gemm_silu_mul(x, qw, s, qz, G)
-    assert y.shape == (M, N // 2)
+    out = Guarded((M, N // 2), torch.float16)
+    y = wql.w4a16_gemm_silu_mul(x, qw, s, qz, G, out=out.t)
+    out.check()
+    assert y.shape == (M, N // 2) and np.isfinite(host(y)).all()
     rows = sample_rows(M)
-    # the oracle: fp64 GEMM of the packed weight, then silu(gate) * up in fp64
-    y2 = oracle.w4a16_linear(X, host(qw).view(np.uint32), host(s), host(qz).view(np.uint32), G, rows=rows)
+    # the oracle: fp64 GEMM of the oracle-packed weight, then silu(gate) * up in fp64
+    qw_r, s_r, qz_r = packed
+    y2 = oracle.w4a16_linear(X, qw_r, s_r, qz_r, G, rows=rows)
     ref = oracle.silu_mul_f64(y2)
     got = host(y)[rows].astype(np.float64)
     num = np.linalg.norm(got - ref, axis=1)
@@ -81,16 +89,16 @@ def _check(wql, X, qw, s, qz, G, M, N):
                                      (128, 4096, 1024, 128), (300, 4096, 22016, 128), (2048, 4096, 4096, 128),
                                      (37, 1024, 192, 64)])
 def test_w4a16_silu_mul(wql, M, K, N, G):
-    X, qw, s, qz = _case(wql, M, K, N, G, seed=M + N)
-    _check(wql, X, qw, s, qz, G, M, N)
+    X, packed, qw, s, qz = _case(wql, M, K, N, G, seed=M + N)
+    _check(wql, X, packed, qw, s, qz, G, M, N)
 
 
 @pytest.mark.parametrize("force", ["decode", "prefill"])
 def test_w4a16_silu_mul_both_kernels_mid_m(wql, monkeypatch, force):
     M, K, N, G = 24, 2048, 1024, 128
     monkeypatch.setenv("WQL_FORCE_KERNEL", force)
-    X, qw, s, qz = _case(wql, M, K, N, G, seed=7)
-    _check(wql, X, qw, s, qz, G, M, N)
+    X, packed, qw, s, qz = _case(wql, M, K, N, G, seed=7)
+    _check(wql, X, packed, qw, s, qz, G, M, N)
 
 
 def test_w4a16_silu_mul_gate_up_interleave_helper(wql):
@@ -100,9 +108,11 @@ def test_w4a16_silu_mul_gate_up_interleave_helper(wql):
     fused = wql.interleave_gate_up(dev(wg), dev(wu))
     f = host(fused)
     assert np.array_equal(f[:, 0::2], wg) and np.array_equal(f[:, 1::2], wu)
+    packed = oracle.awq_quantize(np.concatenate([wg[:, :, None], wu[:, :, None]], axis=2).reshape(K, 2 * I), G)
     qw, s, qz = wql.awq_pack(fused, G)
+    assert np.array_equal(host(qw), packed[0].view(np.int32))  # the device packing agrees bit for bit
     X = inputs.activations(M, K, seed=13)
-    _check(wql, X, qw, s, qz, G, M, 2 * I)
+    _check(wql, X, packed, qw, s, qz, G, M, 2 * I)
 
 
 def test_w4a16_silu_mul_rejects_odd_pairs(wql):

@@ -10,8 +10,12 @@ failure has then already run every other test.
 import numpy as np
 import pytest
 
+import oracle
+
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
+
+from _gpu_util import tile_rows  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -31,9 +35,12 @@ def _case(M, K, N, seed):
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(wql):
-    # Two different problems back to back through the C ABI: the second call reuses the shared
-    # scratch the first one filled, and both must equal the workspace-taking entry point bit for bit.
-    for M, K, N, seed in [(257, 4096, 4096, 1), (1024, 2048, 4160, 2)]:
+    # Problems back to back through the C ABI: each call reuses the shared scratch the previous one
+    # filled, and each must equal the workspace-taking entry point bit for bit.  The third problem
+    # is smaller than the second, so the scratch still holds the second call's data past its own
+    # M * K elements: nothing left over from an earlier call may leak into a result.  The oracle
+    # checks the accumulators and outputs on the first and last row of every 32-row block.
+    for M, K, N, seed in [(257, 4096, 4096, 1), (1024, 2048, 4160, 2), (300, 1024, 256, 3)]:
         q, xs, qw, ws = _case(M, K, N, seed)
         y_ref = wql.w8a8_gemm(q, xs, qw, ws)
         acc_ref = torch.empty((M, N), dtype=torch.int32, device="cuda")
@@ -44,6 +51,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(wql):
         torch.cuda.synchronize()
         assert torch.equal(acc, acc_ref)
         assert torch.equal(y, y_ref)
+        rows = tile_rows(M)
+        qh, qwh, xsh, wsh = q.cpu().numpy(), qw.cpu().numpy(), xs.cpu().numpy(), ws.cpu().numpy()
+        acc_o = oracle.w8a8_acc(qh, qwh, rows=rows)
+        assert np.array_equal(acc.cpu().numpy()[rows], acc_o)
+        y_o = oracle.w8a8_epilogue(acc_o, xsh[rows], wsh)
+        assert np.array_equal(y.cpu().numpy()[rows].view(np.uint16), y_o.view(np.uint16))
     wql.device_status()
 
 

@@ -131,6 +131,10 @@ __global__ void __launch_bounds__(kPackThreads, 4)
     const uint32_t other = __shfl_xor_sync(live, half, 1);
     if (!upper) qweight[(size_t)(k0 + r) * NW + c] = half | (other << 16);
   }
+  // The GEMMs read packed weights before waiting for the preceding kernel (programmatic dependent
+  // launch): make this thread's writes visible device-wide before it exits, and so before this
+  // grid completes, which is when a GEMM launched right after it on the stream may start.
+  __threadfence();
 }
 
 __device__ __forceinline__ float block_max256(float v, float* red) {
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(256) colmax_scale_kernel(float* __restrict__ w
   if (n >= N) return;
   const float a = ws[n];
   ws[n] = a == 0.f ? 1.0f : __fdiv_rn(a, qmax);
+  __threadfence();  // visible before the grid completes (see awq_pack_kernel)
 }
 
 // qw[n, k] = clamp(rint(w[k, n] / ws_n), -127, 127) (FP8: the e4m3 code of w[k, n] / ws_n),
@@ -266,6 +271,7 @@ __global__ void __launch_bounds__(256)
     const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + row * kQTStride + 16 * part);
     *reinterpret_cast<uint4*>(qw + (size_t)nn * K + kk) = make_uint4(src[0], src[1], src[2], src[3]);
   }
+  __threadfence();  // the decode GEMMs read qw before their dependency wait (see awq_pack_kernel)
 }
 
 }  // namespace
