@@ -210,6 +210,61 @@ def test_sumsq_close_to_exact_sum():
         assert abs(oracle.sumsq(row) - exact) <= 1e-6 * exact
 
 
+def _round_f32(v: Fraction) -> Fraction:
+    """v rounded to the nearest binary32 value, ties to even (normal range), in exact rationals."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    ulp = Fraction(2) ** (e - 23)
+    q = a / ulp
+    n = q.numerator // q.denominator
+    r = q - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return (n * ulp) if v > 0 else -(n * ulp)
+
+
+def _sumsq_in_lanes(sq, lane_of):
+    """Sum of the squares in 256 lanes (each in increasing k), then the pairwise fold (t, t+128),
+    (t, t+64), ..., (t, t+1), rounding to fp32 after every addition."""
+    lanes = [Fraction(0)] * 256
+    for k, v in enumerate(sq):
+        t = lane_of(k)
+        lanes[t] = _round_f32(lanes[t] + v)
+    stride = 128
+    while stride >= 1:
+        for t in range(stride):
+            lanes[t] = _round_f32(lanes[t] + lanes[t + stride])
+        stride //= 2
+    return lanes[0]
+
+
+def test_sumsq_follows_the_documented_lane_order():
+    """The fixed reduction order that the bit-exact QRMSNorm comparison depends on (element k in
+    lane (k / 8) mod 256, lanes in increasing k, then the pairwise fold), re-evaluated in exact
+    rationals with an explicit round-to-fp32 after each addition.  The row is built so that the
+    sequential order and the (k mod 256) lane order give other fp32 sums: large squares (2^20)
+    share lanes with mid-size ones under one order and not under the other."""
+    K = 4096
+    x = np.zeros(K, np.float16)
+    j = np.arange(16)
+    x[8 * j] = 1024.0
+    x[8 * j + 1] = (0.8 + 0.0137 * j).astype(np.float16)
+    rest = np.setdiff1d(np.arange(K), np.concatenate([8 * j, 8 * j + 1]))
+    x[rest] = (np.random.default_rng(3).standard_normal(rest.size) * 0.05).astype(np.float16)
+    sq = [Fraction(float(v)) ** 2 for v in x]  # each square is exact in fp32 (11-bit significands)
+    documented = _sumsq_in_lanes(sq, lambda k: (k // 8) % 256)
+    mod256 = _sumsq_in_lanes(sq, lambda k: k % 256)
+    sequential = Fraction(0)
+    for v in sq:
+        sequential = _round_f32(sequential + v)
+    assert len({documented, mod256, sequential}) == 3  # the three orders are told apart
+    assert Fraction(oracle.sumsq(x)) == documented
+
+
 def test_qrmsnorm_against_float64_definition():
     # Independent fp64 evaluation of RMSNorm + absmax/127 + round-half-even: codes may differ only
     # where the fp64 quotient sits within 1e-4 of a .5 boundary; scales agree to fp32 precision.
