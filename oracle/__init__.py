@@ -51,6 +51,8 @@ _SIGS = {
     "wql_oracle_w8a8_epilogue": (None, [_P, _P, _P, _I, _I, _P]),
     "wql_oracle_w8a8_epilogue_fused": (None, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "wql_oracle_add_qrmsnorm_quant_i8": (None, [_P, _P, _P, _F, _I, _I, _P, _P, _P]),
+    "wql_oracle_per_token_quant_i8": (None, [_P, _I, _I, _P, _P]),
+    "wql_oracle_per_token_quant_fp8": (None, [_P, _I, _I, _P, _P]),
     "wql_oracle_w8a8_epilogue_f64": (None, [_P, _P, _P, _I, _I, _P]),
     "wql_oracle_sym_int4_per_tensor": (_F, [_P, _I64, _P]),
     "wql_oracle_e4m3_to_float_n": (None, [_P, _P, _I64]),
@@ -213,6 +215,26 @@ def add_qrmsnorm_quant_i8(X, R, gamma, eps: float):
     _load().wql_oracle_add_qrmsnorm_quant_i8(_ptr(Xb), _ptr(Rb), _ptr(_half_bits(gamma)), eps, M, K, _ptr(h),
                                              _ptr(q), _ptr(xs))
     return h.view(np.float16), q, xs
+
+
+def per_token_quant_i8(X):
+    """[W8A8] per_token_quant_int8 of plain fp16 activations: returns (q int8 [M, K], xs fp32 [M])."""
+    Xb = _half_bits(X)
+    M, K = Xb.shape
+    q = np.empty((M, K), np.int8)
+    xs = np.empty((M,), np.float32)
+    _load().wql_oracle_per_token_quant_i8(_ptr(Xb), M, K, _ptr(q), _ptr(xs))
+    return q, xs
+
+
+def per_token_quant_fp8(X):
+    """fp8 (e4m3) twin of per_token_quant_i8: returns (q e4m3 codes uint8 [M, K], xs fp32 [M])."""
+    Xb = _half_bits(X)
+    M, K = Xb.shape
+    q = np.empty((M, K), np.uint8)
+    xs = np.empty((M,), np.float32)
+    _load().wql_oracle_per_token_quant_fp8(_ptr(Xb), M, K, _ptr(q), _ptr(xs))
+    return q, xs
 
 
 def act_absmax(X, gamma, eps: float) -> np.ndarray:

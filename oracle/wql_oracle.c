@@ -265,6 +265,27 @@ void wql_oracle_qrmsnorm_quant_i8(const uint16_t* X, const uint16_t* gamma, floa
   }
 }
 
+/* [W8A8] per_token_quant_int8, the quantiser QLinear.forward applies to an input that does not come
+ * from QRMSNorm: the same per-token rule on the activations themselves,
+ * xs_m = max_k |x_mk| / 127 (1.0 for an all-zero row); q_mk = clamp(rint(x_mk / xs_m), -128, 127),
+ * with x_mk the fp16 value widened to fp32 and one rounding per operation. */
+void wql_oracle_per_token_quant_i8(const uint16_t* X, int M, int K, int8_t* q, float* xs) {
+#pragma omp parallel for schedule(static)
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* x = X + (size_t)m * K;
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float a = fabsf(wql_oracle_half_to_float(x[k]));
+      if (a > amax) amax = a;
+    }
+    float scale = amax / 127.0f;
+    if (amax == 0.0f) scale = 1.0f;
+    xs[m] = scale;
+    for (int k = 0; k < K; ++k)
+      q[(size_t)m * K + k] = (int8_t)clamp_rint(wql_oracle_half_to_float(x[k]) / scale, -128.0f, 127.0f);
+  }
+}
+
 /* [W8A8] calibration statistic used by smoothing: a_j = max_m |RMSNorm_gamma(X)_mj|. */
 /* [W8A8] "inference kernels": rms_norm_dynamic_quant with its residual fusion
  * (add_rms_norm_quant_kernel).  Reading (the page names the fusion, not its arithmetic):
@@ -463,6 +484,24 @@ void wql_oracle_qrmsnorm_quant_fp8(const uint16_t* X, const uint16_t* gamma, flo
     xs[m] = scale;
     for (int k = 0; k < K; ++k) q[(size_t)m * K + k] = wql_oracle_float_to_e4m3(y[k] / scale);
     free(y);
+  }
+}
+
+/* The fp8 twin of per_token_quant_int8: xs_m = max_k |x_mk| / 448 (1.0 for an all-zero row);
+ * q_mk = e4m3(x_mk / xs_m), the e4m3 value nearest the fp32 quotient (ties to even). */
+void wql_oracle_per_token_quant_fp8(const uint16_t* X, int M, int K, uint8_t* q, float* xs) {
+#pragma omp parallel for schedule(static)
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* x = X + (size_t)m * K;
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float a = fabsf(wql_oracle_half_to_float(x[k]));
+      if (a > amax) amax = a;
+    }
+    float scale = amax / 448.0f;
+    if (amax == 0.0f) scale = 1.0f;
+    xs[m] = scale;
+    for (int k = 0; k < K; ++k) q[(size_t)m * K + k] = wql_oracle_float_to_e4m3(wql_oracle_half_to_float(x[k]) / scale);
   }
 }
 

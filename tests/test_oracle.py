@@ -561,6 +561,72 @@ def test_qrmsnorm_fp8_against_definition_and_brute_force():
     assert _e4m3_error_ok(q, y, xs[:, None])
 
 
+def test_per_token_quant_i8_recovers_exactly_representable_rows():
+    # each row is c * 2^-e with integer codes c in [-127, 127] and |c| = 127 present: the scale is
+    # 127 * 2^-e / 127 = 2^-e exactly, so the codes come back as c
+    rng = np.random.default_rng(70)
+    M, K = 7, 1000
+    c = rng.integers(-127, 128, size=(M, K))
+    c[np.arange(M), (np.arange(M) * 37) % K] = np.where(np.arange(M) % 2 == 0, 127, -127)
+    e = np.arange(M) - 3  # 2^3 .. 2^-3
+    x = (c * (2.0 ** -e)[:, None]).astype(np.float16)
+    q, xs = oracle.per_token_quant_i8(x)
+    assert np.array_equal(xs, (2.0 ** -e).astype(np.float32))
+    assert np.array_equal(q.astype(np.int64), c)
+
+
+def test_per_token_quant_i8_definition_bounds_and_zero_row():
+    X = inputs.activations(11, 4096, seed=71, outlier_channels=True)
+    X[4] = 0  # an all-zero row
+    X[6] *= np.float16(1e-3)
+    q, xs = oracle.per_token_quant_i8(X)
+    xf = X.astype(np.float32)
+    amax = np.abs(xf).max(axis=1)
+    want = np.where(amax == 0, np.float32(1.0), amax / np.float32(127.0)).astype(np.float32)
+    assert np.array_equal(xs.view(np.uint32), want.view(np.uint32))  # absmax / Q_MAX in fp32
+    assert xs[4] == 1.0 and np.all(q[4] == 0)
+    nz = amax > 0
+    assert np.all(np.abs(q[nz].astype(np.int64)).max(axis=1) == 127)  # the row's absmax lands on 127
+    err = np.abs(q.astype(np.float64) * xs[:, None].astype(np.float64) - xf)
+    assert np.all(err <= xs[:, None].astype(np.float64) * (0.5 + 1e-5))  # nearest code: half a step
+    # an independent fp64 evaluation: codes may differ only within 1e-4 of a .5 tie
+    t = xf.astype(np.float64) / xs[:, None].astype(np.float64)
+    ref = np.clip(np.round(t), -128, 127)  # numpy rounds half to even
+    diff = q.astype(np.float64) != ref
+    assert np.all(np.abs(np.abs(t[diff] - np.floor(t[diff])) - 0.5) < 1e-4)
+
+
+def test_per_token_quant_i8_half_integer_ties_go_to_even():
+    # a row whose scale is exactly 1 (absmax 127) holds every half-integer tie in [-126.5, 126.5]
+    ties = np.arange(-126.5, 127.0, 1.0)
+    x = np.concatenate([[127.0], ties, [0.0] * 2]).astype(np.float16)[None, :]
+    q, xs = oracle.per_token_quant_i8(x)
+    assert xs[0] == 1.0
+    assert np.array_equal(q[0, 1:1 + ties.size].astype(np.float64), np.round(ties))  # to even
+
+
+def test_per_token_quant_fp8_against_definition_and_brute_force():
+    M, K = 9, 640
+    X = inputs.activations(M, K, seed=72, outlier_channels=True)
+    X[3] = 0  # an all-zero row
+    q, xs = oracle.per_token_quant_fp8(X)
+    xf = X.astype(np.float32)
+    amax = np.abs(xf).max(axis=1)
+    want_xs = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(xs.view(np.uint32), want_xs.view(np.uint32))
+    t = (xf / xs[:, None]).astype(np.float32).astype(np.float64)
+    nz = np.abs(t) >= 2.0 ** -12
+    assert np.array_equal(q[nz], _nearest_e4m3_brute(t[nz]))
+    assert np.all((q[~nz] & 0x7f) == 0)
+    dec = oracle.e4m3_to_float(q)
+    for m in range(M):
+        if m == 3:
+            assert xs[m] == 1.0 and np.all((q[m] & 0x7f) == 0)
+        else:
+            assert np.abs(dec[m]).max() == 448.0  # the row's absmax lands exactly on Q_MAX
+    assert _e4m3_error_ok(q, xf, xs[:, None])
+
+
 def test_add_qrmsnorm_fp8_residual_sum():
     M, K = 5, 256
     X = inputs.activations(M, K, seed=43)
