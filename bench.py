@@ -577,6 +577,14 @@ def run_sweep(args):
 
                     sec = timed(norms, 24, 20)
                     emit("a4_qrmsnorm_quant_i8", f"M{M}K{K}", sec, qrmsnorm_bytes(M, K), 0, "hbm")
+
+                    # per_token_quant_int8 of a plain activation (no norm): 2MK in, MK + 4M out
+                    def ptq(X=X, q=q, xs=xs):
+                        for _ in range(24):
+                            wql.per_token_quant_i8(X, q=q, xs=xs)
+
+                    sec = timed(ptq, 24, 20)
+                    emit("a4b_per_token_quant_i8", f"M{M}K{K}", sec, 3 * M * K + 4 * M, 0, "hbm")
                 stack = [qW] + [qW.clone() for _ in range(copies - 1)]
                 wsp = torch.empty((max(1, wql.w8a8_workspace_bytes(M, K, N)),), dtype=torch.uint8, device=dev)
 

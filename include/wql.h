@@ -169,6 +169,21 @@ wql_status wql_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* residual
                                      uint16_t* residual_out, int8_t* q, float* xs, void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * per_token_quant_i8 / per_token_quant_fp8  [W8A8] per_token_quant_int8, the quantiser
+ * QLinear.forward applies when its input is a plain tensor rather than QRMSNorm's output.
+ * Per row m of x [M, K] fp16, with x_k the fp16 value widened to fp32:
+ *     xs_m = max_k |x_k| / Q_MAX    (Q_MAX = 127 for int8, 448 for e4m3; 1.0 if the row is zero)
+ *     q_mk = clamp(round_half_even(x_k / xs_m), -128, 127)     (int8)
+ *     q_mk = e4m3(x_k / xs_m)       (fp8: the e4m3 value nearest the fp32 quotient, ties to even)
+ * Outputs q [M, K] (int8, or e4m3 bytes) and xs [M] fp32, bit-exact with the definition above;
+ * (q, xs) feed wql_w8a8_gemm / wql_w8a8_gemm_fp8 as QRMSNorm's outputs do.
+ * Requires K % 8 == 0, 8 <= K <= 16384 (WQL_EUNSUPPORTED above); x and q 16-byte aligned, xs
+ * 4-byte aligned.
+ * ---------------------------------------------------------------------------------------- */
+wql_status wql_per_token_quant_i8(const uint16_t* x, int M, int K, int8_t* q, float* xs, void* stream);
+wql_status wql_per_token_quant_fp8(const uint16_t* x, int M, int K, uint8_t* q, float* xs, void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * w8a8_gemm  [W8A8] QLinear.forward / matmul_kernel_dynamic_quant.
  *     acc[m, n] = sum_k q[m, k] * qw[n, k]                 (exact int32)
  *     y[m, n]   = fp16((float(acc[m, n]) * xs[m]) * ws[n])  (fp32, left to right)

@@ -20,6 +20,8 @@ from ._lib import (  # noqa: F401
     load,
     per_channel_quant_fp8,
     per_channel_quant_i8,
+    per_token_quant_fp8,
+    per_token_quant_i8,
     qrmsnorm_quant_fp8,
     qrmsnorm_quant_i8,
     smooth,
@@ -35,7 +37,8 @@ from ._lib import (  # noqa: F401
 
 __all__ = [
     "E4M3", "WQLError", "act_absmax", "add_qrmsnorm_quant_fp8", "add_qrmsnorm_quant_i8", "awq_pack", "device_status",
-    "diag_expire_wait", "interleave_gate_up", "kv_dequant_i8", "kv_quant_i8", "load", "per_channel_quant_fp8", "per_channel_quant_i8", "qrmsnorm_quant_fp8", "qrmsnorm_quant_i8", "smooth",
+    "diag_expire_wait", "interleave_gate_up", "kv_dequant_i8", "kv_quant_i8", "load", "per_channel_quant_fp8", "per_channel_quant_i8",
+    "per_token_quant_fp8", "per_token_quant_i8", "qrmsnorm_quant_fp8", "qrmsnorm_quant_i8", "smooth",
     "w4a16_gemm", "w4a16_gemm_silu_mul", "w4a16_kernel_for", "w8a8_gemm", "w8a8_gemm_fp8", "w8a8_gemm_fused", "w8a8_gemm_noalloc",
     "w8a8_workspace_bytes",
 ]

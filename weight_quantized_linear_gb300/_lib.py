@@ -36,6 +36,8 @@ SIGNATURES = {
     "wql_w4a16_gemm_silu_mul": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_add_qrmsnorm_quant_i8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
+    "wql_per_token_quant_i8": (_I, [_P, _I, _I, _P, _P, _P]),
+    "wql_per_token_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "wql_w8a8_workspace_bytes": (_SZ, [_I, _I, _I]),
     "wql_w8a8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "wql_w8a8_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
@@ -190,6 +192,35 @@ def qrmsnorm_quant_i8(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
     _need(xs, "xs", torch.float32, (M,))
     _check(load().wql_qrmsnorm_quant_i8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q), _ptr(xs), _stream(x.device)),
            "wql_qrmsnorm_quant_i8")
+    return q, xs
+
+
+def per_token_quant_i8(x: torch.Tensor, q: torch.Tensor | None = None, xs: torch.Tensor | None = None):
+    """x [M, K] fp16 -> (q int8 [M, K], xs fp32 [M]): per-token int8 of the row itself (no norm)."""
+    M, K = x.shape
+    _need(x, "x", torch.float16, (M, K))
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(q, "q", torch.int8, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _check(load().wql_per_token_quant_i8(_ptr(x), M, K, _ptr(q), _ptr(xs), _stream(x.device)), "wql_per_token_quant_i8")
+    return q, xs
+
+
+def per_token_quant_fp8(x: torch.Tensor, q: torch.Tensor | None = None, xs: torch.Tensor | None = None):
+    """x [M, K] fp16 -> (q float8_e4m3fn [M, K], xs fp32 [M]) with xs = absmax / 448."""
+    M, K = x.shape
+    _need(x, "x", torch.float16, (M, K))
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(q, "q", torch.float8_e4m3fn, (M, K))
+    _need(xs, "xs", torch.float32, (M,))
+    _check(load().wql_per_token_quant_fp8(_ptr(x), M, K, _ptr(q), _ptr(xs), _stream(x.device)),
+           "wql_per_token_quant_fp8")
     return q, xs
 
 

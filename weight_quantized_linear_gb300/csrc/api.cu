@@ -233,6 +233,35 @@ wql_status norm_args(const uint16_t* x, const uint16_t* gamma, int M, int K, con
 
 }  // namespace
 
+namespace {
+
+wql_status per_token_quant(const char* fn, const uint16_t* x, int M, int K, bool fp8, uint8_t* q, float* xs,
+                           void* stream) {
+  WQL_REQUIRE(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8");
+  WQL_REQUIRE(M >= 0, "M must be >= 0");
+  if (K > 16384) return fail(WQL_EUNSUPPORTED, "K > 16384 is not supported by the register-resident row kernel");
+  if (M == 0) {
+    g_last_error.clear();
+    return WQL_OK;
+  }
+  WQL_REQUIRE_PTR(x);
+  WQL_REQUIRE_PTR(q);
+  WQL_REQUIRE(xs != nullptr && (reinterpret_cast<uintptr_t>(xs) & 3u) == 0, "xs must be a 4-byte aligned device pointer");
+  return cuda_status(wql::launch_per_token_quant(x, M, K, fp8, q, xs, device_error_word(),
+                                                 static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+}  // namespace
+
+wql_status wql_per_token_quant_i8(const uint16_t* x, int M, int K, int8_t* q, float* xs, void* stream) {
+  return per_token_quant("wql_per_token_quant_i8", x, M, K, false, reinterpret_cast<uint8_t*>(q), xs, stream);
+}
+
+wql_status wql_per_token_quant_fp8(const uint16_t* x, int M, int K, uint8_t* q, float* xs, void* stream) {
+  return per_token_quant("wql_per_token_quant_fp8", x, M, K, true, q, xs, stream);
+}
+
 wql_status wql_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, uint8_t* q,
                                   float* xs, void* stream) {
   const wql_status st = norm_args(x, gamma, M, K, q, xs, false, nullptr, nullptr);

@@ -73,6 +73,10 @@ cudaError_t launch_add_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* resi
                                          float eps, int M, int K, uint16_t* residual_out, int8_t* q, float* xs,
                                          unsigned* dev_err, cudaStream_t s);
 
+// per_token_quant of plain fp16 rows: xs = absmax / 127 (int8) or / 448 (fp8), q the codes of x / xs.
+cudaError_t launch_per_token_quant(const uint16_t* x, int M, int K, bool fp8, uint8_t* q, float* xs, unsigned* dev_err,
+                                   cudaStream_t s);
+
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
                               float* absmax, unsigned* dev_err, cudaStream_t s);
 

@@ -1,5 +1,5 @@
-// norm.cu -- QRMSNorm fused with per-token dynamic int8 or fp8 quantisation, and the calibration
-// statistic used by weight smoothing ("LMDeploy W8A8 quantisation guide": QRMSNorm.forward,
+// norm.cu -- QRMSNorm fused with per-token dynamic int8 or fp8 quantisation, the same per-token
+// quantisation of a row without the norm, and the calibration statistic used by weight smoothing ("LMDeploy W8A8 quantisation guide": QRMSNorm.forward,
 // rms_norm_dynamic_quant, per_token_quant_int8 with scale = absmax / Q_MAX; int8 codes are rounded
 // to integers (Q_MAX = 127), fp8 codes are the e4m3 cast (Q_MAX = 448); smoothing statistics are
 // the per-channel absmax of the norm output).
@@ -42,9 +42,11 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
 }
 
 // Modes of the row kernel: 0 int8 codes, 1 per-channel absmax (atomic max into absmax), 2 residual
-// add then int8 codes, 3 fp8 codes, 4 residual add then fp8 codes.
+// add then int8 codes, 3 fp8 codes, 4 residual add then fp8 codes, 5 int8 and 6 fp8 codes of the row
+// itself (per_token_quant: no normalisation, no gamma).
 __host__ __device__ constexpr bool mode_residual(int mode) { return mode == 2 || mode == 4; }
-__host__ __device__ constexpr bool mode_fp8(int mode) { return mode == 3 || mode == 4; }
+__host__ __device__ constexpr bool mode_fp8(int mode) { return mode == 3 || mode == 4 || mode == 6; }
+__host__ __device__ constexpr bool mode_no_norm(int mode) { return mode == 5 || mode == 6; }
 
 // Rows in flight per CTA: four, or three when each slot holds two long rows (residual, K > 8192).
 __host__ __device__ constexpr int norm_slots(int cpt, int mode) { return (mode_residual(mode) && cpt > 4) ? 3 : 4; }
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) 
                     __half* h_out, unsigned* err) {
   constexpr int kNormSlots = norm_slots(CPT, MODE), kRowsPerSlot = norm_rows_per_slot(MODE);
   constexpr bool kResid = mode_residual(MODE);
+  constexpr bool kNorm = !mode_no_norm(MODE);
   __shared__ float red[272];  // [0, 256) lane partials, 256 row sum, [264, 272) warp maxima
   __shared__ __align__(8) uint64_t full[kNormSlots];
   extern __shared__ __align__(16) uint8_t rows[];  // kNormSlots x kRowsPerSlot x 2K bytes
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) 
 #pragma unroll
   for (int i = 0; i < CPT; ++i) {
     const int c = tid + kNormThreads * i;
-    if (c < nchunks) {
+    if (kNorm && c < nchunks) {
       const uint4 gv = __ldg(gr + c);
       const __half* gh = reinterpret_cast<const __half*>(&gv);
 #pragma unroll
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) 
         for (int e = 0; e < 8; ++e) {
           const float v = __half2float(h[e]);
           yv[i][e] = v;
-          p = __fadd_rn(p, __fmul_rn(v, v));
+          if constexpr (kNorm) p = __fadd_rn(p, __fmul_rn(v, v));
         }
       }
     }
@@ -183,19 +186,29 @@ __global__ void __launch_bounds__(kNormThreads, CPT <= 2 ? (mode_residual(MODE) 
         if (c < nchunks) *reinterpret_cast<uint4*>(h_out + (size_t)m * K + 8 * c) = hv[i];
       }
     }
-    const float mean = __fdiv_rn(ss, (float)K);
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-
     float amax = 0.f;
+    if constexpr (kNorm) {
+      const float mean = __fdiv_rn(ss, (float)K);
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      const int c = tid + kNormThreads * i;
-      if (c < nchunks) {
+      for (int i = 0; i < CPT; ++i) {
+        const int c = tid + kNormThreads * i;
+        if (c < nchunks) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float yy = __fmul_rn(__fmul_rn(yv[i][e], r), gf[i][e]);
-          yv[i][e] = yy;
-          amax = fmaxf(amax, fabsf(yy));
+          for (int e = 0; e < 8; ++e) {
+            const float yy = __fmul_rn(__fmul_rn(yv[i][e], r), gf[i][e]);
+            yv[i][e] = yy;
+            amax = fmaxf(amax, fabsf(yy));
+          }
+        }
+      }
+    } else {  // per-token quantisation of the row itself
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = tid + kNormThreads * i;
+        if (c < nchunks) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(yv[i][e]));
         }
       }
     }
@@ -338,6 +351,12 @@ cudaError_t launch_qrmsnorm_quant_fp8(const uint16_t* x, const uint16_t* residua
                                       cudaStream_t s) {
   if (residual) return launch_norm<4>(x, residual, gamma, eps, M, K, q, xs, nullptr, residual_out, dev_err, s);
   return launch_norm<3>(x, nullptr, gamma, eps, M, K, q, xs, nullptr, nullptr, dev_err, s);
+}
+
+cudaError_t launch_per_token_quant(const uint16_t* x, int M, int K, bool fp8, uint8_t* q, float* xs, unsigned* dev_err,
+                                   cudaStream_t s) {
+  if (fp8) return launch_norm<6>(x, nullptr, nullptr, 0.f, M, K, q, xs, nullptr, nullptr, dev_err, s);
+  return launch_norm<5>(x, nullptr, nullptr, 0.f, M, K, q, xs, nullptr, nullptr, dev_err, s);
 }
 
 cudaError_t launch_act_absmax(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, float* absmax,
