@@ -309,6 +309,105 @@ def time_replays(torch, graph, n, stream):
     return e0.elapsed_time(e1) / 1e3
 
 
+def metric_cases(torch, wql, dev, stream, hbm, bf16, l2):
+    """The rest of the metric, timed after the headline step on the same GPU: the W4A16 prefill cells
+    (M in {512, 2048, 8192} x N in {4096, 11008}, K = 4096, G = 128, 1% x20 activation channels), the
+    Llama-7B layer sweep at G = 128 (fused QKV 4096x12288, gate_up 4096x22016, down 11008x4096;
+    M in {1, 8, 32, 128, 256}) and the SmoothQuant W8A8 block (K = 4096, N in {4096, 11008},
+    M in {1, 16, 512, 4096}: the int8 GEMM alone and QRMSNorm + GEMM).  Each case is a CUDA graph of
+    calls over enough distinct weight copies to exceed 3x L2; the per-call time is reported against
+    the roofline that bounds it (the larger of the HBM time of its algorithmic bytes and the tensor
+    time of its flops at the measured bf16 peak; int8 runs as exact fp16 on the tensor cores)."""
+    import numpy as np
+    from weight_quantized_linear_gb300 import inputs
+
+    def timed(fn, copies, reps):
+        g = capture(torch, fn, stream)
+        g.replay()
+        torch.cuda.synchronize()
+        t = time_replays(torch, g, reps, stream)
+        del g
+        return t / (reps * copies)
+
+    def record(cfg, op, M, K, N, G, sec, nbytes, flops, extra=None):
+        t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (bf16 * 1e12)
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        gbs, tfs = nbytes / sec / 1e9, flops / sec / 1e12
+        rec = {"config": cfg, "op": op, "M": M, "K": K, "N": N, "us": round(sec * 1e6, 3), "GB_s": round(gbs, 1),
+               "TFLOP_s": round(tfs, 2), "bound": bound, "frac": round(gbs / hbm if bound == "hbm" else tfs / bf16, 4)}
+        if G:
+            rec["G"] = G
+        if extra:
+            rec.update(extra)
+        return rec
+
+    cases = []
+    G = 128
+    # W4A16: prefill cells and the layer sweep at G = 128
+    w4 = [("prefill", M, 4096, N, False, True) for M in (512, 2048, 8192) for N in (4096, 11008)]
+    w4 += [("layer sweep", M, K, N, True, False) for (K, N) in ((4096, 12288), (4096, 22016), (11008, 4096))
+           for M in (1, 8, 32, 128, 256)]
+    packed = {}
+    for cfg, M, K, N, w_out, x_out in w4:
+        key = (K, N, w_out)
+        if key not in packed:
+            packed.clear()
+            W = torch.from_numpy(inputs.weight(K, N, seed=0, outliers=w_out)).to(dev)
+            qw, sc, qz = wql.awq_pack(W, G)
+            del W
+            copies = int(max(2, min(64, -(-3 * l2 // w4a16_bytes(0, K, N, G)))))
+            packed[key] = [(qw, sc, qz)] + [(qw.clone(), sc.clone(), qz.clone()) for _ in range(copies - 1)]
+        stack = packed[key]
+        x = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=x_out)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+
+        def fn(stack=stack, x=x, y=y):
+            for (a, b, z) in stack:
+                wql.w4a16_gemm(x, a, b, z, G, out=y)
+
+        flops = gemm_flops(M, K, N)
+        sec = timed(fn, len(stack), 20 if flops * len(stack) < 5e12 else 3)
+        kern = "tcgen05" if wql.w4a16_kernel_for(M, K, N) == "prefill" else "decode"
+        cases.append(record(cfg, "w4a16_gemm", M, K, N, G, sec, w4a16_bytes(M, K, N, G), flops, {"kernel": kern}))
+        del x, y
+    packed.clear()
+    # W8A8 SmoothQuant block: smoothing and quantisation on the GPU, then the GEMM and the block
+    K = 4096
+    for N in (4096, 11008):
+        W = torch.from_numpy(inputs.weight(K, N, seed=0)).to(dev)
+        copies = int(max(2, min(64, -(-3 * l2 // (N * K)))))
+        for M in (1, 16, 512, 4096):
+            X = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
+            g = torch.from_numpy(inputs.gamma(K, seed=0)).to(dev)
+            a = wql.act_absmax(X, g, inputs.EPS)
+            _, g2, W2 = wql.smooth(a, g, W)
+            qW, ws = wql.per_channel_quant_i8(W2)
+            q, xs = wql.qrmsnorm_quant_i8(X, g2, inputs.EPS)
+            stack = [qW] + [qW.clone() for _ in range(copies - 1)]
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            wsp = torch.empty((max(1, wql.w8a8_workspace_bytes(M, K, N)),), dtype=torch.uint8, device=dev)
+
+            def gemm(stack=stack, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
+                for w in stack:
+                    wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
+
+            def block(stack=stack, X=X, g2=g2, q=q, xs=xs, ws=ws, y=y, wsp=wsp):
+                for w in stack:
+                    wql.qrmsnorm_quant_i8(X, g2, inputs.EPS, q=q, xs=xs)
+                    wql.w8a8_gemm(q, xs, w, ws, out=y, workspace=wsp)
+
+            flops = gemm_flops(M, K, N)
+            reps = 20 if flops * copies < 5e12 else 3
+            note = {"tensor_peak_note": "exact int8 on fp16 tcgen05 (kind::i8 is absent on sm_103a); peak = measured bf16"}
+            cases.append(record("w8a8 block", "w8a8_gemm", M, K, N, 0, timed(gemm, copies, reps),
+                                w8a8_bytes(M, K, N), flops, note if M > 16 else None))
+            cases.append(record("w8a8 block", "qrmsnorm_quant_i8+w8a8_gemm", M, K, N, 0, timed(block, copies, reps),
+                                qrmsnorm_bytes(M, K) + w8a8_bytes(M, K, N), flops, note if M > 16 else None))
+            del stack, y, wsp, q, xs, qW, ws, X, g, a, g2, W2
+        del W
+    return cases
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -375,10 +474,14 @@ def run_gpu(args):
         t = time_replays(torch, g, reps, stream)
         per_launch = t / (reps * layers)
         b = w4a16_bytes(m, DECODE_K, DECODE_N, DECODE_G)
-        cases.append({"M": m, "us_per_launch": round(per_launch * 1e6, 3),
-                      "GB_s": round(b / per_launch / 1e9, 1), "TFLOP_s": round(gemm_flops(m, DECODE_K, DECODE_N) / per_launch / 1e12, 2),
-                      "frac_hbm": round(b / per_launch / 1e9 / hbm, 4)})
+        cases.append({"config": "decode", "op": "w4a16_gemm", "M": m, "K": DECODE_K, "N": DECODE_N, "G": DECODE_G,
+                      "us": round(per_launch * 1e6, 3), "GB_s": round(b / per_launch / 1e9, 1),
+                      "TFLOP_s": round(gemm_flops(m, DECODE_K, DECODE_N) / per_launch / 1e12, 2), "bound": "hbm",
+                      "frac": round(b / per_launch / 1e9 / hbm, 4), "kernel": "decode"})
         del g
+
+    # the other configurations of the metric (prefill, layer sweep, W8A8 block), timed on this GPU
+    more_cases = [] if args.no_extra_cases else metric_cases(torch, wql, dev, stream, hbm, bf16, l2_bytes(torch, dev))
 
     # End to end through the public call, as a serving engine replays a decode step: one CUDA graph
     # per step holds the copy of each M's activations in from pinned host memory, the 48 layers
@@ -446,7 +549,7 @@ def run_gpu(args):
                            "last layer's y out; host waits each step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clock_info,
-            "cases": cases,
+            "cases": cases + more_cases,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -806,6 +909,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-cases", action="store_true",
+                    help="skip the prefill / layer-sweep / W8A8 cases that follow the headline timing")
     ap.add_argument("--sweep", default=None, help="measure every hot-path row; JSON lines to this file")
     ap.add_argument("--profile-case", default=None,
                     help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N[,1] | fp8:M,K,N[,1] | "
