@@ -15,8 +15,8 @@
 //     reduced by a single warp).  They feed the legacy
 //     mma.sync.m16n8k16 tensor-core path with the weights as the 16-row operand and the tokens as
 //     the 8-column operand ("swap AB").  The int4 codes enter the MMA as the exact fp16 values
-//     1024 + q (or 1024 + 16 q): one PRMT pairs rows k and k+1, one LOP3 per two weights splices
-//     the nibbles into the fp16 bit pattern.  Offset, zero point and scale are applied once per
+//     1024 + q (or 1024 + 16 q): a transposed ldmatrix pairs rows k and k+1 of the packed tile in
+//     one register, one LOP3 per two weights splices the nibbles into the fp16 bit pattern.  Offset, zero point and scale are applied once per
 //     group to the fp32 partial sums:
 //         sum_k (q - z) x = D - (1024 + z) sum_k x       (D = sum_k (1024 + q) x)
 //         sum_k (q - z) x = D / 16 - (64 + z) sum_k x    (D = sum_k (1024 + 16 q) x)
@@ -110,12 +110,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Byte offset of packed word j (0..15) of row r in a TMA tile with 64-byte rows and the 64B swizzle
-// (16-byte chunk index XOR bits 1..2 of the row).
-__device__ __forceinline__ uint32_t wtile_off(int r, int j) {
-  return r * 64 + ((((j >> 2) ^ (r >> 1)) & 3) << 4) + (j & 3) * 4;
-}
-
 // The four f16x2 MMA operands held in the nibbles of T: columns 0 and 2 as 1024 + q, columns 1 and
 // 3 as 1024 + 16 q (both exact).
 __device__ __forceinline__ void splice4(uint32_t T, uint32_t out[4]) {
@@ -128,7 +122,7 @@ __device__ __forceinline__ void splice4(uint32_t T, uint32_t out[4]) {
 }
 
 template <int MT, int LG>
-__global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
+__global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
     w4a16_decode_kernel(const __grid_constant__ CUtensorMap tm_x,   // x: 3D {64, M, K/64} box {64, 8MT, 2}, or
                                                                     //    2D {K, M} box {64, 8MT} (x3d == 0)
                         const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8], box {16, 128}, SW64
@@ -177,7 +171,6 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
 
   const int cg = warp & 1, kq = warp >> 1;
   const int g = lane >> 2, t = lane & 3;
-  const int wc = cg * 8 + g;  // packed word column within the strip
 
   if (warp == kConsumerWarps) {
     // ---------------- producer: one thread issues every TMA copy ----------------
@@ -247,14 +240,17 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) tot[j][mt][i] = 0.f;
-    const uint32_t sel_lo = (t & 1) ? 0x1054u : 0x5410u;
-    const uint32_t sel_hi = (t & 1) ? 0x3276u : 0x7632u;
     const uint32_t kOnes[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
-    // rows 2t, 2t+1, 2t+8, 2t+9 of k16 step 0, ordered so that the four t lanes hit distinct banks;
-    // step u sits 16 rows = 1024 bytes further
-    const int ra = 2 * t + (t & 1), rb = 2 * t + 1 - (t & 1);
-    const uint32_t offa = wtile_off(ra, wc), offb = wtile_off(rb, wc);
-    const uint32_t offc = wtile_off(ra + 8, wc), offd = wtile_off(rb + 8, wc);
+    // The packed tile's rows are k (64 bytes = 16 words = 128 columns, 64B swizzle: the 16-byte chunk
+    // index is XORed with bits 1..2 of the row).  One transposed ldmatrix per k16 step loads four
+    // 8 x 8 b16 matrices: lane 4g + t receives half-word g of a 16-byte chunk (four codes, columns
+    // 4g .. 4g + 3 of the chunk's 32) for k rows 2t and 2t + 1 -- the row pairing the MMA's A
+    // fragment wants.  Matrices: (k 0-7, chunk 2cg), (k 0-7, chunk 2cg + 1), (k 8-15, chunk 2cg),
+    // (k 8-15, chunk 2cg + 1).  Row address of this lane for step 0; step u sits 16 rows further.
+    const int mi = lane >> 3, wr = 8 * (mi >> 1) + (lane & 7);
+    const uint32_t woff = wr * 64 + ((((2 * cg + (mi & 1)) ^ (wr >> 1)) & 3) << 4);
+    // MMA row g holds column c0 + j of MMA j, row g + 8 column c0 + 32 + j
+    const int c0 = 64 * cg + 4 * g;
     // ldmatrix row addresses for chunk pair u2 (k16 step) within one activation slab (128-byte rows,
     // 128B swizzle); matrices: (tokens 0-7, chunks 2u2, 2u2+1), then the next token tile
     uint32_t xoff[4][(MT + 1) / 2];
@@ -294,13 +290,13 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
             else
               ldmatrix_x2(xt + hb * L::kSlab + xoff[u2][p], bx[2 * p][0], bx[2 * p][1]);
           }
-          const uint32_t w0 = lds_u32(wt + u * 1024 + offa), w1 = lds_u32(wt + u * 1024 + offb);
-          const uint32_t w2 = lds_u32(wt + u * 1024 + offc), w3 = lds_u32(wt + u * 1024 + offd);
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(wt + u * 1024 + woff, r0, r1, r2, r3);
           uint32_t lo[4], hi[4], lo2[4], hi2[4];
-          splice4(prmt(w0, w1, sel_lo), lo);
-          splice4(prmt(w0, w1, sel_hi), hi);
-          splice4(prmt(w2, w3, sel_lo), lo2);
-          splice4(prmt(w2, w3, sel_hi), hi2);
+          splice4(r0, lo);
+          splice4(r1, hi);
+          splice4(r2, lo2);
+          splice4(r3, hi2);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t a[4] = {lo[j], hi[j], lo2[j], hi2[j]};
@@ -317,22 +313,24 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
           }
         }
         // group epilogue: tot += ca * acc - cb * sx per column
-        const uint32_t zw = lds_u32(zbase + gi * (kStripWords * 4) + wc * 4);
-        const uint4 sv = lds_u128(sbase + gi * (kStripCols * 2) + wc * 16);
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+        // coefficients of column c0 + 32 h + j at [j + 4 h]: its zero point is nibble 4 (g & 1) + j of
+        // packed word (c0 + 32 h) / 8, its scale the fp16 at column c0 + 32 h
         float ca[8], cb[8];
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[c2]));
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t zw = lds_u32(zbase + gi * (kStripWords * 4) + ((c0 + 32 * h) >> 3) * 4) >> (16 * (g & 1));
+          const uint2 sv = lds_u64(sbase + gi * (kStripCols * 2) + (c0 + 32 * h) * 2);
+          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
+          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+          const float sc4[4] = {f01.x, f01.y, f23.x, f23.y};
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = 2 * c2 + e;
-            const float sc = e ? f.y : f.x;
-            // 1024 + z (even columns) or 64 + z (odd columns) built directly as fp32 bit patterns
-            const uint32_t zb = (cc & 1) ? (0x42800000u | (((zw >> (4 * cc)) & 15u) << 17))
-                                         : (0x44800000u | (((zw >> (4 * cc)) & 15u) << 13));
-            ca[cc] = (cc & 1) ? sc * 0.0625f : sc;
-            cb[cc] = sc * __uint_as_float(zb);
+          for (int j = 0; j < 4; ++j) {
+            // 1024 + z (j even: codes entered as 1024 + q) or 64 + z (j odd: 1024 + 16 q), built
+            // directly as fp32 bit patterns
+            const uint32_t z = (zw >> (4 * j)) & 15u;
+            const uint32_t zb = (j & 1) ? (0x42800000u | (z << 17)) : (0x44800000u | (z << 13));
+            ca[j + 4 * h] = (j & 1) ? sc4[j] * 0.0625f : sc4[j];
+            cb[j + 4 * h] = sc4[j] * __uint_as_float(zb);
           }
         }
 #pragma unroll
@@ -365,7 +363,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, MT <= 1 ? 2 : 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = 8 * mt + 2 * t + (e & 1);
-        const int col = 8 * wc + 4 * (e >> 1);
+        const int col = c0 + 32 * (e >> 1);
         stage4[kq * L::kNQ + ((row * kStripCols + col) >> 2)] =
             make_float4(tot[0][mt][e], tot[1][mt][e], tot[2][mt][e], tot[3][mt][e]);
       }
