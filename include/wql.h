@@ -35,6 +35,9 @@
  *     they then record a device-side error that wql_device_status() returns as WQL_ETIMEOUT.
  *   - M = 0 is a valid empty call: it returns WQL_OK and launches nothing.
  *   - The library holds no per-call state; calls on different streams may run concurrently.
+ *     It keeps per-device state for the life of the process (kernel attributes, the device
+ *     error word's address, the scratch-free GEMM's array address).  cudaDeviceReset
+ *     invalidates that state: no call may follow a reset of that device in the same process.
  *   - Weight prefetch (programmatic dependent launch): the W4A16 GEMMs and the decode path of the
  *     W8A8 GEMMs (int8 and fp8, up to 16 tokens) are launched so that they may start while the
  *     kernel enqueued just before them on the stream is still running, and they begin copying
@@ -225,7 +228,9 @@ wql_status wql_w8a8_gemm_fused(const int8_t* q, const float* xs, const int8_t* q
  *     WQL_EUNSUPPORTED with a message in wql_last_error() and launch nothing;
  *   - one array per GPU that loads the library, held until the process exits;
  *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture;
+ *     with that device current) and keeps it; make that first call before any stream capture.
+ *     cudaDeviceReset invalidates the kept address: no call may follow a reset of that device
+ *     in the same process;
  *   - every call on a device shares the one array.  Calls that may overlap on the GPU (other
  *     streams, other threads) race on it and must be serialised by the caller.  Nothing in it
  *     needs to start at zero: each call overwrites every byte it later reads.

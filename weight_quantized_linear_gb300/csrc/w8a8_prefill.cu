@@ -12,8 +12,9 @@
 //     weight rows are K-contiguous, so its 64 codes are four 16-byte shared-memory loads (the tile
 //     arrives with a 128-byte swizzle, which spreads a warp's rows over all banks).  Keeping the
 //     fp16 operand out of shared memory removes two thirds of the shared-memory traffic per stage;
-//   * exactness: products are at most 128 * 127 < 2^14 and each accumulator covers at most 1024 k,
-//     so every partial sum is an integer below 2^24 that fp32 holds exactly.  The MMA thread
+//   * exactness: |product| <= 128 * 128 = 2^14 (both codes may be -128) and each accumulator covers
+//     at most 1024 k, so every partial sum is an integer of magnitude <= 2^24 that fp32 holds
+//     exactly.  The MMA thread
 //     alternates two TMEM chunk accumulators; the epilogue warps turn each finished chunk into
 //     int32 and add it to an int32 running sum kept in TMEM, so the MMAs never wait for them.
 //     The tile's last chunk yields acc (written to acc_out if requested) and
