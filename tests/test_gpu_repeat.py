@@ -34,16 +34,20 @@ def _repeat(fn, out):
     return bad
 
 
-# tcgen05 W4A16: 64-token tiles with split-K (few tiles), 128-token tiles, 256-token tiles
-@pytest.mark.parametrize("M,K,N", [(64, 4096, 1024), (512, 4096, 4096), (2048, 4096, 11008)])
+# tcgen05 W4A16: 64- and 128-token tiles with split-K (few tiles; the exchange through bulk copies
+# between the CTAs of a cluster), 128-token tiles, 256-token tiles (one accumulator: the epilogue
+# hands it back to the MMAs of the next tile), up to 18 tiles per persistent CTA
+@pytest.mark.parametrize("M,K,N", [(64, 4096, 1024), (128, 4096, 4096), (256, 11008, 4096), (512, 4096, 4096),
+                                   (2048, 4096, 11008), (8192, 4096, 11008)])
 def test_w4a16_prefill_repeatable(wql, M, K, N):
     G = 128
     qw, s, qz = wql.awq_pack(dev(inputs.weight(K, N, seed=N, outliers=True)), G)
     x = dev(inputs.activations(M, K, seed=M, outlier_channels=True))
-    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
     assert wql.w4a16_kernel_for(M, K, N) == "prefill"
     bad = _repeat(lambda: wql.w4a16_gemm(x, qw, s, qz, G, out=y), y)
     assert bad == 0, f"{bad} of {REPS} calls differ"
+    assert bool(torch.isfinite(y).all())
     wql.device_status()
 
 

@@ -184,6 +184,17 @@ __device__ __forceinline__ void st_cluster_i4(uint32_t addr, int4 v) {
 
 // Asynchronous store of 16 bytes into a peer CTA's shared memory; its completion is counted as 16
 // transaction bytes on the peer's mbarrier (both addresses in the shared::cluster window).
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared
+// memory to the shared memory of a CTA of the cluster; completes transaction bytes on that CTA's
+// mbarrier.  Both remote addresses come from mapa.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   remote_dst),
+               "r"(local_src), "r"(bytes), "r"(remote_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                    remote_addr),

@@ -2,17 +2,19 @@
 //
 // y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n] ("LMDeploy ... INT4 quantisation"
 // tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  Tiles of 128 output
-// channels x BN tokens, K walked in blocks of 128 (64 for the widest tile), one ring of stages
-// [x tile | A | packed | s | z]:
-//   * warp 0, one thread: TMA copies of the activation tile (K-major, 128B swizzle), the packed
-//     weight tile, and its scale / zero-point rows;
+// channels x BN tokens (BN = 32, 64, 128 or 256), K walked in blocks of 128, one ring of stages
+// [x tile | packed | s | z]:
+//   * warps 0 and 14, one thread each: TMA copies of the packed weight tile with its scale /
+//     zero-point rows, and of the activation tile (K-major, 128B swizzle);
 //   * warps 2-9: dequantise the packed tile into the MMA's A operand, fp16 (q - z) * s (exact q - z
-//     via the 1024 + q bit-splice trick, one rounding for the scale).  Token tiles up to 128: into
-//     tensor memory with tcgen05.st, one channel per TMEM lane, so that shared memory carries only
-//     the activations and the packed weights; the widest tile: into an MN-major 128B-swizzled
-//     shared-memory layout, one 16-byte chunk per packed word (8 channels at one k);
+//     via the 1024 + q bit-splice trick, one rounding for the scale), written to tensor memory
+//     with tcgen05.st, one channel per TMEM lane, so that shared memory carries only the
+//     activations and the packed weights;
 //   * warp 1: allocates TMEM; one thread issues tcgen05.mma.kind::f16 (M = 128 channels,
-//     N = BN tokens, K = 16) into a double-buffered fp32 accumulator and commits stage releases;
+//     N = BN tokens, K = 16, A from TMEM) into an fp32 accumulator and commits stage releases.
+//     BN <= 128: two accumulators, so a tile's epilogue overlaps the next tile's MMAs; BN = 256:
+//     one accumulator (512 TMEM columns hold it and the A slots) and a three-stage ring, the N = 256
+//     MMAs carrying twice the work of the 128-token tile per issued instruction;
 //   * warps 10-13: tcgen05.ld the accumulator (lane = channel, column = token), round to fp16, store.
 // Swapping A and B puts the dequantised weights (not the activations) in the 128-row operand, so
 // the dequantisers write 128 x kBK fp16 per stage whatever the token count.
@@ -22,8 +24,9 @@
 //   * split-K (gridDim.y == S in {2, 4, 8}, clusters of S CTAs along y): when the tiles are fewer
 //     than half the SMs, the S CTAs of a cluster each take 1/S of K for one tile.  After their
 //     main loops they exchange partial sums through distributed shared memory (the stage ring is
-//     reused as the receive buffer): CTA r owns token columns [r BN/S, (r+1) BN/S) and adds the S
-//     partials in split order, so the result does not depend on timing.
+//     reused for the exchange buffers; one bulk copy per peer): CTA r owns token columns
+//     [r BN/S, (r+1) BN/S) and every warp then adds the S partials in split order, so the result
+//     does not depend on timing.
 // Launched with programmatic dependent launch: the packed weights of the first stages are
 // requested before waiting for the preceding kernel, whose output may be x.
 #include <atomic>
@@ -35,9 +38,7 @@
 namespace wql {
 namespace {
 
-// k per stage: 128 for token tiles up to 128 (eight MMAs per barrier round trip of the MMA thread),
-// 64 for the widest tile, whose stages would not fit twice in shared memory otherwise
-__host__ __device__ constexpr int bk_for(int bn) { return bn <= 128 ? 128 : 64; }
+constexpr int kBK = 128;         // k per stage: eight MMAs per barrier round trip of the MMA thread
 constexpr int kBM = 128;         // output channels per tile (MMA M)
 constexpr int kStripWords = 16;  // packed words per tile row
 // Warp 0 issues the weight copies and warp 14 the activation copies: copies issued by one thread
@@ -49,45 +50,45 @@ constexpr int kThreads = (kXProducerWarp + 1) * 32;
 template <int BN, int LG>
 struct PLayout {
   static constexpr int G = 1 << LG;
-  // Token tiles up to 128: the dequantised weights go straight to tensor memory (tcgen05.st) and the
-  // MMA reads its A operand there, so shared memory carries only the activations and packed
-  // weights.  The widest tile needs all 512 TMEM columns for its two accumulators and keeps A in
-  // shared memory.
-  static constexpr bool kTA = BN <= 128;
-  static constexpr int kBK = bk_for(BN);
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;
   static constexpr int kXBox = BN * 128;                 // BN token rows x 64 k fp16
   static constexpr int kXBoxes = kBK / 64;
   static constexpr int kXBytes = kXBoxes * kXBox;
-  static constexpr int kAAtom = kBK * 128;               // 64 channels x kBK k fp16, MN-major
-  static constexpr int kABytes = kTA ? 0 : 2 * kAAtom;   // kBK k rows x 128 channels fp16
   static constexpr int kWBytes = kBK * kStripWords * 4;  // kBK rows x 16 packed words
   static constexpr int kSBytes = kGR * kBM * 2;
   static constexpr int kZBytes = kGR * kStripWords * 4;
-  static constexpr int kOffA = kXBytes;                  // both 1024-aligned (the packed tile: 512)
-  static constexpr int kOffW = kOffA + kABytes;
+  static constexpr int kOffW = kXBytes;                  // 1024-aligned (the packed tile needs 512)
   static constexpr int kOffS = kOffW + kWBytes;
   static constexpr int kOffZ = kOffS + kSBytes;
   static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
-  // with A in TMEM, stage s also owns A slot s: the producers' wait for the stage to be free (the
-  // MMAs of the stage kStages earlier have completed) frees the slot too
-  static constexpr int kStages = 4;
+  // stage s also owns TMEM A slot s: the producers' wait for the stage to be free (the MMAs of the
+  // stage kStages earlier have completed) frees the slot too.  The widest tile has 72 KB stages:
+  // three fit in shared memory.
+  static constexpr int kStages = BN > 128 ? 3 : 4;
+  static constexpr int kAccBufs = BN > 128 ? 1 : 2;  // accumulators (with 2 the epilogue of a tile
+                                                     // overlaps the next tile's MMAs)
   static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
-  static constexpr int kBarBytes = (3 * kStages + 5) * 8 + 16;
+  static constexpr int kBarBytes = (3 * kStages + 6) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
-  static constexpr uint32_t kAColBase = 2 * BN;  // A slots (64 columns = 128 k each) after the accumulators
-  static constexpr uint32_t kTmemCols = kTA ? 512 : (2 * BN < 32 ? 32 : 2 * BN);
-  static_assert(!kTA || (kBK == 128 && kAColBase + 64 * kStages <= kTmemCols), "TMEM budget");
-  // split-K receive buffer (aliases the ring once every main loop of the cluster has ended):
-  // [source split][channel][BN / S + 4] fp32, largest for S = 8
-  static constexpr int kRecvBytesMax = 8 * kBM * (BN / 8 + 4) * 4;
-  static_assert(kRecvBytesMax <= kStages * kStage, "split-K receive buffer must fit in the ring");
+  static constexpr uint32_t kAColBase = kAccBufs * BN;  // A slots (64 columns = 128 k each) after the accumulators
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kAColBase + 64 * kStages <= kTmemCols, "TMEM budget");
+  // split-K exchange buffers (alias the ring once every main loop of the cluster has ended): a
+  // receive buffer [source split][channel][BN / S + 4] fp32 and a send buffer with the same chunks
+  // for the S - 1 other owners: 2 S - 1 chunks of kBM (BN / S + 4) fp32
+  static constexpr int exchange_bytes(int S) { return (2 * S - 1) * kBM * (BN / S + 4) * 4; }
+  static constexpr bool split_fits(int S) { return S == 1 || (BN / S >= 4 && exchange_bytes(S) <= kStages * kStage); }
+  static_assert(split_fits(2), "a two-way split must fit");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
+
+// The output channel (within the 128-channel tile) held by TMEM lane i: the dequantisers' stores put
+// channel 32 q + 4 g + e (g = 0..7, e = 0..3) in lane 32 q + 8 e + g.
+__device__ __forceinline__ int tmem_lane_channel(int i) { return 32 * (i >> 5) + 4 * (i & 7) + ((i >> 3) & 3); }
 
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                          int M, int N, int K, __half* __restrict__ y, int act, unsigned* err) {
   using L = PLayout<BN, LG>;
-  constexpr int kStages = L::kStages, kBK = L::kBK;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStage);
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accfull = afull + kStages;  // [2]
   uint64_t* accempty = accfull + 2;     // [2]
   uint64_t* finalbar = accempty + 2;    // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(finalbar + 1);
+  uint64_t* recvbar = finalbar + 1;     // [1] split-K: this CTA's receive buffer is complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvbar + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntn = (N + kBM - 1) / kBM;
@@ -134,15 +136,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 2);               // the weight and the activation producer
       mbar_init(&empty[s], 1);              // tcgen05.commit of the MMAs reading the stage
-      // A in TMEM: one arrival per dequantising warp; A in shared memory: every dequantising thread
-      mbar_init(&afull[s], L::kTA ? kDqWarps : kDqWarps * 32);
+      mbar_init(&afull[s], kDqWarps);       // one arrival per dequantising warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], kEpiWarps);
     }
     mbar_init(finalbar, 1);
+    mbar_init(recvbar, 1);
     fence_mbarrier_init();
+    // split-K: every other CTA of the cluster sends this CTA its partials of the token columns it
+    // owns, one bulk copy of kBM x (BN / S + 4) fp32 each
+    if (gridDim.y > 1)
+      mbar_arrive_expect_tx(recvbar, (uint32_t)((gridDim.y - 1) * kBM * (BN / gridDim.y + 4) * 4));
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, L::kTmemCols);
@@ -184,10 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * L::kStage;
           if (wprod) {
             mbar_arrive_expect_tx(&full[stage], L::kWTx);
-            if constexpr (L::kTA)  // rows k = 4a + b land at row 32 b + a of the tile
-              tma_load_3d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * (kBK / 4), 0);
-            else
-              tma_load_2d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * kBK);
+            // rows k = 4a + b land at row 32 b + a of the tile
+            tma_load_3d(st + L::kOffW, &tm_qw, &full[stage], nt * kStripWords, kb * (kBK / 4), 0);
             tma_load_2d(st + L::kOffS, &tm_s, &full[stage], nt * kBM, (kb * kBK) >> LG);
             tma_load_2d(st + L::kOffZ, &tm_z, &full[stage], nt * kStripWords, (kb * kBK) >> LG);
           } else {
@@ -215,22 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A MN-major (smem) or TMEM*/ L::kTA ? 0 : 1, /*B K-major*/ 0);
+      constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A from TMEM*/ 0, /*B K-major*/ 0);
       int stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-        const int b = it & 1;
-        if (!mbar_wait_bounded(&accempty[b], ((it >> 1) & 1) ^ 1)) {
+        const int b = it % L::kAccBufs;
+        if (!mbar_wait_bounded(&accempty[b], ((it / L::kAccBufs) & 1) ^ 1)) {
           report_error(err, kErrTimeoutMma);
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          // With A in TMEM the dequantisers wait for the stage's copies before they arrive on afull,
-          // so that wait also orders the x tile (one wait per stage: M = 64, N = 12288: 19.0 ->
-          // 18.0 us); the wider tile keeps both (measured neutral to slightly slower with one)
-          if (!mbar_wait_bounded(&afull[stage], phase) || (!L::kTA && !mbar_wait_bounded(&full[stage], phase))) {
+          // The dequantisers wait for the stage's copies before they arrive on afull, so that wait
+          // also orders the x tile (one wait per stage: M = 64, N = 12288: 19.0 -> 18.0 us)
+          if (!mbar_wait_bounded(&afull[stage], phase)) {
             report_error(err, kErrTimeoutMma);
             ok = false;
             break;
@@ -243,15 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < kBK / 16; ++s) {
             // B: 64-k boxes of K-major 128-byte rows, 8-row groups 1 KB apart; a k16 step is 32
-            // bytes along the row.  A in TMEM: slot `stage`, eight columns per k16 step.  A in
-            // shared memory: MN-major, 2 channel atoms of 64 (kAAtom apart), k groups of 8 rows
-            // 1 KB apart; a k16 step spans two k groups (2048 bytes).
+            // bytes along the row.  A: TMEM slot `stage`, eight columns per k16 step.
             const uint64_t bdesc = bdesc0 + (uint64_t)(((s >> 2) * L::kXBox + (s & 3) * 32) >> 4);
             const uint32_t acc = (kb != kb0 || s != 0) ? 1u : 0u;
-            if constexpr (L::kTA)
-              umma_f16_ta(d_tmem, tmem_base + L::kAColBase + stage * 64 + s * 8, bdesc, idesc, acc);
-            else
-              umma_f16(d_tmem, umma_sdesc_sw128(xs + L::kOffA + s * 2048, L::kAAtom, 1024), bdesc, idesc, acc);
+            umma_f16_ta(d_tmem, tmem_base + L::kAColBase + stage * 64 + s * 8, bdesc, idesc, acc);
           }
           umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == kStages) {
@@ -266,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(finalbar);
       if (!mbar_wait_bounded(finalbar, 0)) report_error(err, kErrTimeoutDrain);
     }
-  } else if (warp < kEpiWarp0 && L::kTA) {
+  } else if (warp < kEpiWarp0) {
     // ---------------- dequantisers: packed int4 -> fp16 A operand in TMEM ----------------
     // Warp w writes TMEM lane quarter q = w % 4 (channels 32 q ..) for k in [64 hk, 64 hk + 64) of
     // each stage.  Thread (g, c) = (lane / 4, lane % 4) takes packed word 4 q + g / 2, nibbles
@@ -350,85 +348,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < kEpiWarp0) {
-    // ---------------- dequantisers: packed int4 -> fp16 A operand in shared memory ----------------
-    const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
-    const int j = d & 15, r0 = d >> 4;          // packed word column, first row (rows r0 + 16 i)
-    const uint32_t aoff_col = (j >> 3) * L::kAAtom;
-    int stage = 0, phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase)) {
-          report_error(err, kErrTimeoutFull);
-          ok = false;
-          break;
-        }
-        const uint32_t st = smem_u32(smem + stage * L::kStage);
-        // per-group constants: -(1024+z) / -(64+z) pairs and (s_c, s_c+4) pairs in chunk order
-        uint32_t zc[L::kGR][4], sp[L::kGR][4];
-#pragma unroll
-        for (int gi = 0; gi < L::kGR; ++gi) {
-          const uint32_t zw = lds_u32(st + L::kOffZ + gi * (kStripWords * 4) + j * 4);
-          const uint32_t zw8 = zw >> 8;
-          zc[gi][0] = and_or(zw, 0x000F000Fu, 0xE400E400u);
-          zc[gi][1] = and_or(zw, 0x00F000F0u, 0xD400D400u);
-          zc[gi][2] = and_or(zw8, 0x000F000Fu, 0xE400E400u);
-          zc[gi][3] = and_or(zw8, 0x00F000F0u, 0xD400D400u);
-          const uint4 sv = lds_u128(st + L::kOffS + gi * (kBM * 2) + j * 16);
-          sp[gi][0] = prmt(sv.x, sv.z, 0x5410u);  // (s0, s4)
-          sp[gi][1] = prmt(sv.x, sv.z, 0x7632u);  // (s1, s5)
-          sp[gi][2] = prmt(sv.y, sv.w, 0x5410u);  // (s2, s6)
-          sp[gi][3] = prmt(sv.y, sv.w, 0x7632u);  // (s3, s7)
-        }
-#pragma unroll
-        for (int i = 0; i < kBK / 16; ++i) {
-          const int r = r0 + 16 * i;
-          // rows [16 i, 16 i + 16) lie in one quantisation group (G >= 32): a compile-time index
-          const int gi = L::kGR == 1 ? 0 : ((16 * i) >> LG);
-          const uint32_t w = lds_u32(st + L::kOffW + r * 64 + j * 4);
-          const uint32_t w8 = w >> 8;
-          const uint32_t kMagic = 0x64006400u, kSixteenth = 0x2C002C00u;
-          uint4 o;
-          o.x = hmul2_u32(hadd2_u32(and_or(w, 0x000F000Fu, kMagic), zc[gi][0]), sp[gi][0]);
-          o.y = hmul2_u32(hfma2_u32(and_or(w, 0x00F000F0u, kMagic), kSixteenth, zc[gi][1]), sp[gi][1]);
-          o.z = hmul2_u32(hadd2_u32(and_or(w8, 0x000F000Fu, kMagic), zc[gi][2]), sp[gi][2]);
-          o.w = hmul2_u32(hfma2_u32(and_or(w8, 0x00F000F0u, kMagic), kSixteenth, zc[gi][3]), sp[gi][3]);
-          const int rr = r & 7;
-          const uint32_t dst = st + L::kOffA + aoff_col + (r >> 3) * 1024 + rr * 128 + ((((j & 7) ^ rr)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                       : "memory");
-        }
-        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-        mbar_arrive(&afull[stage]);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: TMEM -> fp16 -> global ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int i = quad * 32 + lane;
-    // channel of TMEM lane i: A in TMEM, lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8; A in
-    // shared memory, rows follow the chunk order n0 n4 n1 n5 ...
-    const int col_in_tile = L::kTA ? 32 * (i >> 5) + 4 * (i & 7) + ((i >> 3) & 3)
-                                   : 8 * (i >> 3) + ((i & 7) >> 1) + 4 * (i & 1);
+    // channel of TMEM lane i: lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8
+    const int col_in_tile = tmem_lane_channel(i);
     // with the gate/up activation (act), channel pairs (2j, 2j + 1) meet in lanes differing in bit 3
-    // (A in TMEM) or bit 1 (A in shared memory).  The two lanes of a pair split the tokens: for
+    // (pair_mask).  The two lanes of a pair split the tokens: for
     // tokens k, k + 1 the even-channel lane computes output (k, j) from its gate and the partner's up,
     // the odd-channel lane output (k + 1, j) from the partner's gate and its own up -- one shuffle
     // carries both, and every lane evaluates the activation once per two tokens
-    const int pair_mask = L::kTA ? 8 : 2;
+    const int pair_mask = 8;
     const int NO = act ? N / 2 : N;  // output row length
     grid_dependency_wait();  // y may still be read by the preceding kernel
     if (S == 1) {
       int it = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int nt = tile % ntn, mt = tile / ntn;
-        const int b = it & 1;
-        if (!mbar_wait_warp(&accfull[b], (it >> 1) & 1)) {
+        const int b = it % L::kAccBufs;
+        if (!mbar_wait_warp(&accfull[b], (it / L::kAccBufs) & 1)) {
           report_error(err, kErrTimeoutMma);
           break;
         }
@@ -464,14 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
-      const int tile = blockIdx.x;
-      const int nt = tile % ntn, mt = tile / ntn;
       if (!mbar_wait_warp(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
       tc_fence_after_sync();
       const int CW = BN / S;       // token columns owned by each CTA of the cluster
-      const int rstride = CW + 4;  // floats per receive row (16 bytes of padding)
-      cluster_phase();             // (1) every main loop of the cluster is over: the ring is free
+      const int rstride = CW + 4;  // floats per exchange row (16 bytes of padding against bank conflicts)
+      const uint32_t chunk = (uint32_t)(kBM * rstride * 4);
+      cluster_phase();             // (1) every main loop of the cluster is over: the rings are free
+      // recv [S][kBM][rstride]: the partials of this CTA's columns, its own written here directly;
+      // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
       const uint32_t recv = smem_u32(smem);
+      const uint32_t sendb = recv + (uint32_t)S * chunk;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 32) {
@@ -482,50 +423,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < 8; ++g) {
           const int col = cc + 4 * g;
           const int owner = col / CW, cl = col - owner * CW;
-          const uint32_t off = (uint32_t)(((split * kBM + i) * rstride + cl) * 4);
-          st_cluster_f4(map_cluster_addr(recv + off, (uint32_t)owner),
-                        make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                    __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+          const uint32_t base = owner == split ? recv + (uint32_t)split * chunk
+                                               : sendb + (uint32_t)(owner < split ? owner : owner - 1) * chunk;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + (uint32_t)((i * rstride + cl) * 4)),
+                       "r"(r[4 * g]), "r"(r[4 * g + 1]), "r"(r[4 * g + 2]), "r"(r[4 * g + 3])
+                       : "memory");
         }
       }
       tc_fence_before_sync();
-      cluster_phase();  // (2) every partial has landed in its owner's receive buffer
-      const int n = nt * kBM + col_in_tile;
-      if (act || n < N) {  // (with act every lane takes part in the pair shuffles)
-#pragma unroll 1
-        for (int cl = 0; cl < CW; cl += 4) {
-          float4 acc = lds_f4(recv + (uint32_t)((i * rstride + cl) * 4));
-          for (int src = 1; src < S; ++src) {
-            const float4 p = lds_f4(recv + (uint32_t)(((src * kBM + i) * rstride + cl) * 4));
-            acc.x = __fadd_rn(acc.x, p.x);
-            acc.y = __fadd_rn(acc.y, p.y);
-            acc.z = __fadd_rn(acc.z, p.z);
-            acc.w = __fadd_rn(acc.w, p.w);
-          }
-          const int m = mt * BN + split * CW + cl;
-          const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-          if (act) {
-            const bool even = (n & 1) == 0;
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-              const float got = __shfl_xor_sync(0xffffffffu, even ? v[e + 1] : v[e], pair_mask);
-              const int mm = m + e + (even ? 0 : 1);
-              const __half o = silu_mul_h(even ? v[e] : got, even ? got : v[e + 1]);  // (gate, up)
-              if (n < N && mm < M) y[(size_t)mm * NO + n / 2] = o;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
-          }
+      fence_proxy_async_smem();  // the send chunks are read by the bulk copies (async proxy)
+      named_barrier_sync(1, kEpiWarps * 32);
+      // One bulk copy per other owner, into its receive slot `split`: the copy engine moves the
+      // chunks (st.shared::cluster or st.async stores from these 128 threads took 3-10 us for a
+      // 128 x 128 tile).
+      if (threadIdx.x == kEpiWarp0 * 32) {
+        const uint32_t rbar = smem_u32(recvbar);
+        for (int o = 0; o < S; ++o) {
+          if (o == split) continue;
+          bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk, (uint32_t)o),
+                            sendb + (uint32_t)(o < split ? o : o - 1) * chunk, chunk,
+                            map_cluster_addr(rbar, (uint32_t)o));
         }
       }
+      // every other CTA's chunk has landed once the receive barrier completes
+      if (!mbar_wait_warp(recvbar, 0)) report_error(err, kErrTimeoutMma);
     }
   }
 
-  if (S > 1 && (warp < kEpiWarp0 || warp >= kEpiWarp0 + kEpiWarps)) {
-    // the other warps take part in the two cluster barriers of the split-K exchange
-    cluster_phase();
+  if (S > 1) {
+    // ---------------- split-K: every warp adds the partials of this CTA's columns ----------------
+    if (warp < kEpiWarp0 || warp >= kEpiWarp0 + kEpiWarps) cluster_phase();  // the other warps' part in (1)
+    __syncthreads();  // the epilogue warps have seen the receive buffer complete
+    grid_dependency_wait();  // y may still be read by the preceding kernel
+    const int tile = blockIdx.x;
+    const int nt = tile % ntn, mt = tile / ntn;
+    const int CW = BN / S, rstride = CW + 4;
+    const uint32_t recv = smem_u32(smem);
+    const int NO = act ? N / 2 : N;
+    // Item j: TMEM lane i = j % kBM (a channel), tokens [4 c, 4 c + 4) of this CTA's columns with
+    // c = j / kBM.  The 32 lanes of a warp take 32 consecutive TMEM lanes (kThreads and kBM are
+    // multiples of 32), so the gate/up pairs meet in the warp as in the epilogue warps, and the
+    // stores of one instruction cover 32 channels of one token.  Spreading the additions and stores
+    // over all warps instead of the four epilogue warps (a 128 x 128 owner slice: 6.7 -> ? us).
+    const int items = kBM * (CW / 4);
+    for (int j = threadIdx.x; j < items; j += kThreads) {
+      const int i = j % kBM, cl = 4 * (j / kBM);
+      const int col_in_tile = tmem_lane_channel(i);
+      const int pair_mask = 8;
+      const int n = nt * kBM + col_in_tile;
+      float4 acc = lds_f4(recv + (uint32_t)((i * rstride + cl) * 4));
+      for (int src = 1; src < S; ++src) {  // split order
+        const float4 p = lds_f4(recv + (uint32_t)(((src * kBM + i) * rstride + cl) * 4));
+        acc.x = __fadd_rn(acc.x, p.x);
+        acc.y = __fadd_rn(acc.y, p.y);
+        acc.z = __fadd_rn(acc.z, p.z);
+        acc.w = __fadd_rn(acc.w, p.w);
+      }
+      const int m = mt * BN + split * CW + cl;
+      const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+      if (act) {
+        const bool even = (n & 1) == 0;
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const float got = __shfl_xor_sync(0xffffffffu, even ? v[e + 1] : v[e], pair_mask);
+          const int mm = m + e + (even ? 0 : 1);
+          const __half o = silu_mul_h(even ? v[e] : got, even ? got : v[e + 1]);  // (gate, up)
+          if (n < N && mm < M) y[(size_t)mm * NO + n / 2] = o;
+        }
+      } else if (n < N) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
+      }
+    }
+    // (2) no CTA leaves (freeing the shared memory that its bulk copies read, or that receives
+    // another CTA's copies) before every CTA of the cluster has received all of its chunks
     cluster_phase();
   }
   tc_fence_before_sync();
@@ -548,15 +520,16 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
     attr_set[dev].store(true, std::memory_order_release);
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int nkb = (K + L::kBK - 1) / L::kBK;
+  const int nkb = (K + kBK - 1) / kBK;
   const int sms = num_sms();
   int S = 1;
   // Few tiles: split K over a cluster so that (nearly) every SM streams weights.  Each split keeps
-  // at least 512 k; S is a power of two dividing BN into owner column ranges of >= 4.
+  // at least 512 k; S is a power of two dividing BN into owner column ranges of >= 4 whose exchange
+  // buffers fit the stage ring.
   if (2 * ntiles <= sms)
-    S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, L::kBytes, ntiles, nkb * L::kBK / 512,
+    S = pick_k_split(reinterpret_cast<const void*>(kern), kThreads, L::kBytes, ntiles, nkb * kBK / 512,
                      /*pow2=*/true);
-  while (S > 1 && BN / S < 4) S >>= 1;
+  while (S > 1 && !L::split_fits(S)) S >>= 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = S == 1 ? dim3(ntiles < sms ? ntiles : sms, 1, 1) : dim3(ntiles, S, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -599,16 +572,13 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
   const int ntn = (N + kBM - 1) / kBM;
   int BN = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   if (BN == 256 && M <= 512 && (ntn * ((M + 127) / 128) <= num_sms() || (M % 256 != 0 && M % 256 <= 128))) BN = 128;
-  const int BK = bk_for(BN);
-  const int GR = group >= BK ? 1 : BK / group;
+  const int GR = group >= kBK ? 1 : kBK / group;
   CUtensorMap tx, tq, ts, tz;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B, err) ||
-      !(BN <= 128  // A in TMEM: rows k = 4a + b as a 3D box {words, a, b}, so that b varies slowest
-            ? make_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N / 8, K / 4, 4, (uint64_t)N * 2,
-                           (uint64_t)N / 2, kStripWords, BK / 4, 4, CU_TENSOR_MAP_SWIZZLE_64B, err)
-            : make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qweight, N / 8, K, (uint64_t)N / 2, kStripWords,
-                           BK, CU_TENSOR_MAP_SWIZZLE_NONE, err)) ||
+      // rows k = 4a + b as a 3D box {words, a, b}, so that b varies slowest
+      !make_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, N / 8, K / 4, 4, (uint64_t)N * 2, (uint64_t)N / 2,
+                    kStripWords, kBK / 4, 4, CU_TENSOR_MAP_SWIZZLE_64B, err) ||
       !make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / group, (uint64_t)N * 2, kBM, GR,
                     CU_TENSOR_MAP_SWIZZLE_NONE, err) ||
       !make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, qzeros, N / 8, K / group, (uint64_t)N / 2, kStripWords, GR,
