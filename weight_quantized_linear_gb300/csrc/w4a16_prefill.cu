@@ -47,8 +47,17 @@ constexpr int kProducerWarp = 0, kMmaWarp = 1, kDqWarp0 = 2, kDqWarps = 8, kEpiW
 constexpr int kXProducerWarp = kEpiWarp0 + kEpiWarps;
 constexpr int kThreads = (kXProducerWarp + 1) * 32;
 
-template <int BN, int LG>
+constexpr int imin(int a, int b) { return a < b ? a : b; }
+
+// NACC accumulators in TMEM: 2 when a CTA walks several tiles (a tile's epilogue then overlaps the
+// next tile's MMAs), 1 when it owns one tile, which leaves TMEM for more A slots and so a deeper
+// ring.  Each stage owns one 64-column A slot, so the ring depth is the smaller of what shared
+// memory and TMEM hold (at most 8).  The pipeline of the smaller tiles is latency-bound: a stage's
+// copy, its dequantisation and its MMAs follow one another before the stage is refilled (128-token
+// tiles, one tile per CTA: 4 -> 5 stages).
+template <int BN, int LG, int NACC>
 struct PLayout {
+  static_assert(NACC == 1 || (NACC == 2 && BN <= 128), "the 256-token tile has one accumulator");
   static constexpr int G = 1 << LG;
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;
   static constexpr int kXBox = BN * 128;                 // BN token rows x 64 k fp16
@@ -62,11 +71,10 @@ struct PLayout {
   static constexpr int kOffZ = kOffS + kSBytes;
   static constexpr int kStage = (kOffZ + kZBytes + 1023) / 1024 * 1024;
   // stage s also owns TMEM A slot s: the producers' wait for the stage to be free (the MMAs of the
-  // stage kStages earlier have completed) frees the slot too.  The widest tile has 72 KB stages:
-  // three fit in shared memory.
-  static constexpr int kStages = BN > 128 ? 3 : 4;
-  static constexpr int kAccBufs = BN > 128 ? 1 : 2;  // accumulators (with 2 the epilogue of a tile
-                                                     // overlaps the next tile's MMAs)
+  // stage kStages earlier have completed) frees the slot too
+  static constexpr int kAccBufs = NACC;
+  static constexpr int kMaxBarBytes = (3 * 8 + 6) * 8 + 16;
+  static constexpr int kStages = imin(8, imin((227 * 1024 - 1024 - kMaxBarBytes) / kStage, (512 - NACC * BN) / 64));
   static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
   static constexpr int kBarBytes = (3 * kStages + 6) * 8 + 16;
   static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
@@ -103,7 +111,7 @@ __device__ __forceinline__ void cluster_phase() {
   cluster_wait();
 }
 
-template <int BN, int LG>
+template <int BN, int LG, int NACC>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_prefill_kernel(const __grid_constant__ CUtensorMap tm_x,   // x [M][K] fp16, box {64, BN}, SW128
                          const __grid_constant__ CUtensorMap tm_qw,  // qweight [K][N/8]: box {16, 64}, or (A in TMEM)
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_s,   // scales [K/G][N], box {128, GR}
                          const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                          int M, int N, int K, __half* __restrict__ y, int act, unsigned* err) {
-  using L = PLayout<BN, LG>;
+  using L = PLayout<BN, LG, NACC>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -506,11 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
-template <int BN, int LG>
+template <int BN, int LG, int NACC>
 cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts, const CUtensorMap& tz,
                      int M, int N, int K, __half* y, int act, unsigned* dev_err, cudaStream_t stream) {
-  using L = PLayout<BN, LG>;
-  auto kern = w4a16_prefill_kernel<BN, LG>;
+  using L = PLayout<BN, LG, NACC>;
+  auto kern = w4a16_prefill_kernel<BN, LG, NACC>;
   static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
   int dev = 0;
   cudaGetDevice(&dev);
@@ -547,18 +555,29 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tq, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, tx, tq, ts, tz, M, N, K, y, act, dev_err);
 }
 
-template <int BN>
+template <int BN, int NACC>
 cudaError_t launch_pg(int group, const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts,
                       const CUtensorMap& tz, int M, int N, int K, __half* y, int act, unsigned* dev_err,
                       cudaStream_t s) {
   switch (group) {
     case 32:
-      return launch_p<BN, 5>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
+      return launch_p<BN, 5, NACC>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
     case 64:
-      return launch_p<BN, 6>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
+      return launch_p<BN, 6, NACC>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
     default:
-      return launch_p<BN, 7>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
+      return launch_p<BN, 7, NACC>(tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
   }
+}
+
+// One accumulator when every CTA owns at most one tile (the split-K launches always do).
+template <int BN>
+cudaError_t launch_pa(int group, const CUtensorMap& tx, const CUtensorMap& tq, const CUtensorMap& ts,
+                      const CUtensorMap& tz, int M, int N, int K, __half* y, int act, unsigned* dev_err,
+                      cudaStream_t s) {
+  const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  if (BN > 128 || ntiles <= num_sms()) return launch_pg<BN, 1>(group, tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
+  if constexpr (BN <= 128) return launch_pg<BN, 2>(group, tx, tq, ts, tz, M, N, K, y, act, dev_err, s);
+  return cudaErrorInvalidValue;  // not reached
 }
 
 }  // namespace
@@ -586,10 +605,10 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
     return cudaErrorInvalidValue;
   }
   __half* yh = reinterpret_cast<__half*>(y);
-  if (BN == 32) return launch_pg<32>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
-  if (BN == 64) return launch_pg<64>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
-  if (BN == 128) return launch_pg<128>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
-  return launch_pg<256>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 32) return launch_pa<32>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 64) return launch_pa<64>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 128) return launch_pa<128>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  return launch_pa<256>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
 }
 
 }  // namespace wql
