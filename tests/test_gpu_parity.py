@@ -193,7 +193,10 @@ def test_pack_then_gemm_on_one_stream_without_sync(wql):
 # QRMSNorm + per-token int8: bit-exact
 # ------------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M,K", [(1, 8), (7, 512), (33, 4096), (3, 11008), (2, 16384), (512, 4096)])
+# M >= 2048 takes the row groups of 128 threads (K <= 4096) or 64 threads (K <= 2048), with
+# ragged lanes at K = 1032 (129 chunks of 8 for 256 lanes) and one chunk at K = 8
+@pytest.mark.parametrize("M,K", [(1, 8), (7, 512), (33, 4096), (3, 11008), (2, 16384), (512, 4096), (2048, 4096),
+                                 (2304, 2048), (4096, 1032), (2048, 8), (2048, 11008)])
 def test_qrmsnorm_quant_bit_exact(wql, M, K):
     X = inputs.activations(M, K, seed=1, outlier_channels=True)
     g = inputs.gamma(K, seed=1)
@@ -230,7 +233,7 @@ def _w8a8_chain(wql, M, K, N, seed=0):
     return got, ref, (q, xs, qW, ws)
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 512, 64), (16, 4096, 4096), (37, 1024, 96)])
+@pytest.mark.parametrize("M,K,N", [(1, 512, 64), (16, 4096, 4096), (37, 1024, 96), (2048, 2048, 64)])
 def test_w8a8_prep_chain_bit_exact(wql, M, K, N):
     got, ref, _ = _w8a8_chain(wql, M, K, N)
     for k in ("a", "s", "W2", "ws", "xs"):
