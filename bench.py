@@ -901,6 +901,118 @@ def run_profile_case(args):
     return 0
 
 
+# Phase points stamped by the W4A16 kernels in a build with -DWQL_PHASE_TRACE (slot order).
+TRACE_PHASES = {
+    0: ["start", "dependency resolved", "first stage landed", "last consumer warp done", "lanes folded",
+        "own slice received", "end"],
+    1: ["start", "TMEM allocated", "dependency resolved", "first stage's MMAs", "last stage's MMAs",
+        "last MMAs issued", "accumulator ready", "cluster barrier passed", "partials sent",
+        "partials received", "outputs stored", "end", "stage 8 at the dequantisers", "stage 8 dequantised",
+        "stage 8 at the MMA thread", "stage 8's MMAs issued"],
+}
+TRACE_END = {0: 6, 1: 11}  # the slot each CTA stamps last
+
+
+def run_trace(args):
+    """Phase trace of back-to-back W4A16 calls: ``--trace M,K,N,G``.
+
+    Builds the developer library with the kernels' phase stamps (-DWQL_PHASE_TRACE; stamps only,
+    no work skipped), runs a CUDA graph of ``--calls`` calls over distinct weight copies and output
+    buffers, replays it, and prints for each phase the median over the middle launches of the
+    per-launch median over CTAs, in microseconds from the launch's median "dependency resolved"
+    stamp, with the spread over CTAs.  Also: the time from the preceding launch's last CTA end to
+    this launch's dependency resolution (the dependent-launch flush), and the launch period.
+    """
+    import ctypes
+    import numpy as np
+    import torch
+    from weight_quantized_linear_gb300 import build, inputs
+    import weight_quantized_linear_gb300 as wql
+    lib_path = build.build(trace=True)
+    wql.load(lib_path)
+    lib = wql._lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, K, N, G = (int(v) for v in args.trace.split(","))
+    kernel = int(lib.wql_w4a16_kernel_for(M, K, N))
+    if kernel not in TRACE_PHASES:
+        raise SystemExit(f"no phase trace for kernel {kernel}")
+    names = TRACE_PHASES[kernel]
+    dep = names.index("dependency resolved")
+    L = max(4, args.calls)
+    qw, s, qz = wql.awq_pack(torch.from_numpy(inputs.weight(K, N, seed=0, outliers=True)).to(dev), G)
+    stack = [(qw, s, qz)] + [(qw.clone(), s.clone(), qz.clone()) for _ in range(L - 1)]
+    x = torch.from_numpy(inputs.activations(M, K, seed=0, outlier_channels=True)).to(dev)
+    ystride = (M * N * 2 + 4095) // 4096 * 4096
+    yflat = torch.empty(L * ystride // 2, dtype=torch.float16, device=dev)
+    ys = [yflat[l * ystride // 2: l * ystride // 2 + M * N].view(M, N) for l in range(L)]
+    ctas = 2048
+    buf = torch.zeros(L * ctas * 32, dtype=torch.int64, device=dev)
+    st = lib.wql_trace_setup(ctypes.c_void_p(buf.data_ptr()), ctypes.c_void_p(yflat.data_ptr()), ystride, L, ctas)
+    if st != 0:
+        raise SystemExit(f"wql_trace_setup: {lib.wql_last_error().decode()}")
+    stream = torch.cuda.Stream(device=dev)
+
+    def fn():
+        for (a, b, z), y in zip(stack, ys):
+            wql.w4a16_gemm(x, a, b, z, G, out=y)
+    try:
+        g = capture(torch, fn, stream)
+        for _ in range(3):
+            g.replay()
+        sec = time_replays(torch, g, 10, stream) / (10 * L)
+        buf.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        wql.device_status(dev)
+    finally:
+        lib.wql_trace_setup(None, None, 0, 0, 0)
+    t = buf.view(L, ctas, 32).cpu().numpy().astype(np.int64)
+    live = t[:, :, 0] > 0
+    nctas = int(live.sum(axis=1).max())
+    rel = {k: [] for k in range(len(names))}
+    spread = {k: [] for k in range(len(names))}
+    flush, period = [], []
+    prev_end = prev_dep = None
+    for l in range(L):
+        rows = t[l][live[l]]
+        dep_t = np.median(rows[:, dep][rows[:, dep] > 0])
+        end_t = rows[:, TRACE_END[kernel]].max()
+        if 2 <= l < L - 1:
+            for k in range(len(names)):
+                v = rows[:, k][rows[:, k] > 0]
+                if v.size:
+                    rel[k].append((np.median(v) - dep_t) / 1e3)
+                    spread[k].append((v.min() - dep_t, v.max() - dep_t))
+            flush.append((dep_t - prev_end) / 1e3)
+            period.append((dep_t - prev_dep) / 1e3)
+        prev_end, prev_dep = end_t, dep_t
+    smids = t[L // 2][live[L // 2]][:, 31]
+    out = {"case": f"w4a16 M={M} K={K} N={N} G={G}", "kernel": ["decode", "prefill"][kernel], "calls": L,
+           "ctas_per_launch": nctas, "distinct_sms": int(np.unique(smids).size),
+           "us_per_call_graph": round(sec * 1e6, 2),
+           "launch_period_us": round(float(np.median(period)), 2),
+           "flush_us": round(float(np.median(flush)), 2),
+           "phases_us_from_dependency": {}}
+    print(f"{out['case']}: {out['kernel']} kernel, {nctas} CTAs on {out['distinct_sms']} SMs, "
+          f"{out['us_per_call_graph']} us per call (graph of {L})")
+    print(f"  preceding launch's last CTA end -> dependency resolved: {out['flush_us']:.2f} us; "
+          f"period {out['launch_period_us']:.2f} us")
+    print(f"  {'phase':<28} {'median':>8} {'earliest CTA':>13} {'latest CTA':>11}   (us from dependency resolved)")
+    for k, name in enumerate(names):
+        if not rel[k]:
+            continue
+        med = float(np.median(rel[k]))
+        lo = float(np.median([a for a, _ in spread[k]])) / 1e3
+        hi = float(np.median([b for _, b in spread[k]])) / 1e3
+        out["phases_us_from_dependency"][name] = [round(med, 2), round(lo, 2), round(hi, 2)]
+        print(f"  {name:<28} {med:8.2f} {lo:13.2f} {hi:11.2f}")
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -916,11 +1028,16 @@ def main():
                     help="run one operation a few times for a profiler: w4a16:M,K,N,G | w8a8:M,K,N[,1] | fp8:M,K,N[,1] | "
                          "norm:M,K | normfp8:M,K | kv:rows,D | prep:K,N")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--trace", default=None,
+                    help="phase trace of back-to-back W4A16 calls M,K,N,G (builds the -DWQL_PHASE_TRACE library; "
+                         "--calls launches per graph, at least 4)")
     ap.add_argument("--rows", default=None,
                     help="with --sweep: comma-separated row families to measure (e.g. a6,f2); default all")
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)
+    if args.trace:
+        return run_trace(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

@@ -92,6 +92,16 @@ wql_status wql_device_status(void* stream);
  * caller memory.  Returns WQL_ECUDA if the launch fails. */
 wql_status wql_diag_expire_wait(void* stream);
 
+/* Phase trace of the W4A16 kernels, for a developer build compiled with -DWQL_PHASE_TRACE (a
+ * library file of its own; the default build returns WQL_EUNSUPPORTED and does nothing).
+ * Registers a device buffer buf of launches x ctas x 32 uint64 (caller-owned, zero-filled by the
+ * caller): every later w4a16 launch whose output pointer y lies at ybase + l * ystride
+ * (0 <= l < launches) writes, per CTA c < ctas, %globaltimer nanoseconds at its phase points into
+ * buf[(l * ctas + c) * 32 + slot], and its SM id into slot 31.  Launches whose y lies elsewhere
+ * are not recorded.  buf == NULL switches the trace off.  Stamps only: the kernels skip and
+ * reorder nothing.  Call it between launches, not while one may be running. */
+wql_status wql_trace_setup(uint64_t* buf, const void* ybase, uint64_t ystride, int launches, int ctas);
+
 /* ----------------------------------------------------------------------------------------
  * awq_pack  [AWQ] section 2; [AUQ] sections 3.3 and 5.4.
  * Quantise fp32 weights w [K, N] to asymmetric int4, per group of G consecutive input

@@ -43,6 +43,9 @@ def test_host_only_entry_points(wql_lib):
     assert lib.wql_w4a16_kernel_for(33, 4096, 4096) == 1
     assert lib.wql_w4a16_kernel_for(32, 11008, 4096) == 1   # long K: split-K pays
     assert lib.wql_w4a16_kernel_for(32, 4096, 4096) == 0    # 32 output tiles: decode
+    # the phase trace exists only in the developer build; the default library refuses it
+    assert lib.wql_trace_setup(None, None, 0, 0, 0) == 2  # WQL_EUNSUPPORTED
+    assert b"WQL_PHASE_TRACE" in lib.wql_last_error()
 
 
 def test_validation_rejects_bad_arguments_without_a_gpu(wql_lib):

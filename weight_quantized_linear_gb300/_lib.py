@@ -30,6 +30,7 @@ SIGNATURES = {
     "wql_version": (_I, []),
     "wql_device_status": (_I, [_P]),
     "wql_diag_expire_wait": (_I, [_P]),
+    "wql_trace_setup": (_I, [_P, _P, ctypes.c_uint64, _I, _I]),
     "wql_awq_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),

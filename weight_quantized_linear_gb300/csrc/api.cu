@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "trace.cuh"
 #include "wql.h"
 
 namespace {
@@ -458,6 +459,26 @@ wql_status wql_diag_expire_wait(void* stream) {
   if (!dev_err) return fail(WQL_ECUDA, "wql_diag_expire_wait: cannot locate the device error word");
   expire_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dev_err);
   return cuda_status(cudaGetLastError(), "wql_diag_expire_wait");
+}
+
+wql_status wql_trace_setup(uint64_t* buf, const void* ybase, uint64_t ystride, int launches, int ctas) {
+#ifdef WQL_PHASE_TRACE
+  WQL_REQUIRE(buf == nullptr || (launches > 0 && ctas > 0 && ystride > 0 &&
+                                 (reinterpret_cast<uintptr_t>(buf) & 7u) == 0),
+              "buf must be null, or 8-byte aligned with positive launches, ctas and ystride");
+  wql::TraceDesc d{reinterpret_cast<unsigned long long*>(buf), reinterpret_cast<unsigned long long>(ybase),
+                   (unsigned long long)ystride, launches, ctas};
+  cudaError_t e = wql::trace_set_w4a16_decode(d);
+  if (e == cudaSuccess) e = wql::trace_set_w4a16_prefill(d);
+  return cuda_status(e, "wql_trace_setup");
+#else
+  (void)buf;
+  (void)ybase;
+  (void)ystride;
+  (void)launches;
+  (void)ctas;
+  return fail(WQL_EUNSUPPORTED, "wql_trace_setup: this library was built without WQL_PHASE_TRACE");
+#endif
 }
 
 }  // extern "C"

@@ -121,4 +121,11 @@ cudaError_t launch_kv_quant_i8(const uint16_t* kv, long long rows, int D, int8_t
 cudaError_t launch_kv_dequant_i8(const int8_t* q, const float* scales, long long rows, int D, uint16_t* out,
                                  cudaStream_t s);
 
+#ifdef WQL_PHASE_TRACE
+// Phase-trace builds only: register the stamp buffer with the traced kernels of each source file.
+struct TraceDesc;
+cudaError_t trace_set_w4a16_decode(const TraceDesc& d);
+cudaError_t trace_set_w4a16_prefill(const TraceDesc& d);
+#endif
+
 }  // namespace wql

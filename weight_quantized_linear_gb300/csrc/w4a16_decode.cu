@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "trace.cuh"
 
 namespace wql {
 namespace {
@@ -130,6 +131,13 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
                         const __grid_constant__ CUtensorMap tm_z,   // qzeros [K/G][N/8], box {16, GR}
                         int M, int N, int kblocks, int x3d, __half* __restrict__ y, int act, unsigned* err) {
   using L = Layout<MT, LG>;
+  // phase stamps (trace builds only): 0 start, 1 dependency resolved, 2 first stage landed, 3 last
+  // consumer warp done, 4 lanes folded, 5 own slice received, 6 end
+  WQL_TRACE_ROW(y);
+  if (threadIdx.x == 0) {
+    WQL_STAMP(0);
+    WQL_STAMP_SMID();
+  }
   constexpr int kLanes = L::kLanes;
   constexpr int kConsumerWarps = Warps<MT>::kConsumerWarps;
   constexpr int kThreads = Warps<MT>::kThreads;
@@ -204,6 +212,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
       const int pro = nkb < kStages ? nkb : kStages;
       for (int i = 0; i < pro; ++i) issue_weights(i);
       grid_dependency_wait();  // activations may come from the preceding kernel
+      WQL_STAMP(1);
       for (int i = 0; i < pro; ++i) issue_x(i);
       // Only now may the next kernel launch: its CTAs share these SMs and open with a burst of
       // weight copies, which would otherwise queue in the SM's TMA unit ahead of the activation
@@ -270,6 +279,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
         report_error(err, kErrTimeoutFull);
         break;
       }
+      if (i == 0 && threadIdx.x == 0) WQL_STAMP(2);
       const uint32_t xt = smem_u32(smem + s * L::kStage);
       const uint32_t wt = xt + L::kXBytes;
       const uint32_t sbase = smem_u32(smem + L::kOffSZ + s * L::kSZ), zbase = sbase + L::kSBytes;
@@ -352,6 +362,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if (lane == 0) WQL_STAMP_MAX(3);
 
     // Fold the lanes' partials in shared memory first.  Once all consumer warps pass this
     // named barrier every stage has been consumed and every issued copy has landed (each one was
@@ -371,6 +382,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
             make_float4(tot[0][mt][e], tot[1][mt][e], tot[2][mt][e], tot[3][mt][e]);
       }
     named_barrier_sync(1, kConsumerWarps * 32);
+    if (threadIdx.x == 0) WQL_STAMP(4);
     // split-K: send each folded float4 to its owner CTA
     const uint32_t recv_base = smem_u32(recv);
     const uint32_t bar_local = smem_u32(recv_full);
@@ -394,6 +406,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
   // ---------------- owners: add the partials of their slice in a fixed order ----------------
   const bool received = mbar_wait_bounded(recv_full, 0);
   if (!received) report_error(err, kErrTimeoutMma);
+  if (threadIdx.x == 0) WQL_STAMP(5);
   __syncwarp();
   // phase 1: this CTA's slice is complete (an execution barrier only: the receive barrier has
   // already ordered the data, so no release fence is needed)
@@ -428,6 +441,7 @@ __global__ void __launch_bounds__(Warps<MT>::kThreads, 2)
   }
   __syncwarp();
   cluster_wait();  // phase 1: no CTA exits before every slice in the cluster is complete
+  if (threadIdx.x == 0) WQL_STAMP(6);
 }
 
 template <int MT, int LG>
@@ -486,6 +500,10 @@ cudaError_t launch_g(int group, const CUtensorMap& tx, int x3d, const CUtensorMa
 }
 
 }  // namespace
+
+#ifdef WQL_PHASE_TRACE
+cudaError_t trace_set_w4a16_decode(const TraceDesc& d) { return trace_set_local(d); }
+#endif
 
 cudaError_t launch_w4a16_decode(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
                                 const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,

@@ -34,6 +34,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
+#include "trace.cuh"
 
 namespace wql {
 namespace {
@@ -137,6 +138,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntm = (M + BN - 1) / BN;
   const int ntiles = ntn * ntm;
   const int nkb = (K + kBK - 1) / kBK;
+  // phase stamps (trace builds only): 0 start, 1 TMEM allocated, 2 dependency resolved, 3 first
+  // stage's MMAs may start, 4 last stage's MMAs may start, 5 last MMAs issued, 6 accumulator ready
+  // (first tile), 7 split-K cluster barrier passed, 8 partials sent, 9 partials received,
+  // 10 outputs stored, 11 end; the ninth stage of the first tile: 12 at the dequantisers (first
+  // warp), 13 dequantised, 14 at the MMA thread, 15 its MMAs issued
+  WQL_TRACE_ROW(y);
+  if (threadIdx.x == 0) {
+    WQL_STAMP(0);
+    WQL_STAMP_SMID();
+  }
   const int S = gridDim.y, split = blockIdx.y;  // split-K: cluster (1, S, 1), rank = blockIdx.y
   const int kb0 = (int)(((long long)split * nkb) / S), kb1 = (int)(((long long)(split + 1) * nkb) / S);
 
@@ -166,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) WQL_STAMP(1);
   // A grid of at most one tile per CTA leaves SMs free for most of its run: let the next kernel be
   // scheduled on them now and start its own weight prefetch (its consumers still wait for this
   // grid to complete).  A persistent grid over many tiles triggers only when it exits.
@@ -182,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         tma_prefetch_desc(&tm_x);
         grid_dependency_wait();  // the activations may come from the preceding kernel
+        WQL_STAMP(2);
       }
       // The packed weights do not depend on the preceding kernel: the weight producer never waits
       // for it, so its first stages stream while the preceding kernel is still running.
@@ -247,6 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+          if (kb == kb0 && it == 0) WQL_STAMP(3);
+          if (kb == kb1 - 1) WQL_STAMP(4);
+          if (kb == kb0 + 8 && it == 0) WQL_STAMP(14);
           const uint32_t xs = smem_u32(smem + stage * L::kStage);
           // the B descriptors of the stage differ only in the start address (bits 0-13, addr >> 4;
           // shared-memory addresses stay below 2^18, so adding to it never carries)
@@ -259,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = (kb != kb0 || s != 0) ? 1u : 0u;
             umma_f16_ta(d_tmem, tmem_base + L::kAColBase + stage * 64 + s * 8, bdesc, idesc, acc);
           }
+          if (kb == kb0 + 8 && it == 0) WQL_STAMP(15);
           umma_commit(&empty[stage]);  // the stage is free once these MMAs have read it
           if (++stage == kStages) {
             stage = 0;
@@ -266,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        WQL_STAMP(5);
         umma_commit(&accfull[b]);
       }
       // every MMA issued by this thread has completed before TMEM is released
@@ -298,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();  // this slot's earlier MMAs (ordered through the stage barriers) come first
+        if (threadIdx.x == kDqWarp0 * 32 && kb == kb0 + 8 && tile == (int)blockIdx.x) WQL_STAMP(12);
         const uint32_t st = smem_u32(smem + stage * L::kStage);
         uint32_t r0[16], r1[16];
         uint32_t zc[4], sp[4];  // per channel e: -(1024 + z) or -(64 + z), and s, in both halves
@@ -350,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[stage]);
+        if (threadIdx.x == kDqWarp0 * 32 && kb == kb0 + 8 && tile == (int)blockIdx.x) WQL_STAMP(13);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
@@ -380,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
+        if (it == 0 && threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(6);
         const int n = nt * kBM + col_in_tile;
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + b * BN;
 #pragma unroll 1
@@ -413,10 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
       if (!mbar_wait_warp(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
       tc_fence_after_sync();
+      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(6);
       const int CW = BN / S;       // token columns owned by each CTA of the cluster
       const int rstride = CW + 4;  // floats per exchange row (16 bytes of padding against bank conflicts)
       const uint32_t chunk = (uint32_t)(kBM * rstride * 4);
       cluster_phase();             // (1) every main loop of the cluster is over: the rings are free
+      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(7);
       // recv [S][kBM][rstride]: the partials of this CTA's columns, its own written here directly;
       // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
       const uint32_t recv = smem_u32(smem);
@@ -453,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             map_cluster_addr(rbar, (uint32_t)o));
         }
       }
+      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(8);
       // every other CTA's chunk has landed once the receive barrier completes
       if (!mbar_wait_warp(recvbar, 0)) report_error(err, kErrTimeoutMma);
+      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(9);
     }
   }
 
@@ -508,10 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // another CTA's copies) before every CTA of the cluster has received all of its chunks
     cluster_phase();
   }
+  if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(10);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
+  if (threadIdx.x == 0) WQL_STAMP(11);
 }
 
 template <int BN, int LG, int NACC>
@@ -581,6 +608,10 @@ cudaError_t launch_pa(int group, const CUtensorMap& tx, const CUtensorMap& tq, c
 }
 
 }  // namespace
+
+#ifdef WQL_PHASE_TRACE
+cudaError_t trace_set_w4a16_prefill(const TraceDesc& d) { return trace_set_local(d); }
+#endif
 
 cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, const uint16_t* scales,
                                  const uint32_t* qzeros, int M, int K, int N, int group, uint16_t* y, int act,
