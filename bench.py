@@ -913,6 +913,46 @@ TRACE_PHASES = {
 TRACE_END = {0: 6, 1: 11}  # the slot each CTA stamps last
 
 
+def trace_summary(t, kernel):
+    """Summarise phase stamps t [launches][ctas][32] (ns, 0 = not stamped) of one traced graph.
+
+    Per phase: the median over the middle launches (the third to the second-to-last) of the median
+    over a launch's CTAs, and of its earliest and latest CTA, in microseconds from the launch's
+    median "dependency resolved" stamp.  Also the dependent-launch flush (this launch's dependency
+    resolution after the preceding launch's last CTA end) and the launch period.
+    """
+    import numpy as np
+    names = TRACE_PHASES[kernel]
+    dep = names.index("dependency resolved")
+    L = t.shape[0]
+    live = t[:, :, 0] > 0
+    rel = {k: [] for k in range(len(names))}
+    flush, period = [], []
+    prev_end = prev_dep = None
+    for l in range(L):
+        rows = t[l][live[l]]
+        d = rows[:, dep][rows[:, dep] > 0]
+        dep_t = float(np.median(d)) if d.size else float("nan")
+        end_t = rows[:, TRACE_END[kernel]].max() if rows.size else 0
+        if 2 <= l < L - 1:
+            for k in range(len(names)):
+                v = rows[:, k][rows[:, k] > 0]
+                if v.size:
+                    rel[k].append(((np.median(v) - dep_t) / 1e3, (v.min() - dep_t) / 1e3, (v.max() - dep_t) / 1e3))
+            flush.append((dep_t - prev_end) / 1e3)
+            period.append((dep_t - prev_dep) / 1e3)
+        prev_end, prev_dep = end_t, dep_t
+    smids = t[L // 2][live[L // 2]][:, 31]
+    phases = {}
+    for k, name in enumerate(names):
+        if rel[k]:
+            phases[name] = [round(float(np.median([r[i] for r in rel[k]])), 2) for i in range(3)]
+    return {"ctas_per_launch": int(live.sum(axis=1).max()), "distinct_sms": int(np.unique(smids).size),
+            "launch_period_us": round(float(np.median(period)), 2) if period else None,
+            "flush_us": round(float(np.median(flush)), 2) if flush else None,
+            "phases_us_from_dependency": phases}
+
+
 def run_trace(args):
     """Phase trace of back-to-back W4A16 calls: ``--trace M,K,N,G``.
 
@@ -937,8 +977,6 @@ def run_trace(args):
     kernel = int(lib.wql_w4a16_kernel_for(M, K, N))
     if kernel not in TRACE_PHASES:
         raise SystemExit(f"no phase trace for kernel {kernel}")
-    names = TRACE_PHASES[kernel]
-    dep = names.index("dependency resolved")
     L = max(4, args.calls)
     qw, s, qz = wql.awq_pack(torch.from_numpy(inputs.weight(K, N, seed=0, outliers=True)).to(dev), G)
     stack = [(qw, s, qz)] + [(qw.clone(), s.clone(), qz.clone()) for _ in range(L - 1)]
@@ -970,44 +1008,15 @@ def run_trace(args):
     finally:
         lib.wql_trace_setup(None, None, 0, 0, 0)
     t = buf.view(L, ctas, 32).cpu().numpy().astype(np.int64)
-    live = t[:, :, 0] > 0
-    nctas = int(live.sum(axis=1).max())
-    rel = {k: [] for k in range(len(names))}
-    spread = {k: [] for k in range(len(names))}
-    flush, period = [], []
-    prev_end = prev_dep = None
-    for l in range(L):
-        rows = t[l][live[l]]
-        dep_t = np.median(rows[:, dep][rows[:, dep] > 0])
-        end_t = rows[:, TRACE_END[kernel]].max()
-        if 2 <= l < L - 1:
-            for k in range(len(names)):
-                v = rows[:, k][rows[:, k] > 0]
-                if v.size:
-                    rel[k].append((np.median(v) - dep_t) / 1e3)
-                    spread[k].append((v.min() - dep_t, v.max() - dep_t))
-            flush.append((dep_t - prev_end) / 1e3)
-            period.append((dep_t - prev_dep) / 1e3)
-        prev_end, prev_dep = end_t, dep_t
-    smids = t[L // 2][live[L // 2]][:, 31]
     out = {"case": f"w4a16 M={M} K={K} N={N} G={G}", "kernel": ["decode", "prefill"][kernel], "calls": L,
-           "ctas_per_launch": nctas, "distinct_sms": int(np.unique(smids).size),
-           "us_per_call_graph": round(sec * 1e6, 2),
-           "launch_period_us": round(float(np.median(period)), 2),
-           "flush_us": round(float(np.median(flush)), 2),
-           "phases_us_from_dependency": {}}
-    print(f"{out['case']}: {out['kernel']} kernel, {nctas} CTAs on {out['distinct_sms']} SMs, "
+           "us_per_call_graph": round(sec * 1e6, 2)}
+    out.update(trace_summary(t, kernel))
+    print(f"{out['case']}: {out['kernel']} kernel, {out['ctas_per_launch']} CTAs on {out['distinct_sms']} SMs, "
           f"{out['us_per_call_graph']} us per call (graph of {L})")
     print(f"  preceding launch's last CTA end -> dependency resolved: {out['flush_us']:.2f} us; "
           f"period {out['launch_period_us']:.2f} us")
     print(f"  {'phase':<28} {'median':>8} {'earliest CTA':>13} {'latest CTA':>11}   (us from dependency resolved)")
-    for k, name in enumerate(names):
-        if not rel[k]:
-            continue
-        med = float(np.median(rel[k]))
-        lo = float(np.median([a for a, _ in spread[k]])) / 1e3
-        hi = float(np.median([b for _, b in spread[k]])) / 1e3
-        out["phases_us_from_dependency"][name] = [round(med, 2), round(lo, 2), round(hi, 2)]
+    for name, (med, lo, hi) in out["phases_us_from_dependency"].items():
         print(f"  {name:<28} {med:8.2f} {lo:13.2f} {hi:11.2f}")
     print(json.dumps(out), flush=True)
     return 0

@@ -38,3 +38,36 @@ def test_algorithmic_byte_counts():
     assert bench.qrmsnorm_bytes(M, K) == 2 * M * K + 2 * K + M * K + 4 * M
     assert bench.add_qrmsnorm_bytes(M, K) == bench.qrmsnorm_bytes(M, K) + 4 * M * K
     assert bench.gemm_flops(M, K, N) == 2 * M * K * N
+
+
+def test_phase_trace_summary_on_synthetic_stamps():
+    # Six launches of four CTAs of the decode kernel, 10 us apart.  Launch l resolves its
+    # dependency at 10 l + 1 us; its CTAs end at 10 l + 3.5, 3.6, 3.7 and 4 us, so the flush
+    # (dependency resolution after the preceding launch's last CTA end) is 7 us.  Phase k of CTA c
+    # is stamped 0.1 k + 0.02 c us after the dependency; slot 31 holds the SM id.
+    import numpy as np
+    import bench
+    L, C = 6, 4
+    t = np.zeros((L, C, 32), dtype=np.int64)
+    names = bench.TRACE_PHASES[0]
+    end = bench.TRACE_END[0]
+    dep = names.index("dependency resolved")
+    for l in range(L):
+        for c in range(C):
+            base = 10_000 * l + 1_000
+            for k in range(len(names)):
+                t[l, c, k] = base + 100 * k + 20 * c
+            t[l, c, dep] = base
+            t[l, c, 0] = base - 500 + 20 * c  # start, before the dependency resolves
+            t[l, c, end] = 10_000 * l + [3_500, 3_600, 3_700, 4_000][c]
+            t[l, c, 31] = 7 + c
+    out = bench.trace_summary(t, 0)
+    assert out["ctas_per_launch"] == C and out["distinct_sms"] == C
+    assert out["launch_period_us"] == 10.0
+    assert out["flush_us"] == 7.0
+    ph = out["phases_us_from_dependency"]
+    assert ph["dependency resolved"] == [0.0, 0.0, 0.0]
+    assert ph["start"] == [-0.47, -0.5, -0.44]
+    k = names.index("lanes folded")
+    assert ph["lanes folded"] == [round(0.1 * k + 0.03, 2), round(0.1 * k, 2), round(0.1 * k + 0.06, 2)]
+    assert ph["end"] == [2.65, 2.5, 3.0]
