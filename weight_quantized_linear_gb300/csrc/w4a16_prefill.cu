@@ -183,6 +183,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   // grid to complete).  A persistent grid over many tiles triggers only when it exits.
   if (threadIdx.x == 0 && ntiles <= (int)gridDim.x) grid_dependents_launch();
 
+  // One tile per CTA (every split-K launch, and grids with no more tiles than CTAs): once the
+  // accumulator is ready the dequantisers are idle, so they drain it together with the epilogue
+  // warps.  Each TMEM lane quarter has three such warps, and the quarter's 32-column chunk j goes to
+  // drain rank j % 3 (0: its epilogue warp, 1 and 2: its two dequantisers).  CTAs that walk several
+  // tiles drain with the four epilogue warps alone while the dequantisers move on to the next tile.
+  const bool single = ntiles <= (int)gridDim.x;
+  constexpr int kDrainRanks = 3, kDrainWarps = kEpiWarps + kDqWarps;
+  auto drain_single = [&](int quad, int rank) {
+    const int i = quad * 32 + lane;
+    // channel of TMEM lane i: lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8
+    const int col_in_tile = tmem_lane_channel(i);
+    const int pair_mask = 8;  // gate/up pairs meet in lanes differing in bit 3 (see the epilogue)
+    const int NO = act ? N / 2 : N;
+    const int nt = (int)blockIdx.x % ntn, mt = (int)blockIdx.x / ntn;
+    const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
+    const bool ready = mbar_wait_warp(&accfull[0], 0);
+    if (!ready) report_error(err, kErrTimeoutMma);
+    tc_fence_after_sync();
+    if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(6);
+    if (S == 1) {
+      grid_dependency_wait();  // y may still be read by the preceding kernel
+      const int n = nt * kBM + col_in_tile;
+#pragma unroll 1
+      for (int cc = 32 * rank; ready && cc < BN; cc += 32 * kDrainRanks) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + cc, r);
+        tmem_ld_wait();
+        const int mbase = mt * BN + cc;
+        if (act) {
+          const bool even = (n & 1) == 0;
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+            const float got = __shfl_xor_sync(0xffffffffu, even ? v1 : v0, pair_mask);
+            const int m = mbase + k + (even ? 0 : 1);
+            const __half o = silu_mul_h(even ? v0 : got, even ? got : v1);  // (gate, up)
+            if (n < N && m < M) y[(size_t)m * NO + n / 2] = o;
+          }
+        } else if (n < N) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (mbase + k < M) y[(size_t)(mbase + k) * N + n] = __float2half_rn(__uint_as_float(r[k]));
+          }
+        }
+      }
+      return;
+    }
+    // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
+    const int CW = BN / S;       // token columns owned by each CTA of the cluster
+    const int rstride = CW + 4;  // floats per exchange row (16 bytes of padding against bank conflicts)
+    const uint32_t chunk = (uint32_t)(kBM * rstride * 4);
+    cluster_phase();             // (1) every main loop of the cluster is over: the rings are free
+    if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(7);
+    // recv [S][kBM][rstride]: the partials of this CTA's columns, its own written here directly;
+    // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
+    const uint32_t recv = smem_u32(smem);
+    const uint32_t sendb = recv + (uint32_t)S * chunk;
+#pragma unroll 1
+    for (int cc = 32 * rank; ready && cc < BN; cc += 32 * kDrainRanks) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + cc, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int col = cc + 4 * g;
+        const int owner = col / CW, cl = col - owner * CW;
+        const uint32_t base = owner == split ? recv + (uint32_t)split * chunk
+                                             : sendb + (uint32_t)(owner < split ? owner : owner - 1) * chunk;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + (uint32_t)((i * rstride + cl) * 4)),
+                     "r"(r[4 * g]), "r"(r[4 * g + 1]), "r"(r[4 * g + 2]), "r"(r[4 * g + 3])
+                     : "memory");
+      }
+    }
+    tc_fence_before_sync();
+    fence_proxy_async_smem();  // the send chunks are read by the bulk copies (async proxy)
+    named_barrier_sync(1, kDrainWarps * 32);
+    // One bulk copy per other owner, into its receive slot `split`: the copy engine moves the
+    // chunks (st.shared::cluster or st.async stores from the epilogue threads took 3-10 us for a
+    // 128 x 128 tile).
+    if (threadIdx.x == kEpiWarp0 * 32) {
+      const uint32_t rbar = smem_u32(recvbar);
+      for (int o = 0; o < S; ++o) {
+        if (o == split) continue;
+        bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk, (uint32_t)o),
+                          sendb + (uint32_t)(o < split ? o : o - 1) * chunk, chunk,
+                          map_cluster_addr(rbar, (uint32_t)o));
+      }
+      WQL_STAMP(8);
+    }
+    // every other CTA's chunk has landed once the receive barrier completes
+    if (rank == 0) {
+      if (!mbar_wait_warp(recvbar, 0)) report_error(err, kErrTimeoutMma);
+      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(9);
+    }
+  };
+
   if (warp == kProducerWarp || warp == kXProducerWarp) {
     // ---------------- producers: weights (warp 0) and activations (warp 14) ----------------
     if (lane == 0) {
@@ -376,21 +472,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (single) drain_single(q, 1 + hk);
   } else if (warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: TMEM -> fp16 -> global ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int i = quad * 32 + lane;
-    // channel of TMEM lane i: lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8
-    const int col_in_tile = tmem_lane_channel(i);
-    // with the gate/up activation (act), channel pairs (2j, 2j + 1) meet in lanes differing in bit 3
-    // (pair_mask).  The two lanes of a pair split the tokens: for
-    // tokens k, k + 1 the even-channel lane computes output (k, j) from its gate and the partner's up,
-    // the odd-channel lane output (k + 1, j) from the partner's gate and its own up -- one shuffle
-    // carries both, and every lane evaluates the activation once per two tokens
-    const int pair_mask = 8;
-    const int NO = act ? N / 2 : N;  // output row length
-    grid_dependency_wait();  // y may still be read by the preceding kernel
-    if (S == 1) {
+    if (single) {
+      drain_single(quad, 0);
+    } else {
+      // several tiles per CTA (never split-K): accumulators b = it % 2 alternate
+      const int i = quad * 32 + lane;
+      // channel of TMEM lane i: lane 32 q + L holds channel 32 q + 4 (L % 8) + L / 8
+      const int col_in_tile = tmem_lane_channel(i);
+      // with the gate/up activation (act), channel pairs (2j, 2j + 1) meet in lanes differing in bit
+      // 3 (pair_mask).  The two lanes of a pair split the tokens: for tokens k, k + 1 the
+      // even-channel lane computes output (k, j) from its gate and the partner's up, the odd-channel
+      // lane output (k + 1, j) from the partner's gate and its own up -- one shuffle carries both,
+      // and every lane evaluates the activation once per two tokens
+      const int pair_mask = 8;
+      const int NO = act ? N / 2 : N;  // output row length
+      grid_dependency_wait();  // y may still be read by the preceding kernel
       int it = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int nt = tile % ntn, mt = tile / ntn;
@@ -430,62 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&accempty[b]);
       }
-    } else {
-      // split-K: exactly one tile per cluster (the host launches gridDim.x == ntiles)
-      if (!mbar_wait_warp(&accfull[0], 0)) report_error(err, kErrTimeoutMma);
-      tc_fence_after_sync();
-      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(6);
-      const int CW = BN / S;       // token columns owned by each CTA of the cluster
-      const int rstride = CW + 4;  // floats per exchange row (16 bytes of padding against bank conflicts)
-      const uint32_t chunk = (uint32_t)(kBM * rstride * 4);
-      cluster_phase();             // (1) every main loop of the cluster is over: the rings are free
-      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(7);
-      // recv [S][kBM][rstride]: the partials of this CTA's columns, its own written here directly;
-      // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
-      const uint32_t recv = smem_u32(smem);
-      const uint32_t sendb = recv + (uint32_t)S * chunk;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
-#pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + cc, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int col = cc + 4 * g;
-          const int owner = col / CW, cl = col - owner * CW;
-          const uint32_t base = owner == split ? recv + (uint32_t)split * chunk
-                                               : sendb + (uint32_t)(owner < split ? owner : owner - 1) * chunk;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + (uint32_t)((i * rstride + cl) * 4)),
-                       "r"(r[4 * g]), "r"(r[4 * g + 1]), "r"(r[4 * g + 2]), "r"(r[4 * g + 3])
-                       : "memory");
-        }
-      }
-      tc_fence_before_sync();
-      fence_proxy_async_smem();  // the send chunks are read by the bulk copies (async proxy)
-      named_barrier_sync(1, kEpiWarps * 32);
-      // One bulk copy per other owner, into its receive slot `split`: the copy engine moves the
-      // chunks (st.shared::cluster or st.async stores from these 128 threads took 3-10 us for a
-      // 128 x 128 tile).
-      if (threadIdx.x == kEpiWarp0 * 32) {
-        const uint32_t rbar = smem_u32(recvbar);
-        for (int o = 0; o < S; ++o) {
-          if (o == split) continue;
-          bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk, (uint32_t)o),
-                            sendb + (uint32_t)(o < split ? o : o - 1) * chunk, chunk,
-                            map_cluster_addr(rbar, (uint32_t)o));
-        }
-      }
-      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(8);
-      // every other CTA's chunk has landed once the receive barrier completes
-      if (!mbar_wait_warp(recvbar, 0)) report_error(err, kErrTimeoutMma);
-      if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(9);
     }
   }
 
   if (S > 1) {
     // ---------------- split-K: every warp adds the partials of this CTA's columns ----------------
-    if (warp < kEpiWarp0 || warp >= kEpiWarp0 + kEpiWarps) cluster_phase();  // the other warps' part in (1)
+    // the warps that did not drain take their part in (1) here
+    if (warp < kDqWarp0 || warp >= kEpiWarp0 + kEpiWarps) cluster_phase();
     __syncthreads();  // the epilogue warps have seen the receive buffer complete
     grid_dependency_wait();  // y may still be read by the preceding kernel
     const int tile = blockIdx.x;
