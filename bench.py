@@ -367,7 +367,7 @@ def metric_cases(torch, wql, dev, stream, hbm, bf16, l2):
 
         flops = gemm_flops(M, K, N)
         sec = timed(fn, len(stack), 20 if flops * len(stack) < 5e12 else 3)
-        kern = "tcgen05" if wql.w4a16_kernel_for(M, K, N) == "prefill" else "decode"
+        kern = "tcgen05" if wql.w4a16_kernel_for(M, K, N, G) == "prefill" else "decode"
         cases.append(record(cfg, "w4a16_gemm", M, K, N, G, sec, w4a16_bytes(M, K, N, G), flops, {"kernel": kern}))
         del x, y
     packed.clear()
@@ -644,7 +644,7 @@ def run_sweep(args):
         nbytes = w4a16_bytes(M, K, N, G)
         reps = 20 if flops * len(stack) < 5e12 else 3
         sec = timed(fn, len(stack), reps)
-        row = "a3_w4a16_prefill" if wql.w4a16_kernel_for(M, K, N) == "prefill" else "a2_w4a16_decode"
+        row = "a3_w4a16_prefill" if wql.w4a16_kernel_for(M, K, N, G) == "prefill" else "a2_w4a16_decode"
         bound = "tensor" if flops / (bf16 * 1e12) > nbytes / (hbm * 1e9) else "hbm"  # the larger roofline time
         emit(row, f"{fam}:M{M}K{K}N{N}G{G}", sec, nbytes, flops, bound, {"copies": len(stack)})
         del x, y
@@ -787,7 +787,7 @@ def run_sweep(args):
             nbytes = w4a16_bytes(M, K, N, G) - M * N  # y is [M, N / 2]
             bound = "tensor" if flops / (bf16 * 1e12) > nbytes / (hbm * 1e9) else "hbm"
             emit("f3_w4a16_gate_up_silu", f"M{M}K{K}N{N}G{G}", tf, nbytes, flops, bound,
-                 {"plain_gemm_us": round(tp * 1e6, 3), "kernel": wql.w4a16_kernel_for(M, K, N)})
+                 {"plain_gemm_us": round(tp * 1e6, 3), "kernel": wql.w4a16_kernel_for(M, K, N, G)})
             del x, y1, y2
         del stack, qw, s3, qz
 
@@ -974,7 +974,7 @@ def run_trace(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     M, K, N, G = (int(v) for v in args.trace.split(","))
-    kernel = int(lib.wql_w4a16_kernel_for(M, K, N))
+    kernel = int(lib.wql_w4a16_kernel_for(M, K, N, G))
     if kernel not in TRACE_PHASES:
         raise SystemExit(f"no phase trace for kernel {kernel}")
     L = max(4, args.calls)

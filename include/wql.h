@@ -146,12 +146,13 @@ wql_status wql_w4a16_gemm_silu_mul(const uint16_t* x, const uint32_t* qweight, c
                                    void* stream);
 
 /* ----------------------------------------------------------------------------------------
- * w4a16_kernel_for: the kernel wql_w4a16_gemm runs for an M x K x N call on the current
- * device: 0 = the weight-streaming decode kernel, 1 = the tcgen05 tensor-core kernel.  Up to
- * 16 tokens it is always 0 and from 33 on always 1; in between it depends on N and K.
- * Host-only, never fails (the WQL_FORCE_KERNEL benchmarking switch is not consulted).
+ * w4a16_kernel_for: the kernel wql_w4a16_gemm runs for an M x K x N call with group size
+ * `group` on the current device: 0 = the weight-streaming decode kernel, 1 = the tcgen05
+ * tensor-core kernel.  Up to 16 tokens it is always 0 and from 33 on always 1; in between it
+ * depends on N, K and the group size.  Host-only, never fails (the WQL_FORCE_KERNEL
+ * benchmarking switch is not consulted).
  * ---------------------------------------------------------------------------------------- */
-int wql_w4a16_kernel_for(int M, int K, int N);
+int wql_w4a16_kernel_for(int M, int K, int N, int group);
 
 /* ----------------------------------------------------------------------------------------
  * qrmsnorm_quant_i8  [W8A8] QRMSNorm.forward + rms_norm_dynamic_quant / per_token_quant_int8.

@@ -38,11 +38,14 @@ def test_host_only_entry_points(wql_lib):
     assert lib.wql_status_string(4) == b"device-side wait timed out"
     assert lib.wql_w8a8_workspace_bytes(16, 4096, 4096) >= 0
     # kernel choice: decode up to 16 tokens, tcgen05 from 33, in between by shape
-    assert lib.wql_w4a16_kernel_for(1, 4096, 4096) == 0
-    assert lib.wql_w4a16_kernel_for(16, 4096, 22016) == 0
-    assert lib.wql_w4a16_kernel_for(33, 4096, 4096) == 1
-    assert lib.wql_w4a16_kernel_for(32, 11008, 4096) == 1   # long K: split-K pays
-    assert lib.wql_w4a16_kernel_for(32, 4096, 4096) == 0    # 32 output tiles: decode
+    assert lib.wql_w4a16_kernel_for(1, 4096, 4096, 128) == 0
+    assert lib.wql_w4a16_kernel_for(16, 4096, 22016, 32) == 0
+    assert lib.wql_w4a16_kernel_for(33, 4096, 4096, 128) == 1
+    assert lib.wql_w4a16_kernel_for(32, 11008, 4096, 128) == 1   # long K: split-K pays
+    assert lib.wql_w4a16_kernel_for(32, 4096, 4096, 128) == 0    # 32 output tiles: decode
+    assert lib.wql_w4a16_kernel_for(32, 4096, 4096, 32) == 1     # G = 32: four group epilogues per stage
+    assert lib.wql_w4a16_kernel_for(24, 4096, 22016, 64) == 1    # G = 64 beyond one wave
+    assert lib.wql_w4a16_kernel_for(24, 4096, 22016, 128) == 0
     # the phase trace exists only in the developer build; the default library refuses it
     assert lib.wql_trace_setup(None, None, 0, 0, 0) == 2  # WQL_EUNSUPPORTED
     assert b"WQL_PHASE_TRACE" in lib.wql_last_error()

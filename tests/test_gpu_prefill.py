@@ -63,10 +63,12 @@ def test_w4a16_prefill_ragged(wql, monkeypatch, M, K, N, G):
 
 
 @pytest.mark.parametrize("M,K,N,G,kernel", [(24, 4096, 12288, 64, "prefill"), (32, 11008, 4096, 128, "prefill"),
-                                            (32, 4096, 4096, 128, "decode"), (16, 4096, 12288, 32, "decode")])
+                                            (32, 4096, 4096, 128, "decode"), (16, 4096, 12288, 32, "decode"),
+                                            (20, 4096, 4096, 32, "prefill"), (24, 4096, 22016, 64, "prefill"),
+                                            (24, 4096, 22016, 128, "decode")])
 def test_w4a16_default_kernel_choice(wql, M, K, N, G, kernel):
     # between 17 and 32 tokens w4a16_gemm picks the kernel by shape; the default path must be correct
-    assert wql.w4a16_kernel_for(M, K, N) == kernel
+    assert wql.w4a16_kernel_for(M, K, N, G) == kernel
     W = inputs.weight(K, N, seed=6, outliers=True)
     X = inputs.activations(M, K, seed=6, outlier_channels=True)
     qw_r, s_r, qz_r = oracle.awq_quantize(W, G)

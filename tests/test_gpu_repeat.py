@@ -44,7 +44,7 @@ def test_w4a16_prefill_repeatable(wql, M, K, N):
     qw, s, qz = wql.awq_pack(dev(inputs.weight(K, N, seed=N, outliers=True)), G)
     x = dev(inputs.activations(M, K, seed=M, outlier_channels=True))
     y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-    assert wql.w4a16_kernel_for(M, K, N) == "prefill"
+    assert wql.w4a16_kernel_for(M, K, N, G) == "prefill"
     bad = _repeat(lambda: wql.w4a16_gemm(x, qw, s, qz, G, out=y), y)
     assert bad == 0, f"{bad} of {REPS} calls differ"
     assert bool(torch.isfinite(y).all())

@@ -33,7 +33,7 @@ SIGNATURES = {
     "wql_trace_setup": (_I, [_P, _P, ctypes.c_uint64, _I, _I]),
     "wql_awq_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "wql_w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
-    "wql_w4a16_kernel_for": (_I, [_I, _I, _I]),
+    "wql_w4a16_kernel_for": (_I, [_I, _I, _I, _I]),
     "wql_w4a16_gemm_silu_mul": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "wql_qrmsnorm_quant_i8": (_I, [_P, _P, _F, _I, _I, _P, _P, _P]),
     "wql_add_qrmsnorm_quant_i8": (_I, [_P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
@@ -249,9 +249,9 @@ def add_qrmsnorm_quant_i8(x: torch.Tensor, residual: torch.Tensor, gamma: torch.
     return residual_out, q, xs
 
 
-def w4a16_kernel_for(M: int, K: int, N: int) -> str:
-    """The kernel w4a16_gemm runs for this shape: "decode" or "prefill"."""
-    return "prefill" if load().wql_w4a16_kernel_for(M, K, N) else "decode"
+def w4a16_kernel_for(M: int, K: int, N: int, group: int) -> str:
+    """The kernel w4a16_gemm runs for this shape and group size: "decode" or "prefill"."""
+    return "prefill" if load().wql_w4a16_kernel_for(M, K, N, group) else "decode"
 
 
 def w8a8_workspace_bytes(M: int, K: int, N: int) -> int:

@@ -150,7 +150,7 @@ wql_status w4a16_gemm(const char* fn, const uint16_t* x, const uint32_t* qweight
   const char* force = getenv("WQL_FORCE_KERNEL");  // benchmarking switch: "decode" or "prefill"
   const bool prefill = force && strcmp(force, "decode") == 0   ? false
                        : force && strcmp(force, "prefill") == 0 ? true
-                                                                : wql::w4a16_use_prefill(M, K, N);
+                                                                : wql::w4a16_use_prefill(M, K, N, group);
   cudaError_t e = prefill ? wql::launch_w4a16_prefill(x, qweight, scales, qzeros, M, K, N, group, y, act, dev_err,
                                                       static_cast<cudaStream_t>(stream), &err)
                           : wql::launch_w4a16_decode(x, qweight, scales, qzeros, M, K, N, group, y, act, dev_err,
@@ -172,7 +172,7 @@ wql_status wql_w4a16_gemm_silu_mul(const uint16_t* x, const uint32_t* qweight, c
   return w4a16_gemm("wql_w4a16_gemm_silu_mul", x, qweight, scales, qzeros, M, K, N, group, y, 1, stream);
 }
 
-int wql_w4a16_kernel_for(int M, int K, int N) { return wql::w4a16_use_prefill(M, K, N) ? 1 : 0; }
+int wql_w4a16_kernel_for(int M, int K, int N, int group) { return wql::w4a16_use_prefill(M, K, N, group) ? 1 : 0; }
 
 wql_status wql_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
                                  float* xs, void* stream) {

@@ -54,16 +54,21 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
 constexpr int kW4A16PrefillMinM = 33;
 
 // Kernel choice for w4a16_gemm.  Up to 16 tokens the decode kernel streams each weight tile once.
-// From 17 to 32 it runs two 16-token blocks, so every tile is dequantised twice; the tcgen05 kernel
-// (one 32-token tile) is then faster when its output tiles of 128 channels fill most SMs in one
-// wave, or when K is long enough for its split-K (measured on GB300, us, decode vs tcgen05 at
-// M = 32: K = 4096 with N = 4096: 7.8 / 9.3, N = 12288: 22.8 / 18.5, N = 22016: 30.0 / 35.3;
-// K = 11008, N = 4096: 17.8 / 16.4).
-inline bool w4a16_use_prefill(int M, int K, int N) {
+// From 17 to 32 it runs two 16-token blocks, so every tile is dequantised twice, and its per-group
+// epilogue runs once per 128 k at G = 128 but four times at G = 32.  The tcgen05 kernel (one
+// 32-token tile) is then faster when its output tiles of 128 channels fill most SMs in one wave,
+// when K is long enough for its split-K, at G = 32 for every shape, and at G = 64 also beyond one
+// wave (measured on GB300, us, decode vs tcgen05 at M = 32, K = 4096 unless stated):
+//   G = 128: N = 4096 7.8 / 9.3, N = 12288 22.8 / 18.5, N = 22016 27.9 / 31.7, K = 11008 17.8 / 16.4;
+//   G = 64:  N = 4096 7.7 / 9.5, N = 12288 24.9 / 16.4, N = 22016 36.5 / 30.8, K = 11008 17.8 / 15.6;
+//   G = 32:  N = 4096 10.6 / 9.8, N = 12288 31.6 / 17.0, N = 22016 53.4 / 33.4, K = 11008 24.4 / 16.1.
+inline bool w4a16_use_prefill(int M, int K, int N, int group) {
   if (M >= kW4A16PrefillMinM) return true;
   if (M <= 16) return false;
   const int ntn = (N + 127) / 128, sms = num_sms();
-  return K >= 8192 || (2 * ntn >= sms && ntn <= sms);
+  if (K >= 8192 || group == 32) return true;
+  if (2 * ntn < sms) return false;
+  return ntn <= sms || group < 128;
 }
 
 cudaError_t launch_qrmsnorm_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
