@@ -45,7 +45,9 @@ def row_rel_err(y, ref):
                                      # split-K over clusters of 2, 4 and 8 CTAs, with uneven k splits,
                                      # owner column ranges down to 4 tokens, and ragged token tails
                                      (20, 4096, 256, 32), (31, 4160, 2048, 64), (64, 4096, 8192, 128),
-                                     (33, 8192, 1024, 128)])
+                                     (33, 8192, 1024, 128),
+                                     # 192-token tiles: one per CTA, several per CTA, a ragged last tile
+                                     (576, 4096, 4096, 128), (448, 4096, 12288, 64), (500, 4096, 12288, 32)])
 def test_w4a16_prefill_ragged(wql, monkeypatch, M, K, N, G):
     monkeypatch.setenv("WQL_FORCE_KERNEL", "prefill")  # below 33 tokens the choice depends on the shape
     W = inputs.weight(K, N, seed=2, outliers=True)

@@ -84,10 +84,10 @@ def _check(wql, X, packed, qw, s, qz, G, M, N):
     wql.device_status()
 
 
-# decode (M <= 16), the tcgen05 kernel (split-K for few tiles, 128- and 256-token tiles), ragged
+# decode (M <= 16), the tcgen05 kernel (split-K for few tiles, 128-, 192- and 256-token tiles), ragged
 @pytest.mark.parametrize("M,K,N,G", [(1, 4096, 22016, 128), (8, 4096, 22016, 64), (16, 1024, 1024, 32),
                                      (128, 4096, 1024, 128), (300, 4096, 22016, 128), (2048, 4096, 4096, 128),
-                                     (37, 1024, 192, 64)])
+                                     (37, 1024, 192, 64), (560, 4096, 11008, 128)])
 def test_w4a16_silu_mul(wql, M, K, N, G):
     X, packed, qw, s, qz = _case(wql, M, K, N, G, seed=M + N)
     _check(wql, X, packed, qw, s, qz, G, M, N)

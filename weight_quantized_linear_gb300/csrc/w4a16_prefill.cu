@@ -2,7 +2,7 @@
 //
 // y[m, n] = sum_k x[m, k] * (q[k, n] - z[k/G, n]) * s[k/G, n] ("LMDeploy ... INT4 quantisation"
 // tutorial, section 2; section 5.1 names the engine's fp16 x int4 GEMM).  Tiles of 128 output
-// channels x BN tokens (BN = 32, 64, 128 or 256), K walked in blocks of 128, one ring of stages
+// channels x BN tokens (BN = 32, 64, 128, 192 or 256), K walked in blocks of 128, one ring of stages
 // [x tile | packed | s | z]:
 //   * warps 0 and 14, one thread each: TMA copies of the packed weight tile with its scale /
 //     zero-point rows, and of the activation tile (K-major, 128B swizzle);
@@ -12,9 +12,9 @@
 //     activations and the packed weights;
 //   * warp 1: allocates TMEM; one thread issues tcgen05.mma.kind::f16 (M = 128 channels,
 //     N = BN tokens, K = 16, A from TMEM) into an fp32 accumulator and commits stage releases.
-//     BN <= 128: two accumulators, so a tile's epilogue overlaps the next tile's MMAs; BN = 256:
-//     one accumulator (512 TMEM columns hold it and the A slots) and a three-stage ring, the N = 256
-//     MMAs carrying twice the work of the 128-token tile per issued instruction;
+//     BN <= 128: two accumulators, so a tile's epilogue overlaps the next tile's MMAs; BN = 192 and
+//     256: one accumulator (512 TMEM columns hold it and the A slots) and a three-stage ring, the
+//     larger MMAs carrying more work per issued instruction than the 128-token tile's;
 //   * warps 10-13: tcgen05.ld the accumulator (lane = channel, column = token), round to fp16, store.
 // Swapping A and B puts the dequantised weights (not the activations) in the 128-row operand, so
 // the dequantisers write 128 x kBK fp16 per stage whatever the token count.
@@ -58,7 +58,7 @@ constexpr int imin(int a, int b) { return a < b ? a : b; }
 // tiles, one tile per CTA: 4 -> 5 stages).
 template <int BN, int LG, int NACC>
 struct PLayout {
-  static_assert(NACC == 1 || (NACC == 2 && BN <= 128), "the 256-token tile has one accumulator");
+  static_assert(NACC == 1 || (NACC == 2 && BN <= 128), "192- and 256-token tiles have one accumulator");
   static constexpr int G = 1 << LG;
   static constexpr int kGR = G >= kBK ? 1 : kBK / G;
   static constexpr int kXBox = BN * 128;                 // BN token rows x 64 k fp16
@@ -673,6 +673,23 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
   const int ntn = (N + kBM - 1) / kBM;
   int BN = M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   if (BN == 256 && M <= 512 && (ntn * ((M + 127) / 128) <= num_sms() || (M % 256 != 0 && M % 256 <= 128))) BN = 128;
+  // From 257 to 576 tokens, 192-token tiles where they need fewer rounds of CTAs: a round of tiles
+  // costs about 0.62 us per 128-k stage at 192 tokens, against 0.70 at 256 and 0.49 at 128 (0.45
+  // when CTAs walk several 128-token tiles and overlap their epilogues).  Only tile counts that fill
+  // at least half the SMs are compared (fewer go to split-K).  Measured on GB300, K = 4096, us, the
+  // previous choice vs 192: M = 512, N = 11008: 51.4 / 45.6; M = 448, N = 12288: 51.2 / 45.7;
+  // M = 576, N = 4096: 25.3 / 22.6; M = 576, N = 22016: 102.2 / 91.2; and the cases it leaves
+  // alone, e.g. M = 512, N = 4096: 17.9 / 22.6; M = 512, N = 22016: 79.1 / 90.5.
+  if (M > 256 && M <= 576) {
+    const int sms = num_sms();
+    auto tiles = [&](int bn) { return ntn * ((M + bn - 1) / bn); };
+    auto cost = [&](int bn) {
+      const int rounds = (tiles(bn) + sms - 1) / sms;
+      const float per = bn == 128 ? (rounds > 1 ? 0.45f : 0.49f) : (bn == 192 ? 0.62f : 0.70f);
+      return rounds * per;
+    };
+    if (2 * tiles(192) >= sms && cost(192) < cost(BN)) BN = 192;
+  }
   const int GR = group >= kBK ? 1 : kBK / group;
   CUtensorMap tx, tq, ts, tz;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, M, (uint64_t)K * 2, 64, BN,
@@ -689,6 +706,7 @@ cudaError_t launch_w4a16_prefill(const uint16_t* x, const uint32_t* qweight, con
   __half* yh = reinterpret_cast<__half*>(y);
   if (BN == 32) return launch_pa<32>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
   if (BN == 64) return launch_pa<64>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
+  if (BN == 192) return launch_pa<192>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
   if (BN == 128) return launch_pa<128>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
   return launch_pa<256>(group, tx, tq, ts, tz, M, N, K, yh, act, dev_err, stream);
 }
