@@ -538,6 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the warps that did not drain take their part in (1) here
     if (warp < kDqWarp0 || warp >= kEpiWarp0 + kEpiWarps) cluster_phase();
     __syncthreads();  // the epilogue warps have seen the receive buffer complete
+    // (2) no CTA leaves (freeing the shared memory that its bulk copies read, or that receives
+    // another CTA's copies) before every CTA of the cluster has received all of its chunks.  This
+    // CTA's chunks have all landed, so it arrives now and waits only before it exits: the adds
+    // below overlap the slower peers' receives.
+    __syncwarp();
+    cluster_arrive_relaxed();
     grid_dependency_wait();  // y may still be read by the preceding kernel
     const int tile = blockIdx.x;
     const int nt = tile % ntn, mt = tile / ntn;
@@ -580,9 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m + e < M) y[(size_t)(m + e) * N + n] = __float2half_rn(v[e]);
       }
     }
-    // (2) no CTA leaves (freeing the shared memory that its bulk copies read, or that receives
-    // another CTA's copies) before every CTA of the cluster has received all of its chunks
-    cluster_phase();
+    __syncwarp();
+    cluster_wait();  // (2)
   }
   if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(10);
   tc_fence_before_sync();
