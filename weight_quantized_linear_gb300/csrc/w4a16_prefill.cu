@@ -240,11 +240,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
     const uint32_t recv = smem_u32(smem);
     const uint32_t sendb = recv + (uint32_t)S * chunk;
+    // With owner ranges of at most 32 columns, the rows of this warp's lane quarter in each owner's
+    // chunk are written by this warp alone: it sends them as soon as they are staged, one bulk copy
+    // per (lane quarter, owner), so the copies overlap the staging and come from up to twelve
+    // warps.  Wider owner ranges span several warps' chunks: one thread sends whole chunks after a
+    // barrier of the draining warps.
+    const bool per_warp = CW <= 32;
+    const uint32_t rbar = smem_u32(recvbar);
+    const uint32_t qoff = (uint32_t)(32 * quad * rstride * 4), qbytes = (uint32_t)(32 * rstride * 4);
 #pragma unroll 1
-    for (int cc = 32 * rank; ready && cc < BN; cc += 32 * kDrainRanks) {
+    for (int cc = 32 * rank; cc < BN; cc += 32 * kDrainRanks) {
       uint32_t r[32];
-      tmem_ld_32x32b_x32(taddr + cc, r);
-      tmem_ld_wait();
+      if (ready) {
+        tmem_ld_32x32b_x32(taddr + cc, r);
+        tmem_ld_wait();
+      } else {  // the accumulator never became ready (an error is reported): send zeros, so that
+                // the peers' receive barriers still complete
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         const int col = cc + 4 * g;
@@ -255,23 +269,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "r"(r[4 * g]), "r"(r[4 * g + 1]), "r"(r[4 * g + 2]), "r"(r[4 * g + 3])
                      : "memory");
       }
+      if (per_warp) {
+        fence_proxy_async_smem();  // the staged rows are read by the bulk copies (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          for (int o = cc / CW; o <= (cc + 31) / CW; ++o) {
+            if (o == split) continue;
+            bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk + qoff, (uint32_t)o),
+                              sendb + (uint32_t)(o < split ? o : o - 1) * chunk + qoff, qbytes,
+                              map_cluster_addr(rbar, (uint32_t)o));
+          }
+        }
+      }
     }
     tc_fence_before_sync();
-    fence_proxy_async_smem();  // the send chunks are read by the bulk copies (async proxy)
-    named_barrier_sync(1, kDrainWarps * 32);
-    // One bulk copy per other owner, into its receive slot `split`: the copy engine moves the
-    // chunks (st.shared::cluster or st.async stores from the epilogue threads took 3-10 us for a
-    // 128 x 128 tile).
-    if (threadIdx.x == kEpiWarp0 * 32) {
-      const uint32_t rbar = smem_u32(recvbar);
-      for (int o = 0; o < S; ++o) {
-        if (o == split) continue;
-        bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk, (uint32_t)o),
-                          sendb + (uint32_t)(o < split ? o : o - 1) * chunk, chunk,
-                          map_cluster_addr(rbar, (uint32_t)o));
+    if (!per_warp) {
+      fence_proxy_async_smem();  // the send chunks are read by the bulk copies (async proxy)
+      named_barrier_sync(1, kDrainWarps * 32);
+      // One bulk copy per other owner, into its receive slot `split`: the copy engine moves the
+      // chunks (st.shared::cluster or st.async stores from the epilogue threads took 3-10 us for a
+      // 128 x 128 tile).
+      if (threadIdx.x == kEpiWarp0 * 32) {
+        for (int o = 0; o < S; ++o) {
+          if (o == split) continue;
+          bulk_copy_to_peer(map_cluster_addr(recv + (uint32_t)split * chunk, (uint32_t)o),
+                            sendb + (uint32_t)(o < split ? o : o - 1) * chunk, chunk,
+                            map_cluster_addr(rbar, (uint32_t)o));
+        }
       }
-      WQL_STAMP(8);
     }
+    if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(8);
     // every other CTA's chunk has landed once the receive barrier completes
     if (rank == 0) {
       if (!mbar_wait_warp(recvbar, 0)) report_error(err, kErrTimeoutMma);
