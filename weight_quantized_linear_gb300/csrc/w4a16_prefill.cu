@@ -75,10 +75,18 @@ struct PLayout {
   // stage kStages earlier have completed) frees the slot too
   static constexpr int kAccBufs = NACC;
   static constexpr int kMaxBarBytes = (3 * 8 + 6) * 8 + 16;
-  static constexpr int kStages = imin(8, imin((227 * 1024 - 1024 - kMaxBarBytes) / kStage, (512 - NACC * BN) / 64));
+  // 32- and 64-token tiles keep a split-K receive buffer of their own after the barriers, sized for
+  // the largest split (S = 8: kBM x (BN / 8 + 4) fp32 from each of 8 splits), without costing a
+  // ring stage: peers may then send before this CTA's main loop is over.  Larger tiles receive
+  // into their ring once every main loop of the cluster is over.
+  static constexpr bool kOwnRecv = BN <= 64;
+  static constexpr int kRecvBytes = kOwnRecv ? kBM * (BN + 4 * 8) * 4 : 0;
+  static constexpr int kStages =
+      imin(8, imin((227 * 1024 - 1024 - kMaxBarBytes - kRecvBytes) / kStage, (512 - NACC * BN) / 64));
   static constexpr uint32_t kWTx = kWBytes + kSBytes + kZBytes;
   static constexpr int kBarBytes = (3 * kStages + 6) * 8 + 16;
-  static constexpr int kBytes = kStages * kStage + kBarBytes + 1024;
+  static constexpr int kOffRecv = (kStages * kStage + kBarBytes + 127) / 128 * 128;
+  static constexpr int kBytes = kOffRecv + kRecvBytes + 1024;
   static constexpr uint32_t kAColBase = kAccBufs * BN;  // A slots (64 columns = 128 k each) after the accumulators
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kAColBase + 64 * kStages <= kTmemCols, "TMEM budget");
@@ -86,7 +94,10 @@ struct PLayout {
   // receive buffer [source split][channel][BN / S + 4] fp32 and a send buffer with the same chunks
   // for the S - 1 other owners: 2 S - 1 chunks of kBM (BN / S + 4) fp32
   static constexpr int exchange_bytes(int S) { return (2 * S - 1) * kBM * (BN / S + 4) * 4; }
-  static constexpr bool split_fits(int S) { return S == 1 || (BN / S >= 4 && exchange_bytes(S) <= kStages * kStage); }
+  static constexpr bool split_fits(int S) {
+    return S == 1 || (BN / S >= 4 && (kOwnRecv ? S <= 8 && (S - 1) * kBM * (BN / S + 4) * 4 <= kStages * kStage
+                                               : exchange_bytes(S) <= kStages * kStage));
+  }
   static_assert(split_fits(2), "a two-way split must fit");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
@@ -176,6 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // split-K with a receive buffer of its own: cluster phase 0 (arrive now, wait before the first
+  // copy to a peer) guarantees every peer's receive barrier is initialised
+  if (L::kOwnRecv && gridDim.y > 1) cluster_arrive_relaxed();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) WQL_STAMP(1);
   // A grid of at most one tile per CTA leaves SMs free for most of its run: let the next kernel be
@@ -234,12 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int CW = BN / S;       // token columns owned by each CTA of the cluster
     const int rstride = CW + 4;  // floats per exchange row (16 bytes of padding against bank conflicts)
     const uint32_t chunk = (uint32_t)(kBM * rstride * 4);
-    cluster_phase();             // (1) every main loop of the cluster is over: the rings are free
+    if constexpr (L::kOwnRecv)
+      cluster_wait();    // (0) every peer is initialised; its own receive buffer is always free
+    else
+      cluster_phase();   // (1) every main loop of the cluster is over: the rings are free
     if (threadIdx.x == kEpiWarp0 * 32) WQL_STAMP(7);
     // recv [S][kBM][rstride]: the partials of this CTA's columns, its own written here directly;
-    // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns
-    const uint32_t recv = smem_u32(smem);
-    const uint32_t sendb = recv + (uint32_t)S * chunk;
+    // sendb [S - 1][kBM][rstride]: this CTA's partials of the other owners' columns (in the ring,
+    // which this CTA's own main loop no longer uses)
+    const uint32_t recv = L::kOwnRecv ? smem_u32(smem + L::kOffRecv) : smem_u32(smem);
+    const uint32_t sendb = L::kOwnRecv ? smem_u32(smem) : recv + (uint32_t)S * chunk;
     // With owner ranges of at most 32 columns, the rows of this warp's lane quarter in each owner's
     // chunk are written by this warp alone: it sends them as soon as they are staged, one bulk copy
     // per (lane quarter, owner), so the copies overlap the staging and come from up to twelve
@@ -563,7 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (S > 1) {
     // ---------------- split-K: every warp adds the partials of this CTA's columns ----------------
     // the warps that did not drain take their part in (1) here
-    if (warp < kDqWarp0 || warp >= kEpiWarp0 + kEpiWarps) cluster_phase();
+    if (warp < kDqWarp0 || warp >= kEpiWarp0 + kEpiWarps) {
+      if constexpr (L::kOwnRecv)
+        cluster_wait();  // (0)
+      else
+        cluster_phase();  // (1)
+    }
     __syncthreads();  // the epilogue warps have seen the receive buffer complete
     // (2) no CTA leaves (freeing the shared memory that its bulk copies read, or that receives
     // another CTA's copies) before every CTA of the cluster has received all of its chunks.  This
@@ -575,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = blockIdx.x;
     const int nt = tile % ntn, mt = tile / ntn;
     const int CW = BN / S, rstride = CW + 4;
-    const uint32_t recv = smem_u32(smem);
+    const uint32_t recv = L::kOwnRecv ? smem_u32(smem + L::kOffRecv) : smem_u32(smem);
     const int NO = act ? N / 2 : N;
     // Item j: TMEM lane i = j % kBM (a channel), tokens [4 c, 4 c + 4) of this CTA's columns with
     // c = j / kBM.  The 32 lanes of a warp take 32 consecutive TMEM lanes (kThreads and kBM are
