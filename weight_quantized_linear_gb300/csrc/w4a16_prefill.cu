@@ -23,10 +23,10 @@
 //   * persistent (gridDim.y == 1): one CTA per SM walks the tiles;
 //   * split-K (gridDim.y == S in {2, 4, 8}, clusters of S CTAs along y): when the tiles are fewer
 //     than half the SMs, the S CTAs of a cluster each take 1/S of K for one tile.  After their
-//     main loops they exchange partial sums through distributed shared memory (the stage ring is
-//     reused for the exchange buffers; one bulk copy per peer): CTA r owns token columns
-//     [r BN/S, (r+1) BN/S) and every warp then adds the S partials in split order, so the result
-//     does not depend on timing.
+//     main loops they exchange partial sums through distributed shared memory by bulk copies
+//     (send buffers in the stage ring; receive buffers in the ring, or in shared memory of their
+//     own for 32- and 64-token tiles): CTA r owns token columns [r BN/S, (r+1) BN/S) and every
+//     warp then adds the S partials in split order, so the result does not depend on timing.
 // Launched with programmatic dependent launch: the packed weights of the first stages are
 // requested before waiting for the preceding kernel, whose output may be x.
 #include <atomic>
