@@ -66,7 +66,7 @@ extern "C" {
 typedef enum wql_status {
   WQL_OK = 0,
   WQL_EINVAL = 1,        /* bad argument: shape, alignment, null pointer, group size */
-  WQL_EUNSUPPORTED = 2,  /* valid request this build does not cover (e.g. K too large) */
+  WQL_EUNSUPPORTED = 2,  /* valid request the library does not cover (e.g. K too large) */
   WQL_ECUDA = 3,         /* CUDA runtime/driver error at launch */
   WQL_ETIMEOUT = 4       /* a kernel's bounded on-chip wait expired (see wql_device_status) */
 } wql_status;

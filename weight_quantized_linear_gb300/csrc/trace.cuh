@@ -25,8 +25,8 @@ struct TraceDesc {
 };
 
 #ifdef WQL_PHASE_TRACE
-// One copy per translation unit (no relocatable device code in this build): each traced source
-// file registers the descriptor with its own trace_set_local().
+// One copy per translation unit (the library is compiled without relocatable device code):
+// each traced source file registers the descriptor with its own trace_set_local().
 static __device__ TraceDesc g_trace_desc;
 
 __device__ __forceinline__ unsigned long long* trace_row(const void* y) {
