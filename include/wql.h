@@ -205,7 +205,8 @@ wql_status wql_per_token_quant_fp8(const uint16_t* x, int M, int K, uint8_t* q, 
  * contiguous, as a torch Linear weight) with per-channel scales ws [N] fp32.
  * y [M, N] fp16 is written in full; acc_out [M, N] int32 is written too when non-NULL.
  * The int32 result is exact for every input (|acc| < 2^31 holds for K <= 131072).
- * workspace: device scratch of at least wql_w8a8_workspace_bytes(M, K, N) bytes, used only
+ * workspace: device scratch of at least wql_w8a8_workspace_bytes(M, K, N) bytes (M * K * 2 +
+ * 16384 for M >= 17: an fp16 copy of q and the largest row L1 norms of q; 0 below), used only
  * during the call (may be NULL when that size is 0).
  * Requires K % 16 == 0, N % 32 == 0, M >= 0, K <= 131072.
  * ---------------------------------------------------------------------------------------- */
@@ -235,7 +236,7 @@ wql_status wql_w8a8_gemm_fused(const int8_t* q, const float* xs, const int8_t* q
  * or a latency-critical loop that must not pay for the allocator's synchronisation.  The source
  * pages have no counterpart to this entry point; it exists for such callers only.
  * Instead of a caller workspace it uses a scratch array built into the library:
- *   - 32 MiB, so M * K * 2 <= 33554432 (e.g. M = K = 4096); larger calls return
+ *   - 32 MiB + 64 KiB, so M * K * 2 + 16384 <= 33619968 (e.g. M = K = 4096); larger calls return
  *     WQL_EUNSUPPORTED with a message in wql_last_error() and launch nothing;
  *   - one array per GPU that loads the library, held until the process exits;
  *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress,

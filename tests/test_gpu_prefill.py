@@ -121,6 +121,33 @@ def test_w8a8_prefill_exact_beyond_fp32_integer_range(wql, K):
     wql.device_status()
 
 
+@pytest.mark.parametrize("over", [False, True])
+def test_w8a8_prefill_one_chunk_bound(wql, over):
+    # One fp32 accumulator takes the whole of K when 128 x every row's L1 norm stays within 2^24.
+    # At the bound (every |q| = 32, K = 4096: L1 = 2^17) against weights of -128 the partial sums
+    # reach exactly 2^24 in magnitude; one code more in one row (over) switches the launch to
+    # 1024-k chunks.  Both must be bit-exact.
+    M, K, N = 64, 4096, 256
+    q = np.full((M, K), 32, np.int8)
+    q[1::2] = -32
+    if over:
+        q[5, 0] = 33
+    qW = np.full((N, K), -128, np.int8)
+    qW[1::2, ::2] = 127
+    xs = np.full((M,), 0.01, np.float32)
+    ws = np.full((N,), 0.001, np.float32)
+    acc = Guarded((M, N), torch.int32)
+    y = Guarded((M, N), torch.float16)
+    wql.w8a8_gemm(dev(q), dev(xs), dev(qW), dev(ws), out=y.t, acc_out=acc.t)
+    acc.check()
+    y.check()
+    ref = oracle.w8a8_acc(q, qW)
+    assert np.abs(ref.astype(np.int64)).max() >= 2 ** 24
+    assert np.array_equal(host(acc.t), ref)
+    assert np.array_equal(host(y.t).view(np.uint16), oracle.w8a8_epilogue(ref, xs, ws).view(np.uint16))
+    wql.device_status()
+
+
 def test_w8a8_smoothquant_block_full_size_sampled(wql):
     # the W8A8 block at a full prefill size: prep chain on the GPU, GEMM through the tcgen05 path
     M, K, N = 4096, 4096, 11008

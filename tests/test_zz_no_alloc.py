@@ -69,12 +69,12 @@ def test_noalloc_decode_shape_needs_no_scratch(wql):
 
 
 def test_noalloc_rejects_calls_beyond_the_static_scratch(wql):
-    # M * K * 2 = 33562624 bytes > 32 MiB: rejected before anything is launched
-    q = torch.zeros((4097, 4096), dtype=torch.int8, device="cuda")
-    xs = torch.ones((4097,), dtype=torch.float32, device="cuda")
+    # M * K * 2 + 16384 = 34422784 bytes > 32 MiB + 64 KiB: rejected before anything is launched
+    q = torch.zeros((4200, 4096), dtype=torch.int8, device="cuda")
+    xs = torch.ones((4200,), dtype=torch.float32, device="cuda")
     qw = torch.zeros((64, 4096), dtype=torch.int8, device="cuda")
     ws = torch.ones((64,), dtype=torch.float32, device="cuda")
-    y = torch.empty((4097, 64), dtype=torch.float16, device="cuda")
+    y = torch.empty((4200, 64), dtype=torch.float16, device="cuda")
     with pytest.raises(wql.WQLError) as ei:
         wql.w8a8_gemm_noalloc(q, xs, qw, ws, out=y)
     assert ei.value.status == 2

@@ -16,9 +16,10 @@
 
 namespace {
 
-// Fixed scratch for the fp16 copy of the activation codes: 32 MiB, i.e. M * K <= 16 Mi elements
-// (M = K = 4096).  It exists once per GPU that loads the library and lives until the process exits.
-constexpr size_t kScratchBytes = size_t(32) << 20;
+// Fixed scratch for the fp16 copy of the activation codes and their row-norm maxima: 32 MiB +
+// 64 KiB, i.e. M * K * 2 + 16384 bytes up to M = K = 4096.  It exists once per GPU that loads the library
+// and lives until the process exits.
+constexpr size_t kScratchBytes = (size_t(32) << 20) + (size_t(64) << 10);
 static __device__ __align__(256) unsigned char g_w8a8_scratch[kScratchBytes];
 
 // The array's device address, looked up once per device (with that device current).  Host code must
@@ -54,7 +55,7 @@ wql_status wql_w8a8_gemm_noalloc(const int8_t* q, const float* xs, const int8_t*
   const size_t need = (M > 0 && K > 0 && N > 0) ? wql_w8a8_workspace_bytes(M, K, N) : 0;
   if (need > kScratchBytes) {
     wql::set_last_error("wql_w8a8_gemm_noalloc: this call needs " + std::to_string(need) +
-                        " bytes of scratch (M * K * 2) but the static scratch holds " + std::to_string(kScratchBytes) +
+                        " bytes of scratch (M * K * 2 + 16384) but the static scratch holds " + std::to_string(kScratchBytes) +
                         " bytes; use wql_w8a8_gemm with a caller-provided workspace");
     return WQL_EUNSUPPORTED;
   }

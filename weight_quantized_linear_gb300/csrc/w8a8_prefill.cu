@@ -12,12 +12,16 @@
 //     weight rows are K-contiguous, so its 64 codes are four 16-byte shared-memory loads (the tile
 //     arrives with a 128-byte swizzle, which spreads a warp's rows over all banks).  Keeping the
 //     fp16 operand out of shared memory removes two thirds of the shared-memory traffic per stage;
-//   * exactness: |product| <= 128 * 128 = 2^14 (both codes may be -128) and each accumulator covers
-//     at most 1024 k, so every partial sum is an integer of magnitude <= 2^24 that fp32 holds
-//     exactly.  The MMA thread
-//     alternates two TMEM chunk accumulators; the epilogue warps turn each finished chunk into
+//   * exactness: |product| <= 128 * 128 = 2^14 (both codes may be -128), so any partial sum of row
+//     m is an integer of magnitude <= 128 * sum_k |q[m, k]|.  When that bound stays within 2^24 for
+//     every row (the conversion pre-pass records the largest row L1 norm of each of its blocks;
+//     typical per-token codes at K = 4096 stay near 2^16), one fp32 accumulator takes the whole of
+//     K exactly, and the TMEM
+//     the chunk scheme needs holds more A slots instead (4 against 2 at 128 tokens).  Otherwise each
+//     accumulator covers at most 1024 k, which bounds every partial sum by 2^24: the MMA thread
+//     alternates two TMEM chunk accumulators, and the epilogue warps turn each finished chunk into
 //     int32 and add it to an int32 running sum kept in TMEM, so the MMAs never wait for them.
-//     The tile's last chunk yields acc (written to acc_out if requested) and
+//     Either way the tile yields the exact acc (written to acc_out if requested) and
 //     y = fp16((float(acc) * xs[m]) * ws[n]);
 //   * each epilogue warp owns 32 channels and writes y in 32-token boxes staged through shared memory
 //     and stored by TMA; a fused residual arrives the same way: TMA loads all of the tile's residual
@@ -36,6 +40,8 @@ namespace {
 constexpr int kBK = 128;        // k per stage (bytes of a weight row): 8 MMAs per barrier round trip
 constexpr int kBM = 128;        // output channels per tile (MMA M)
 constexpr int kChunkKB = 8;     // stages per exact chunk: 8 x 128 = 1024 k
+constexpr int kOneChunkL1 = (1 << 24) / 128;  // largest row L1 norm for which one chunk is exact
+constexpr int kPrepassMaxBlocks = 4096;        // the pre-pass writes one row-norm maximum per block
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kCvWarp0 = 2, kCvWarps = 8, kEpiWarp0 = 10, kEpiWarps = 4;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 
@@ -51,14 +57,18 @@ struct QLayout {
   // TMEM columns: [0, BN) and [BN, 2 BN) chunk accumulators, [2 BN, 3 BN) int32 running sum, then
   // the fp16 A operand: kASlots slots of 64 columns (128 k) each
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kAColBase = 3 * BN;
-  static constexpr int kASlots = BN >= 128 ? 2 : 4;
-  static_assert(kAColBase + 64 * kASlots <= kTmemCols, "TMEM budget");
+  // chunked mode: [2 BN, 3 BN) int32 running sum, then kChunkSlots A slots; one-chunk mode:
+  // kOneSlots A slots from 2 BN
+  static constexpr uint32_t kSumCol = 2 * BN;
+  static constexpr int kChunkSlots = BN >= 128 ? 2 : 4;
+  static constexpr int kOneSlots = (kTmemCols - 2 * BN) / 64;
+  static constexpr int kASlots = kOneSlots;  // the larger ring (barrier count)
+  static_assert(3 * BN + 64 * kChunkSlots <= kTmemCols && 2 * BN + 64 * kOneSlots <= kTmemCols, "TMEM budget");
   static constexpr int kBox = 32 * 32 * 2;  // one 32 tokens x 32 channels fp16 output box
   static constexpr int kBufs = 4;           // output boxes per epilogue warp: a whole tile's
   static constexpr int kOffOut = kStages * kStage;  // [epilogue warp][kBufs] boxes
   static constexpr int kOffBar = kOffOut + kEpiWarps * kBufs * kBox;
-  static constexpr int kBarBytes = (2 * kStages + kASlots + 5 + kBufs * kEpiWarps) * 8 + 16;
+  static constexpr int kBarBytes = (2 * kStages + kASlots + 6 + kBufs * kEpiWarps) * 8 + 16;
   static constexpr int kBytes = kOffBar + kBarBytes + 1024;
   // a converter waits for the stage release of block i - kASlots before reusing its A slot: that
   // barrier is then never a phase ahead
@@ -70,20 +80,43 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// int8 [n] -> fp16 [n], exact; n a multiple of 16, both pointers 16-byte aligned.
-__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ q, __half* __restrict__ out,
-                                                        long long n16) {
-  const uint4* src = reinterpret_cast<const uint4*>(q);
-  uint4* dst = reinterpret_cast<uint4*>(out);
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
-    const uint4 v = __ldg(src + i);
-    uint4 a, b;
-    i8x4_to_f16x2x2(v.x, a.x, a.y);
-    i8x4_to_f16x2x2(v.y, a.z, a.w);
-    i8x4_to_f16x2x2(v.z, b.x, b.y);
-    i8x4_to_f16x2x2(v.w, b.z, b.w);
-    dst[2 * i] = a;
-    dst[2 * i + 1] = b;
+// int8 codes [M][K] -> exact fp16 [M][K], and per block the largest row L1 norm sum_k |q| among its
+// rows (which decides whether one fp32 accumulator takes the whole of K exactly).  One warp per row,
+// 16 codes per lane and step; K a multiple of 16 and both pointers 16-byte aligned.
+__global__ void __launch_bounds__(256) i8_to_f16_rows_kernel(const int8_t* __restrict__ q, __half* __restrict__ out,
+                                                             int* __restrict__ blockmax, int M, int K) {
+  __shared__ int wmax[8];
+  const int lane = threadIdx.x & 31;
+  const int k16 = K / 16;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  unsigned rmax = 0;
+  for (long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M; row += nwarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(q + row * K);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * K);
+    unsigned l1 = 0;
+    for (int i = lane; i < k16; i += 32) {
+      const uint4 v = __ldg(src + i);
+      uint4 a, b;
+      i8x4_to_f16x2x2(v.x, a.x, a.y);
+      i8x4_to_f16x2x2(v.y, a.z, a.w);
+      i8x4_to_f16x2x2(v.z, b.x, b.y);
+      i8x4_to_f16x2x2(v.w, b.z, b.w);
+      dst[2 * i] = a;
+      dst[2 * i + 1] = b;
+      // per-byte |q| (0x80, i.e. -128, reads as the unsigned byte 128), summed by byte
+      l1 += __vsadu4(__vabs4(v.x), 0u) + __vsadu4(__vabs4(v.y), 0u) + __vsadu4(__vabs4(v.z), 0u) +
+            __vsadu4(__vabs4(v.w), 0u);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    rmax = l1 > rmax ? l1 : rmax;
+  }
+  if (lane == 0) wmax[threadIdx.x >> 5] = (int)rmax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int b = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) b = wmax[w] > b ? wmax[w] : b;
+    blockmax[blockIdx.x] = b;
   }
 }
 
@@ -94,7 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float* __restrict__ xs, const float* __restrict__ ws, int M, int N, int K,
                         const __grid_constant__ CUtensorMap tm_y,  // y fp16 [M][N], box {32, 32}
                         const __grid_constant__ CUtensorMap tm_r,  // residual fp16 [M][N], box {32, 32}
-                        int32_t* __restrict__ acc_out, EpilogueAdd ea, unsigned* err) {
+                        int32_t* __restrict__ acc_out, EpilogueAdd ea,
+                        const int* __restrict__ blockmax,  // [nbm] largest row L1 norms of q (pre-pass)
+                        int nbm, unsigned* err) {
   using L = QLayout<BN>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -105,8 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accfull = afull + L::kASlots;  // [2] chunk accumulators
   uint64_t* accempty = accfull + 2;     // [2]
   uint64_t* finalbar = accempty + 2;
-  uint64_t* rfull = finalbar + 1;       // [epilogue warp][kBufs] residual box landed
+  uint64_t* modebar = finalbar + 1;     // the accumulation mode is known
+  uint64_t* rfull = modebar + 1;        // [epilogue warp][kBufs] residual box landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + L::kBufs * kEpiWarps);
+  int* mode_smem = reinterpret_cast<int*>(tmem_slot + 1);  // [0] max row L1 norm, [1] one-chunk mode
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntn = (N + kBM - 1) / kBM;
@@ -126,6 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accempty[b], kEpiWarps);
     }
     mbar_init(finalbar, 1);
+    mbar_init(modebar, 1);
+    mode_smem[0] = 0;
     for (int i = 0; i < L::kBufs * kEpiWarps; ++i) mbar_init(&rfull[i], 1);
     fence_mbarrier_init();
   }
@@ -178,9 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16(kBM, BN, /*A K-major*/ 0, /*B K-major*/ 0);
       int stage = 0, phase = 0, aslot = 0, aph = 0, cseq = 0;  // cseq counts chunks over all tiles
-      bool ok = true;
+      bool ok = mbar_wait_bounded(modebar, 0);
+      if (!ok) report_error(err, kErrTimeoutMma);
+      const bool one = ok && mode_smem[1] != 0;
+      const int chunk_kb = one ? nkb : kChunkKB, nch = one ? 1 : nchunks;
+      const int nslots = one ? L::kOneSlots : L::kChunkSlots;
+      const uint32_t abase = one ? L::kSumCol : L::kSumCol + BN;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        for (int c = 0; c < nchunks && ok; ++c, ++cseq) {
+        for (int c = 0; c < nch && ok; ++c, ++cseq) {
           const int b = cseq & 1;
           if (!mbar_wait_bounded(&accempty[b], ((cseq >> 1) & 1) ^ 1)) {
             report_error(err, kErrTimeoutMma);
@@ -189,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + b * BN;
-          const int kb1 = (c + 1) * kChunkKB < nkb ? (c + 1) * kChunkKB : nkb;
-          for (int kb = c * kChunkKB; kb < kb1; ++kb) {
+          const int kb1 = (c + 1) * chunk_kb < nkb ? (c + 1) * chunk_kb : nkb;
+          for (int kb = c * chunk_kb; kb < kb1; ++kb) {
             // The converters wait for the stage's copies before they arrive on afull, so this wait
             // also orders the x tile (one wait per stage instead of two: 372 -> 354 us at M = 4096,
             // N = 11008)
@@ -201,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t xs_s = smem_u32(smem + stage * L::kStage);
-            const uint32_t a_tmem = tmem_base + L::kAColBase + aslot * 64;
+            const uint32_t a_tmem = tmem_base + abase + aslot * 64;
             // the stage's B descriptors differ only in the start address field (bits 0-13, addr >> 4;
             // shared-memory addresses stay below 2^18, so adding to it never carries)
             const uint64_t bdesc0 = umma_sdesc_sw128(xs_s, 16, 1024);
@@ -209,14 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kBK / 16; ++s) {
               // k16 step s: x box s / 4, 32 bytes per step along its 128-byte rows
               const uint64_t bdesc = bdesc0 + (uint64_t)(((s >> 2) * L::kXBox + (s & 3) * 32) >> 4);
-              umma_f16_ta(d_tmem, a_tmem + s * 8, bdesc, idesc, (kb > c * kChunkKB || s > 0) ? 1u : 0u);
+              umma_f16_ta(d_tmem, a_tmem + s * 8, bdesc, idesc, (kb > c * chunk_kb || s > 0) ? 1u : 0u);
             }
             umma_commit(&empty[stage]);  // the stage and this block's A slot are free again
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
             }
-            if (++aslot == L::kASlots) {
+            if (++aslot == nslots) {
               aslot = 0;
               aph ^= 1;
             }
@@ -234,13 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kCvWarp0) >> 2;  // k half of the tile: bytes [64 half, 64 half + 64)
     const int row = quad * 32 + lane;         // output channel within the tile = TMEM lane
     const int sw = row & 7;                   // 128-byte swizzle: 16-byte chunk c sits at c ^ sw
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + L::kAColBase + 32 * half;
     int stage = 0, phase = 0, aslot = 0, kbi = 0;
-    bool ok = true;
+    bool ok = mbar_wait_warp(modebar, 0);
+    if (!ok) report_error(err, kErrTimeoutFull);
+    const bool one = ok && mode_smem[1] != 0;
+    const int nslots = one ? L::kOneSlots : L::kChunkSlots;
+    const uint32_t lane_addr =
+        tmem_base + ((uint32_t)(quad * 32) << 16) + (one ? L::kSumCol : L::kSumCol + BN) + 32 * half;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb, ++kbi) {
-        // the A slot was last used by block kbi - kASlots: wait until its MMAs have completed
-        const int prev = kbi - L::kASlots;
+        // the A slot was last used by block kbi - nslots: wait until its MMAs have completed
+        const int prev = kbi - nslots;
         const bool okf = mbar_wait_warp(&full[stage], phase);
         const bool oke = prev < 0 || mbar_wait_warp(&empty[prev % kStages], (prev / kStages) & 1);
         if (!okf || !oke) {
@@ -270,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage = 0;
           phase ^= 1;
         }
-        if (++aslot == L::kASlots) aslot = 0;
+        if (++aslot == nslots) aslot = 0;
       }
     }
   } else {
@@ -278,7 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - kEpiWarp0;
     const int quad = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    const uint32_t sum_col = 2 * BN;
+    const uint32_t sum_col = L::kSumCol;
+    // The accumulation mode, for the whole launch: one exact chunk when 128 x every row's L1 norm
+    // stays within 2^24.  These warps reduce the pre-pass blocks' maxima and publish the mode
+    // (modebar) to the MMA thread and the converters, which wait for it before their first stage.
+    int mx = 0;
+    if (blockmax)
+      for (int b = (warp - kEpiWarp0) * 32 + lane; b < nbm; b += kEpiWarps * 32) mx = max(mx, __ldg(blockmax + b));
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) atomicMax(&mode_smem[0], mx);
+    named_barrier_sync(1, kEpiWarps * 32);
+    const bool one = blockmax != nullptr && mode_smem[0] <= kOneChunkL1;
+    if (warp == kEpiWarp0 && lane == 0) {
+      mode_smem[1] = one ? 1 : 0;
+      mbar_arrive(modebar);
+    }
+    const int nch = one ? 1 : nchunks;
     BoxStage<L::kBufs> out;
     out.init(reinterpret_cast<__half*>(smem + L::kOffOut + ew * L::kBufs * L::kBox), rfull + ew * L::kBufs, &tm_y,
              &tm_r, ea.residual != nullptr);
@@ -289,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = nt * kBM + quad * 32, n = n0 + lane;
       const float wn = n < N ? ws[n] : 0.f;
       const float bn = (ea.bias && n < N) ? __half2float(ea.bias[n]) : 0.f;
-      for (int c = 0; c < nchunks && ok; ++c, ++cseq) {
+      for (int c = 0; c < nch && ok; ++c, ++cseq) {
         const int b = cseq & 1;
-        const bool first = c == 0, last = c == nchunks - 1;
+        const bool first = c == 0, last = c == nch - 1;
         if (last) out.begin(n0, mt * BN, BN / 32, lane);  // residual boxes land while the last chunk's MMAs run
         if (!mbar_wait_warp(&accfull[b], (cseq >> 1) & 1)) {
           report_error(err, kErrTimeoutMma);
@@ -351,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN>
 cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const CUtensorMap& tr,
                      const float* xs, const float* ws, int M, int N, int K, int32_t* acc_out, EpilogueAdd ea,
-                     unsigned* dev_err, cudaStream_t stream) {
+                     const int* blockmax, int nbm, unsigned* dev_err, cudaStream_t stream) {
   using L = QLayout<BN>;
   auto kern = w8a8_prefill_kernel<BN>;
   static std::atomic<bool> attr_set[64];  // per device; racing first calls set the same attribute
@@ -364,24 +427,27 @@ cudaError_t launch_q(const CUtensorMap& tx, const CUtensorMap& tw, const CUtenso
   }
   const int ntiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, ty, tr, acc_out, ea, dev_err);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tx, tw, xs, ws, M, N, K, ty, tr, acc_out, ea, blockmax, nbm, dev_err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t w8a8_prefill_workspace_bytes(int M, int K) { return (size_t)M * (size_t)K * 2; }
+// [M][K] fp16 copy of the codes, then the pre-pass blocks' largest row L1 norms (int32)
+size_t w8a8_prefill_workspace_bytes(int M, int K) { return (size_t)M * (size_t)K * 2 + kPrepassMaxBlocks * 4; }
 
 cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* qw, const float* ws, int M, int K,
                                 int N, uint16_t* y, int32_t* acc_out, const uint16_t* bias, const uint16_t* residual,
                                 void* workspace, unsigned* dev_err, cudaStream_t stream, std::string* err) {
   const EpilogueAdd ea{reinterpret_cast<const __half*>(bias), reinterpret_cast<const __half*>(residual)};
-  // 1. activation codes -> exact fp16 in the workspace
+  // 1. activation codes -> exact fp16 in the workspace, and the blocks' largest row L1 norms after them
   __half* xh = reinterpret_cast<__half*>(workspace);
-  const long long n16 = (long long)M * K / 16;
-  const long long blocks = (n16 + 255) / 256;
-  const int grid = (int)(blocks < 4L * num_sms() ? blocks : 4L * num_sms());
-  i8_to_f16_kernel<<<grid, 256, 0, stream>>>(q, xh, n16);
+  int* blockmax = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + (size_t)M * K * 2);
+  long long blocks = ((long long)M + 7) / 8;  // eight rows (warps) per block
+  if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
+  if (blocks > kPrepassMaxBlocks) blocks = kPrepassMaxBlocks;
+  const int grid = (int)blocks;
+  i8_to_f16_rows_kernel<<<grid, 256, 0, stream>>>(q, xh, blockmax, M, K);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. the GEMM
@@ -398,8 +464,8 @@ cudaError_t launch_w8a8_prefill(const int8_t* q, const float* xs, const int8_t* 
     return cudaErrorInvalidValue;
   }
   if (!residual) tr = ty;  // not read
-  if (BN == 64) return launch_q<64>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
-  return launch_q<128>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, dev_err, stream);
+  if (BN == 64) return launch_q<64>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, blockmax, grid, dev_err, stream);
+  return launch_q<128>(tx, tw, ty, tr, xs, ws, M, N, K, acc_out, ea, blockmax, grid, dev_err, stream);
 }
 
 }  // namespace wql
