@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(256) i8_to_f16_rows_kernel(const int8_t* __res
     const uint4* src = reinterpret_cast<const uint4*>(q + row * K);
     uint4* dst = reinterpret_cast<uint4*>(out + row * K);
     unsigned l1 = 0;
-    for (int i = lane; i < k16; i += 32) {
+#pragma unroll 4
+    for (int i = lane; i < k16; i += 32) {  // unrolled: several 16-byte loads in flight per lane
       const uint4 v = __ldg(src + i);
       uint4 a, b;
       i8x4_to_f16x2x2(v.x, a.x, a.y);
