@@ -126,3 +126,17 @@ def test_header_is_plain_c99(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src),
                         "-o", str(tmp_path / "use_wql.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_phase_trace_build_compiles_and_exports_its_setup():
+    # The developer build with the W4A16 kernels' phase stamps (-DWQL_PHASE_TRACE) is compiled only
+    # on demand (bench.py --trace): check here that it still builds and exports the same C ABI.
+    # Registering a buffer needs a GPU; without one the call fails with a CUDA error, not EUNSUPPORTED.
+    from weight_quantized_linear_gb300 import build, _lib
+    path = build.build(trace=True)
+    lib = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    lib.wql_trace_setup.restype = ctypes.c_int
+    lib.wql_trace_setup.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+    assert lib.wql_trace_setup(None, None, 0, 0, 0) != _lib.WQL_EUNSUPPORTED
